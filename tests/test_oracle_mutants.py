@@ -1,0 +1,66 @@
+"""The pins have teeth: each build of the oracle with one planted mistake (a
+swapped boundary, a wrong sign, a dropped term, a wrong identity, a
+transposed comparison or index, a wrong rounding rule) must fail at least one
+pin. The mistakes are planted in a temporary copy of the oracle's C source on
+the CPU; the real oracle is untouched."""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mt_oracle.c")
+
+MUTANTS = {
+    "incl_excl_swapped": ("const double y = inclusive ? lp_next : lp;",
+                          "const double y = inclusive ? lp : lp_next;"),
+    "row_wrong_sign": ("const double lp_next = lp + x;", "const double lp_next = lp - x;"),
+    "row_transposed_index": ("const int64_t k = r * n + i;", "const int64_t k = r + i * rows;"),
+    "i32_dropped_first_term": ("lp += (uint32_t)x[i];", "if (i) lp += (uint32_t)x[i];"),
+    "i32_wrong_max_identity": ("int32_t lp = (op == OR_MIN) ? INT32_MAX : INT32_MIN;",
+                               "int32_t lp = (op == OR_MIN) ? INT32_MAX : 0;"),
+    "f32_min_max_transposed": ("float lp = (op == OR_MIN) ? INFINITY : -INFINITY;",
+                               "float lp = (op == OR_MIN) ? -INFINITY : INFINITY;"),
+    "f32_add_not_accumulated": ("lp += (double)x[i];", "lp = (double)x[i];"),
+    "ties_away_from_zero": ("double r = nearbyint(q);", "double r = floor(q + 0.5);"),
+    "subnormal_scale_off_by_one": ("v = ldexp((double)m, 1 - bias - f.frac_bits);",
+                                   "v = ldexp((double)m, -bias - f.frac_bits);"),
+    "f32_store_perturbed": ("float f = (float)v;", "float f = (float)(v * (1.0 + 1e-7));"),
+    "select_skips_first": ("if (flags[i] == 1) {", "if (flags[i] == 1 && i > 0) {"),
+}
+
+
+def _build_mutant(name, tmpdir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    src = src.replace(old, new, 1)
+    c = os.path.join(tmpdir, f"{name}.c")
+    so = os.path.join(tmpdir, f"{name}.so")
+    with open(c, "w") as f:
+        f.write(src)
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-std=c11", "-shared", "-fPIC",
+                           "-o", so, c, "-lm"])
+    return so
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    oracle.lib()  # bind the real one first so argtypes setup is exercised
+    with tempfile.TemporaryDirectory() as d:
+        so = _build_mutant(name, d)
+        monkeypatch.setattr(oracle, "_LIB", so)
+        monkeypatch.setattr(oracle, "_SRC", so)  # mtime check: never rebuild over it
+        monkeypatch.setattr(oracle, "_lib", None)
+        failed = []
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin()
+            except AssertionError:
+                failed.append(pin.__name__)
+        monkeypatch.setattr(oracle, "_lib", None)
+    assert failed, f"no pin caught the planted mistake {name}"
