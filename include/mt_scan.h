@@ -1,0 +1,178 @@
+/*
+ * mt_scan.h -- C ABI of libmtscan.so, a prefix-scan library for one NVIDIA
+ * GB300 GPU (sm_103a).
+ *
+ * All calls take plain pointers and sizes. Device pointers are CUDA device
+ * (or managed) memory owned by the caller. `stream` is a cudaStream_t passed
+ * as `void*`; NULL means the legacy default stream. Every call only enqueues
+ * work on `stream` and returns without synchronising, except
+ * mt_scan_status(), which synchronises the stream it is given.
+ *
+ * Return codes are mt_status values. A negative code from an enqueueing call
+ * means nothing was launched (argument errors) or a CUDA launch failed
+ * (MT_ERR_CUDA). Faults that only the device can see (a look-back wait that
+ * gave up) are recorded in a device error word and reported by
+ * mt_scan_status().
+ *
+ * Sources, cited by page title and section:
+ *   [scan.rs] metaltile-std 0.1.0, src/mlx/scan.rs (Rust kernel DSL page),
+ *             module doc "Scan benchmark" and fns mt_scan / mt_scan_exclusive.
+ *   [tile]    LuisaCompute, "Tile operations and reductions".
+ *   [algos]   Quadrants user guide, "Algorithms".
+ */
+#ifndef MT_SCAN_H
+#define MT_SCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MT_F32 = 0,  /* float32 */
+    MT_BF16 = 1, /* bfloat16: 8 exponent / 7 fraction bits */
+    MT_F16 = 2,  /* IEEE binary16 */
+    MT_I32 = 3,  /* int32, two's complement */
+    MT_I64 = 4   /* int64, two's complement */
+} mt_dtype;
+
+typedef enum { MT_ADD = 0, MT_MIN = 1, MT_MAX = 2 } mt_op;
+
+typedef enum {
+    MT_SCRATCH_SCAN = 1,   /* for mt_exclusive_scan */
+    MT_SCRATCH_SELECT = 2  /* for mt_select */
+} mt_scratch_kind;
+
+typedef enum {
+    MT_OK = 0,
+    MT_ERR_ARG = -1,              /* null pointer, negative size, bad enum */
+    MT_ERR_DTYPE = -2,            /* dtype not supported by this call */
+    MT_ERR_ALIAS = -3,            /* out == arr where in-place is forbidden */
+    MT_ERR_CUDA = -4,             /* a CUDA runtime call or launch failed */
+    MT_ERR_LOOKBACK_TIMEOUT = -5, /* device: a tile waited too long for a predecessor */
+    MT_ERR_ALIGN = -6             /* pointer not aligned to its element size */
+} mt_status;
+
+/*
+ * mt_scan_rows -- sum scan along the last axis of a contiguous row-major
+ * [rows, n] tensor.
+ *
+ * Definition ([scan.rs] module doc "Scan benchmark"; recurrence from [tile]
+ * "Why not just infer it from reduce?"): for each row independently,
+ *   inclusive: out[r][i] = sum_{j <= i} inp[r][j]
+ *   exclusive: out[r][i] = sum_{j <  i} inp[r][j],  out[r][0] = 0.
+ * Storage is `dtype` (MT_F32, MT_BF16 or MT_F16) for both inp and out; values
+ * are widened to f32, summed in f32 and rounded once to the storage type at
+ * the store (round to nearest, ties to even -- [tile] "Storage and
+ * arithmetic precision"). The f32 additions may be grouped differently from
+ * a left-to-right loop; the element order is never permuted.
+ *
+ * inp, out : device pointers to rows*n elements, each aligned to the element
+ *            size (any 16-byte misalignment of a row start is handled).
+ *            inp == out (in place) is allowed; other overlaps are not.
+ * rows, n  : >= 0. rows*n == 0 is a no-op that returns MT_OK.
+ * inclusive: nonzero for the inclusive form.
+ *
+ * Rows longer than one tile are split across CTAs that chain their carries
+ * with a single-pass decoupled look-back. Those calls take a small status
+ * workspace (8 bytes per tile plus 32 bytes) from a stream-ordered memory
+ * pool owned by the library (cudaMallocFromPoolAsync / cudaFreeAsync on
+ * `stream`); rows that fit in one tile use none.
+ * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIGN, MT_ERR_CUDA.
+ */
+int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
+                 int inclusive, void *stream);
+
+/*
+ * mt_exclusive_scan -- device-wide exclusive scan of a 1-D array
+ * ([algos] "qd.algorithms.exclusive_scan_{add,min,max}"):
+ *   out[i] = op(arr[0], ..., arr[i-1]),  out[0] = identity,
+ * identity from "Semantics > Common conventions > Identity value": add 0;
+ * min +inf (f32) / INT32_MAX / INT64_MAX; max -inf / INT32_MIN / INT64_MIN.
+ * Integer add wraps modulo 2^width. min keeps the earlier element on ties
+ * ((b < a) ? b : a) and max likewise, so the result is the same for every
+ * grouping; f32 add is summed in f32 and may be grouped differently from a
+ * left-to-right loop. Inputs are assumed NaN-free (NaN order is unspecified).
+ *
+ * arr, out : device arrays of `dtype` (MT_I32, MT_I64 or MT_F32), aligned to
+ *            the element size. out must not be arr ([algos]: "No in-place
+ *            scan") -> MT_ERR_ALIAS; other overlaps are undefined.
+ * scratch  : device memory of at least
+ *            mt_scan_scratch_slots(capacity, dtype, MT_SCRATCH_SCAN) 8-byte
+ *            slots, 16-byte aligned. It needs no initialisation ([algos]
+ *            "Scratch space"); the call resets what it uses on `stream`.
+ *            Concurrent calls must not share one scratch buffer.
+ * n_dev    : device pointer to the int32 live count n, read on the device
+ *            ([algos] "Key sizing parameters"). n < 0 is treated as 0.
+ *            n larger than the capacity the scratch was sized for is
+ *            undefined behaviour and is not checked (as on the page).
+ * Only out[0:n] is written; out[n:] is left untouched.
+ * Two kernels are launched: a status reset and the single-pass scan.
+ * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_ALIGN, MT_ERR_CUDA.
+ */
+int mt_exclusive_scan(const void *arr, void *out, void *scratch, const int32_t *n_dev,
+                      int dtype, int op, void *stream);
+
+/*
+ * mt_select -- stream compaction ([algos] "qd.algorithms.select"): every
+ * arr[i] with flags[i] == 1 is copied, in input order, into a dense prefix of
+ * out, and the number copied is written to *num_out. Elements are 4-byte
+ * words copied bit for bit (the copy ignores their type).
+ *
+ * arr      : device array of n 4-byte elements (4-byte aligned).
+ * flags    : device array of n uint8 flags, each exactly 0 or 1 (any other
+ *            value is undefined behaviour, as on the page).
+ * out      : device array with room for n elements; only out[0:*num_out] is
+ *            written, the rest is left untouched. out must not overlap arr.
+ * num_out  : device pointer to one int32.
+ * scratch  : mt_scan_scratch_slots(capacity, MT_I32, MT_SCRATCH_SELECT)
+ *            8-byte slots, 16-byte aligned, no initialisation needed; not
+ *            shared by concurrent calls.
+ * n_dev    : device pointer to the int32 live count (n < 0 treated as 0).
+ * Errors: MT_ERR_ARG, MT_ERR_ALIAS, MT_ERR_ALIGN, MT_ERR_CUDA.
+ */
+int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
+              void *scratch, const int32_t *n_dev, void *stream);
+
+/*
+ * mt_scan_scratch_slots -- number of 8-byte scratch slots that
+ * mt_exclusive_scan (kind MT_SCRATCH_SCAN, with its dtype) or mt_select
+ * (kind MT_SCRATCH_SELECT, dtype ignored) needs for any live count up to
+ * `capacity`. Plain host arithmetic, no device access ([algos] "Scratch
+ * space": ask first, then allocate). Returns -1 for a negative capacity or
+ * an unknown kind/dtype.
+ */
+int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind);
+
+/*
+ * mt_scan_status -- synchronise `stream`, then read and clear the device
+ * error word of every kernel of the library on the current device.
+ * Returns MT_OK, MT_ERR_LOOKBACK_TIMEOUT (a look-back wait gave up and the
+ * results of the calls since the last check are not valid), or MT_ERR_CUDA.
+ */
+int mt_scan_status(void *stream);
+
+/* Number of kernels this process has launched through the library (a host
+ * counter, for benchmarks that report launch counts). */
+uint64_t mt_scan_launches(void);
+
+/* Human-readable name of an mt_status code. */
+const char *mt_scan_strerror(int code);
+
+/*
+ * mt_scan_debug_lookback -- test hook for failure detection. Sets, for the
+ * following launches, (a) a global tile index whose CTA computes its results
+ * but never publishes its look-back status (-1 = none), and (b) the number of
+ * polls after which a waiting tile gives up, records
+ * MT_ERR_LOOKBACK_TIMEOUT and publishes its own status so that later tiles
+ * are not held (0 = the library default, about a second or more of waiting).
+ * Every wait stays bounded. Not for production use.
+ */
+int mt_scan_debug_lookback(int64_t skip_publish_tile, uint32_t spin_limit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MT_SCAN_H */

@@ -1,0 +1,161 @@
+"""Python binding of libmtscan.so (include/mt_scan.h): prefix scans on one
+NVIDIA GB300.
+
+The functions here only marshal arguments (pointers, sizes, the current CUDA
+stream) into the C ABI; every step of the scan runs in the library's CUDA
+kernels. There is no fallback: if the shared library is missing or fails to
+load, importing this package raises.
+
+Names and arguments follow the C ABI:
+
+* ``mt_scan_rows(inp, out, inclusive)`` -- row-wise sum scan of a contiguous
+  [rows, n] f32/bf16/f16 CUDA tensor.
+* ``mt_exclusive_scan(arr, out, scratch, n_dev, op)`` -- device-wide exclusive
+  add/min/max over i32/i64/f32 with the live count in a device int32.
+* ``mt_select(arr, flags, out, num_out, scratch, n_dev)`` -- stream compaction.
+* ``mt_scan_scratch_slots(capacity, dtype, kind)`` -- scratch sizing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmtscan.so")
+
+MT_F32, MT_BF16, MT_F16, MT_I32, MT_I64 = 0, 1, 2, 3, 4
+MT_ADD, MT_MIN, MT_MAX = 0, 1, 2
+MT_SCRATCH_SCAN, MT_SCRATCH_SELECT = 1, 2
+MT_OK = 0
+MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_LOOKBACK_TIMEOUT, MT_ERR_ALIGN = (
+    -1, -2, -3, -4, -5, -6)
+
+DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_F16,
+              torch.int32: MT_I32, torch.int64: MT_I64}
+OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX}
+
+EXPORTS = ("mt_scan_rows", "mt_exclusive_scan", "mt_select", "mt_scan_scratch_slots",
+           "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback")
+
+
+class ScanError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {mt_scan_strerror(code)} ({code})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`"
+            " (the scan library has no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+    L.mt_scan_rows.argtypes = [p, p, i64, i64, i32, i32, p]
+    L.mt_scan_rows.restype = i32
+    L.mt_exclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
+    L.mt_exclusive_scan.restype = i32
+    L.mt_select.argtypes = [p, p, p, p, p, p, p]
+    L.mt_select.restype = i32
+    L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
+    L.mt_scan_scratch_slots.restype = i64
+    L.mt_scan_status.argtypes = [p]
+    L.mt_scan_status.restype = i32
+    L.mt_scan_launches.argtypes = []
+    L.mt_scan_launches.restype = ctypes.c_uint64
+    L.mt_scan_strerror.argtypes = [i32]
+    L.mt_scan_strerror.restype = ctypes.c_char_p
+    L.mt_scan_debug_lookback.argtypes = [i64, u32]
+    L.mt_scan_debug_lookback.restype = i32
+    return L
+
+
+lib = _load()
+
+
+def mt_scan_strerror(code: int) -> str:
+    return lib.mt_scan_strerror(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != MT_OK:
+        raise ScanError(code, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else (t if isinstance(t, int) else t.data_ptr())
+
+
+def mt_scan_rows(inp: torch.Tensor, out: torch.Tensor, inclusive: bool, stream=None) -> None:
+    """Row-wise sum scan of a contiguous 2-D (or 1-D = one row) CUDA tensor."""
+    if inp.dim() == 1:
+        rows, n = 1, inp.shape[0]
+    else:
+        rows, n = inp.shape
+    if out.shape != inp.shape or out.dtype != inp.dtype:
+        raise ValueError("out must match inp in shape and dtype")
+    if not (inp.is_contiguous() and out.is_contiguous()):
+        raise ValueError("inp and out must be contiguous")
+    code = DTYPE_CODE.get(inp.dtype, -99)
+    _check(lib.mt_scan_rows(_ptr(inp), _ptr(out), rows, n, code, int(bool(inclusive)),
+                            _stream(stream)), "mt_scan_rows")
+
+
+def mt_exclusive_scan(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor,
+                      n_dev: torch.Tensor, op: str, stream=None) -> None:
+    """Exclusive scan of arr[0:*n_dev] into out (op: 'add' | 'min' | 'max')."""
+    if out.dtype != arr.dtype:
+        raise ValueError("out must have arr's dtype")
+    if n_dev.dtype != torch.int32:
+        raise ValueError("n_dev must be an int32 device tensor")
+    code = DTYPE_CODE.get(arr.dtype, -99)
+    _check(lib.mt_exclusive_scan(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code,
+                                 OP_CODE[op], _stream(stream)), "mt_exclusive_scan")
+
+
+def mt_select(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out: torch.Tensor,
+              scratch: torch.Tensor, n_dev: torch.Tensor, stream=None) -> None:
+    """Stream compaction of 4-byte elements by exactly-0/1 uint8 flags."""
+    if arr.element_size() != 4 or out.element_size() != 4:
+        raise ValueError("select copies 4-byte elements")
+    if flags.dtype != torch.uint8 or num_out.dtype != torch.int32 or n_dev.dtype != torch.int32:
+        raise ValueError("flags must be uint8, num_out and n_dev int32")
+    _check(lib.mt_select(_ptr(arr), _ptr(flags), _ptr(out), _ptr(num_out), _ptr(scratch),
+                         _ptr(n_dev), _stream(stream)), "mt_select")
+
+
+def mt_scan_scratch_slots(capacity: int, dtype, kind: int) -> int:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    r = lib.mt_scan_scratch_slots(int(capacity), code, int(kind))
+    if r < 0:
+        raise ValueError("mt_scan_scratch_slots: bad capacity, dtype or kind")
+    return r
+
+
+def alloc_scratch(capacity: int, dtype, kind: int, device="cuda") -> torch.Tensor:
+    """Caller-owned scratch of mt_scan_scratch_slots(...) 8-byte slots."""
+    return torch.empty(mt_scan_scratch_slots(capacity, dtype, kind), dtype=torch.int64,
+                       device=device)
+
+
+def mt_scan_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device error words."""
+    return lib.mt_scan_status(_stream(stream))
+
+
+def mt_scan_launches() -> int:
+    return lib.mt_scan_launches()
+
+
+def mt_scan_debug_lookback(skip_publish_tile: int = -1, spin_limit: int = 0) -> None:
+    lib.mt_scan_debug_lookback(int(skip_publish_tile), int(spin_limit))

@@ -1,0 +1,47 @@
+// mt_internal.h -- interface between the C-ABI layer (mt_abi.cu) and the
+// kernel translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mt {
+
+constexpr int kHeaderSlots = 4;              // scratch header: [0] tile counter, rest reserved
+constexpr uint32_t kDefaultSpin = 1u << 20;  // look-back polls before a waiter gives up
+
+struct Launch {
+    cudaStream_t stream;
+    int sm_count;
+    int64_t skip_tile;    // look-back test hook (-1: none)
+    uint32_t spin_limit;  // look-back poll limit
+};
+
+void note_launch();
+
+// ---- row-wise scan (mt_rows.cu) -------------------------------------------
+struct RowPlan {
+    int items;               // 16-byte chunks per thread
+    int64_t tile_elems;      // virtual elements per tile
+    int64_t tiles_per_row;   // 1: no look-back
+};
+RowPlan rows_plan(int dtype, int64_t n, bool heads_zero);
+cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int dtype,
+                        const RowPlan &p, bool inclusive, bool aligned_io, uint64_t *ws,
+                        const Launch &L);
+cudaError_t rows_take_error(int *code);
+
+// ---- device-wide exclusive scan (mt_scan1d.cu) ----------------------------
+int64_t scan1d_tile_elems(int dtype);
+int scan1d_rec_slots(int dtype);
+cudaError_t scan1d_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
+                          int dtype, int op, bool aligned_io, const Launch &L);
+cudaError_t scan1d_take_error(int *code);
+
+// ---- select (mt_select.cu) ------------------------------------------------
+int64_t select_tile_elems();
+cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
+                          uint64_t *scratch, const int32_t *n_dev, bool aligned, const Launch &L);
+cudaError_t select_take_error(int *code);
+
+}  // namespace mt

@@ -1,0 +1,149 @@
+// mt_lookback.cuh -- single-pass decoupled look-back across the tiles of one
+// segment (a row, or the whole 1-D array).
+//
+// Each tile owns a status record in device scratch. After its local reduce a
+// tile publishes its aggregate (flag kAgg); warp 0 then walks back over its
+// predecessors 32 at a time (one lane per predecessor), folding aggregates
+// until it meets a predecessor that has published an inclusive prefix
+// (kIncl); it then publishes its own inclusive prefix. The first tile of a
+// segment publishes its aggregate as inclusive at once. Tile ids come from an
+// atomic counter in launch order, so every tile waited on belongs to a CTA
+// that is already running: the wait always ends.
+//
+// Every wait is bounded: after `spin_limit` polls (or once another tile has
+// recorded an error) the waiter records MT_ERR_LOOKBACK_TIMEOUT in the
+// device error word, publishes what it has so later tiles are not held, and
+// carries on. Results are then invalid but the kernel ends and the context
+// stays usable.
+#pragma once
+
+#include "mt_tile.cuh"
+
+namespace mt {
+
+// Tile status records.
+template <class Acc, bool kPacked = (sizeof(Acc) == 4)> struct Status;
+
+// 4-byte values: one 8-byte word, flag in the high half and value bits in the
+// low half. A 64-bit store or load is single-copy atomic, and the value needs
+// no other data, so relaxed gpu-scope order is enough.
+template <class Acc> struct Status<Acc, true> {
+    static constexpr int kSlots = 1;
+    __device__ __forceinline__ static void publish(uint64_t *rec, uint32_t flag, Acc v) {
+        st_relaxed_u64(rec, ((uint64_t)flag << 32) | bits32<Acc>(v));
+    }
+    __device__ __forceinline__ static void read(const uint64_t *rec, uint32_t &flag, Acc &v) {
+        const uint64_t w = ld_relaxed_u64(rec);
+        flag = (uint32_t)(w >> 32);
+        v = from32<Acc>((uint32_t)w);
+    }
+};
+
+// 8-byte values: three words [flag, aggregate, inclusive]. The value word is
+// written before the flag (release) and read after it (acquire); each value
+// word is written once per call, so a reader never sees it change.
+template <class Acc> struct Status<Acc, false> {
+    static constexpr int kSlots = 3;
+    __device__ __forceinline__ static void publish(uint64_t *rec, uint32_t flag, Acc v) {
+        st_relaxed_u64(rec + (flag == kAgg ? 1 : 2), (uint64_t)v);
+        st_release_u64(rec, (uint64_t)flag);
+    }
+    __device__ __forceinline__ static void read(const uint64_t *rec, uint32_t &flag, Acc &v) {
+        flag = (uint32_t)ld_acquire_u64(rec);
+        if (flag == kAgg)
+            v = (Acc)ld_relaxed_u64(rec + 1);
+        else if (flag == kIncl)
+            v = (Acc)ld_relaxed_u64(rec + 2);
+    }
+};
+
+struct LookBack {
+    uint64_t *recs;      // tile records; nullptr when every segment is one tile
+    int64_t skip_tile;   // test hook: this tile never publishes (-1: none)
+    uint32_t spin_limit; // polls before a waiter gives up
+};
+
+// Called by all 32 lanes of warp 0. Returns the exclusive prefix of `tile`
+// (the combine of every earlier tile of the segment [first, tile)).
+template <class Acc, class Op>
+__device__ __forceinline__ Acc warp_lookback(const uint64_t *recs, int64_t tile, int64_t first,
+                                             uint32_t spin_limit) {
+    using St = Status<Acc>;
+    const int lane = threadIdx.x & 31;
+    const Acc ident = Op::template identity<Acc>();
+    Acc excl = ident;
+    int64_t pos = tile - 1;  // the newest predecessor not yet folded
+    uint32_t polls = 0;
+    for (;;) {
+        const int64_t t = pos - lane;  // lane 0: newest, lane 31: oldest of the window
+        uint32_t flag = kIncl;         // before the segment start: an inclusive identity
+        Acc val = ident;
+        if (t >= first)
+            St::read(recs + t * St::kSlots, flag, val);
+        const unsigned empty = __ballot_sync(kFull, flag == kEmpty);
+        const unsigned incl = __ballot_sync(kFull, flag == kIncl);
+        const unsigned low = incl & (0u - incl);                  // nearest inclusive predecessor
+        const unsigned need = incl ? (low | (low - 1u)) : kFull;  // lanes that must be folded
+        if (empty & need) {
+            ++polls;
+            bool give_up = polls >= spin_limit;
+            if (!give_up && (polls & 63u) == 0)
+                give_up = ld_relaxed_i32(&g_mt_err) != 0;
+            if (__any_sync(kFull, give_up)) {
+                if (lane == 0)
+                    atomicCAS(&g_mt_err, 0, kErrTimeout);
+                return excl;
+            }
+            if (polls > 8)
+                __nanosleep(polls < 64 ? 64 : 256);
+            continue;
+        }
+        // Ordered fold of lanes [0, last needed]: a higher lane holds an
+        // earlier tile, so it goes on the left.
+        Acc c = ((need >> lane) & 1u) ? val : ident;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Acc o = __shfl_down_sync(kFull, c, d);
+            if (lane + d < 32)
+                c = Op::apply(o, c);
+        }
+        c = __shfl_sync(kFull, c, 0);
+        excl = Op::apply(c, excl);
+        if (incl)
+            return excl;
+        pos -= 32;
+    }
+}
+
+// Block-wide: publish this tile's aggregate, look back, publish the inclusive
+// prefix, and return the tile's exclusive prefix to every thread.
+// `tile` and `first` are block-uniform.
+template <class Acc, class Op>
+__device__ __forceinline__ Acc tile_prefix(const LookBack &lb, int64_t tile, int64_t first, Acc agg,
+                                           Acc *sm_prefix) {
+    using St = Status<Acc>;
+    const Acc ident = Op::template identity<Acc>();
+    if (lb.recs == nullptr)
+        return ident;
+    uint64_t *rec = lb.recs + tile * St::kSlots;
+    const bool publish = tile != lb.skip_tile;
+    if (tile == first) {
+        if (threadIdx.x == 0 && publish)
+            St::publish(rec, kIncl, agg);
+        return ident;
+    }
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0 && publish)
+            St::publish(rec, kAgg, agg);
+        const Acc ex = warp_lookback<Acc, Op>(lb.recs, tile, first, lb.spin_limit);
+        if (threadIdx.x == 0) {
+            if (publish)
+                St::publish(rec, kIncl, Op::apply(ex, agg));
+            *sm_prefix = ex;
+        }
+    }
+    __syncthreads();
+    return *sm_prefix;
+}
+
+}  // namespace mt

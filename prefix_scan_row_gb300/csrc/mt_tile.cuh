@@ -1,0 +1,225 @@
+// mt_tile.cuh -- device building blocks shared by the scan kernels (sm_103a).
+//
+// One CTA tile is 256 threads x ITEMS chunks of 16 bytes. A warp owns a
+// contiguous run of 32*ITEMS chunks and reads it "warp-striped": chunk j of
+// lane l is chunk 32*j + l of the warp's run, so each 16-byte vector load or
+// store instruction of a warp touches 512 contiguous bytes.
+//
+// Scan hierarchy inside a tile (all combines keep the element order, the
+// "ordered tree" of LuisaCompute "Tile operations and reductions", section
+// "Why not just infer it from reduce?"):
+//   1. each thread scans the E elements of each of its chunks in registers;
+//   2. for each j, an inclusive warp scan (shfl_up) of the chunk totals;
+//   3. a running carry across j inside the warp;
+//   4. warp totals through shared memory to a block-wide exclusive prefix;
+//   5. a single-pass decoupled look-back across tiles of the same segment
+//      (row or 1-D array) gives the tile's exclusive prefix; the Quadrants
+//      "Algorithms" guide, section "Related", names decoupled look-back as
+//      the more efficient alternative to a multi-pass scan.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mt_internal.h"
+
+namespace mt {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Look-back status flags of a tile record.
+constexpr uint32_t kEmpty = 0;  // nothing published yet (the reset state)
+constexpr uint32_t kAgg = 1;    // the tile's own aggregate is published
+constexpr uint32_t kIncl = 2;   // the inclusive prefix through this tile is published
+
+constexpr int kErrTimeout = -5;  // same value as MT_ERR_LOOKBACK_TIMEOUT
+
+// Per translation unit device error word; written when a look-back wait gives up.
+static __device__ int g_mt_err;
+
+// ---------------------------------------------------------------------------
+// Combine operators. apply(a, b): `a` covers earlier elements than `b`.
+// ---------------------------------------------------------------------------
+template <class T> struct Lim;
+template <> struct Lim<float> {
+    __device__ __forceinline__ static float hi() { return __int_as_float(0x7f800000); }   // +inf
+    __device__ __forceinline__ static float lo() { return __int_as_float((int)0xff800000u); }  // -inf
+};
+template <> struct Lim<int32_t> {
+    __device__ __forceinline__ static int32_t hi() { return 0x7fffffff; }
+    __device__ __forceinline__ static int32_t lo() { return (int32_t)0x80000000u; }
+};
+template <> struct Lim<int64_t> {
+    __device__ __forceinline__ static int64_t hi() { return 0x7fffffffffffffffll; }
+    __device__ __forceinline__ static int64_t lo() { return (int64_t)0x8000000000000000ull; }
+};
+
+struct OpAdd {
+    template <class T> __device__ __forceinline__ static T identity() { return T(0); }
+    __device__ __forceinline__ static float apply(float a, float b) { return a + b; }
+    __device__ __forceinline__ static uint32_t apply(uint32_t a, uint32_t b) { return a + b; }
+    // integer add wraps modulo 2^width (two's complement), done in unsigned arithmetic
+    __device__ __forceinline__ static int32_t apply(int32_t a, int32_t b) {
+        return (int32_t)((uint32_t)a + (uint32_t)b);
+    }
+    __device__ __forceinline__ static int64_t apply(int64_t a, int64_t b) {
+        return (int64_t)((uint64_t)a + (uint64_t)b);
+    }
+};
+
+// min/max keep the earlier operand on ties, so any grouping gives the same
+// bits as a left-to-right fold (the leftmost extreme element).
+struct OpMin {
+    template <class T> __device__ __forceinline__ static T identity() { return Lim<T>::hi(); }
+    template <class T> __device__ __forceinline__ static T apply(T a, T b) { return (b < a) ? b : a; }
+};
+struct OpMax {
+    template <class T> __device__ __forceinline__ static T identity() { return Lim<T>::lo(); }
+    template <class T> __device__ __forceinline__ static T apply(T a, T b) { return (b > a) ? b : a; }
+};
+
+// ---------------------------------------------------------------------------
+// Storage codecs: a 16-byte chunk <-> E accumulator values.
+// bf16/f16 widen exactly to f32 and narrow with round-to-nearest-even
+// (LuisaCompute "Tile operations and reductions", "Storage and arithmetic
+// precision"); the metaltile-std scan.rs kernels likewise load as f32 and
+// cast once at the store.
+// ---------------------------------------------------------------------------
+template <class S> struct Codec;
+
+template <> struct Codec<float> {
+    using Acc = float;
+    static constexpr int E = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                          __float_as_uint(x[2]), __float_as_uint(x[3]));
+    }
+    __device__ __forceinline__ static Acc load1(const float *p) { return *p; }
+    __device__ __forceinline__ static void store1(float *p, Acc v) { *p = v; }
+};
+
+template <> struct Codec<__nv_bfloat16> {
+    using Acc = float;
+    static constexpr int E = 8;
+    __device__ __forceinline__ static void two(uint32_t w, Acc &a, Acc &b) {
+        a = __uint_as_float(w << 16);          // bf16 is the top half of an f32
+        b = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static uint32_t pack2(Acc a, Acc b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x = a (low half)
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        two(v.x, x[0], x[1]); two(v.y, x[2], x[3]); two(v.z, x[4], x[5]); two(v.w, x[6], x[7]);
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+    }
+    __device__ __forceinline__ static Acc load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    __device__ __forceinline__ static void store1(__nv_bfloat16 *p, Acc v) { *p = __float2bfloat16_rn(v); }
+};
+
+template <> struct Codec<__half> {
+    using Acc = float;
+    static constexpr int E = 8;
+    __device__ __forceinline__ static void two(uint32_t w, Acc &a, Acc &b) {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        float2 f = __half22float2(h);
+        a = f.x; b = f.y;
+    }
+    __device__ __forceinline__ static uint32_t pack2(Acc a, Acc b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        two(v.x, x[0], x[1]); two(v.y, x[2], x[3]); two(v.z, x[4], x[5]); two(v.w, x[6], x[7]);
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+    }
+    __device__ __forceinline__ static Acc load1(const __half *p) { return __half2float(*p); }
+    __device__ __forceinline__ static void store1(__half *p, Acc v) { *p = __float2half_rn(v); }
+};
+
+template <> struct Codec<int32_t> {
+    using Acc = int32_t;
+    static constexpr int E = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        x[0] = (int32_t)v.x; x[1] = (int32_t)v.y; x[2] = (int32_t)v.z; x[3] = (int32_t)v.w;
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4((uint32_t)x[0], (uint32_t)x[1], (uint32_t)x[2], (uint32_t)x[3]);
+    }
+    __device__ __forceinline__ static Acc load1(const int32_t *p) { return *p; }
+    __device__ __forceinline__ static void store1(int32_t *p, Acc v) { *p = v; }
+};
+
+template <> struct Codec<int64_t> {
+    using Acc = int64_t;
+    static constexpr int E = 2;
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        x[0] = (int64_t)(((uint64_t)v.y << 32) | v.x);
+        x[1] = (int64_t)(((uint64_t)v.w << 32) | v.z);
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4((uint32_t)x[0], (uint32_t)((uint64_t)x[0] >> 32),
+                          (uint32_t)x[1], (uint32_t)((uint64_t)x[1] >> 32));
+    }
+    __device__ __forceinline__ static Acc load1(const int64_t *p) { return *p; }
+    __device__ __forceinline__ static void store1(int64_t *p, Acc v) { *p = v; }
+};
+
+// ---------------------------------------------------------------------------
+// Memory primitives (inline PTX).
+// ---------------------------------------------------------------------------
+// Streaming 16-byte load that does not allocate in L1 (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed_i32(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <class T> __device__ __forceinline__ uint32_t bits32(T v);
+template <> __device__ __forceinline__ uint32_t bits32<float>(float v) { return __float_as_uint(v); }
+template <> __device__ __forceinline__ uint32_t bits32<int32_t>(int32_t v) { return (uint32_t)v; }
+template <> __device__ __forceinline__ uint32_t bits32<uint32_t>(uint32_t v) { return v; }
+template <class T> __device__ __forceinline__ T from32(uint32_t b);
+template <> __device__ __forceinline__ float from32<float>(uint32_t b) { return __uint_as_float(b); }
+template <> __device__ __forceinline__ int32_t from32<int32_t>(uint32_t b) { return (int32_t)b; }
+template <> __device__ __forceinline__ uint32_t from32<uint32_t>(uint32_t b) { return b; }
+
+}  // namespace mt
