@@ -1,0 +1,83 @@
+"""Comparison of CUDA-path outputs with the CPU oracle.
+
+Tolerances (written here, used by every parity test):
+  * integer add/min/max, float min/max, select (values and count): bit-exact;
+  * f32 add: |gpu - p64| <= 1e-5 * sum_{j<=i} |x_j| + 1e-6, per element, where
+    p64 is the oracle's fp64 prefix;
+  * bf16/f16 add: |gpu - RN_T(p64)| <= ulp_T(RN_T(p64)) + 1e-5 * sum_{j<=i}|x_j|
+    + 1e-6, with RN_T the oracle's round-to-nearest-even to the output type
+    and ulp_T the spacing of T at that value (subnormal spacing near 0);
+  * inputs whose every partial sum is exact in f32 (dyadic k/256 values):
+    bit-exact for all three storage types.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+REL, ABS = 1e-5, 1e-6
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_rows_close(gpu_out: torch.Tensor, x_cpu: torch.Tensor, dtype: str, inclusive: bool,
+                      exact: bool = False):
+    """Full comparison of a row scan with the oracle."""
+    ref, p64, mag = oracle.scan_rows(x_cpu, dtype, inclusive, want_f64=True)
+    if dtype == "f32":
+        got = gpu_out.detach().to("cpu").numpy()
+        if exact:
+            bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))
+            assert bad[0].size == 0, _report(bad, got, ref)
+            return
+        err = np.abs(got.astype(np.float64) - p64)
+        bound = REL * mag + ABS
+    else:
+        gbits = bits16(gpu_out)
+        if exact:
+            bad = np.nonzero(gbits != ref)
+            assert bad[0].size == 0, _report(bad, gbits, ref)
+            return
+        got = oracle.decode_half(gbits, dtype)
+        want = oracle.decode_half(ref, dtype)
+        err = np.abs(got - want)
+        bound = oracle.ulp_array(want, dtype) + REL * mag + ABS
+    bad = np.nonzero(~(err <= bound))
+    if bad[0].size:
+        i = tuple(b[0] for b in bad)
+        raise AssertionError(f"{bad[0].size} elements out of tolerance; first at {i}: "
+                             f"err {err[i]} bound {bound[i]}")
+
+
+def assert_scan_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dtype: str, op: str):
+    """1-D exclusive scan of arr[0:n]: bit-exact except f32 add (tolerance)."""
+    got = gpu_out[:n].detach().to("cpu").numpy()
+    if dtype == "f32" and op == "add":
+        _, p64, mag = oracle.exclusive_scan(arr_cpu, n, dtype, op, want_f64=True)
+        err = np.abs(got.astype(np.float64) - p64)
+        bound = REL * mag + ABS
+        bad = np.nonzero(~(err <= bound))[0]
+        assert bad.size == 0, f"{bad.size} out of tolerance; first {bad[0]}: {got[bad[0]]} vs {p64[bad[0]]}"
+        return
+    ref = oracle.exclusive_scan(arr_cpu, n, dtype, op)
+    w = {"i32": np.uint32, "f32": np.uint32, "i64": np.uint64}[dtype]
+    bad = np.nonzero(got.view(w) != ref.view(w))[0]
+    assert bad.size == 0, f"{bad.size} mismatches; first at {bad[0]}: {got[bad[0]]} vs {ref[bad[0]]}"
+
+
+def assert_select_matches(gpu_out: torch.Tensor, gpu_num: torch.Tensor, arr_cpu, flags_cpu, n: int):
+    ref, k = oracle.select(arr_cpu, flags_cpu, n)
+    got_k = int(gpu_num.item())
+    assert got_k == k, f"num_out {got_k} != {k}"
+    got = gpu_out[:k].detach().to("cpu").contiguous().view(torch.int32).numpy().view(np.uint32)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches; first at {bad[0]}"
+
+
+def _report(bad, got, ref):
+    i = tuple(b[0] for b in bad)
+    return f"{bad[0].size} mismatches; first at {i}: {got[i]} vs {ref[i]}"

@@ -1,0 +1,140 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every function
+include/mt_scan.h declares, and rejects bad arguments on the host before any
+CUDA call. No kernel is launched here."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mt_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from prefix_scan_row_gb300 import _build
+    path = _build.build()
+    L = ctypes.CDLL(path)
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.mt_scan_rows.argtypes = [p, p, i64, i64, i32, i32, p]
+    L.mt_exclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
+    L.mt_select.argtypes = [p, p, p, p, p, p, p]
+    L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
+    L.mt_scan_scratch_slots.restype = i64
+    L.mt_scan_strerror.argtypes = [i32]
+    L.mt_scan_strerror.restype = ctypes.c_char_p
+    L.mt_scan_launches.restype = ctypes.c_uint64
+    return L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mt_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in mt_scan.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (mt_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_binding_names_match_header():
+    import prefix_scan_row_gb300 as m
+    assert sorted(m.EXPORTS) == declared_functions()
+    for name in m.EXPORTS:
+        assert callable(getattr(m, name))
+
+
+F32, BF16, F16, I32, I64 = 0, 1, 2, 3, 4
+OK, ARG, DTYPE, ALIAS, CUDA, TIMEOUT, ALIGN = 0, -1, -2, -3, -4, -5, -6
+A, B, S, N = 0x10000, 0x20000, 0x30000, 0x40000  # fake, 16-byte aligned; never dereferenced
+
+
+def test_rows_host_checks(lib):
+    assert lib.mt_scan_rows(A, B, -1, 5, F32, 1, None) == ARG
+    assert lib.mt_scan_rows(A, B, 5, -1, F32, 1, None) == ARG
+    assert lib.mt_scan_rows(A, B, 2, 2, I32, 1, None) == DTYPE
+    assert lib.mt_scan_rows(A, B, 2, 2, 9, 1, None) == DTYPE
+    assert lib.mt_scan_rows(A, B, 0, 7, F32, 1, None) == OK       # empty: no-op
+    assert lib.mt_scan_rows(None, None, 3, 0, BF16, 0, None) == OK  # empty: no-op
+    assert lib.mt_scan_rows(None, B, 2, 2, F32, 1, None) == ARG
+    assert lib.mt_scan_rows(A + 2, B, 2, 2, F32, 1, None) == ALIGN
+    assert lib.mt_scan_rows(A + 1, B, 2, 2, F16, 1, None) == ALIGN
+    assert lib.mt_scan_rows(A, B, 1 << 40, 1 << 40, F32, 1, None) == ARG  # size overflow
+
+
+def test_exclusive_scan_host_checks(lib):
+    assert lib.mt_exclusive_scan(A, B, S, N, BF16, 0, None) == DTYPE
+    assert lib.mt_exclusive_scan(A, B, S, N, I32, 3, None) == ARG
+    assert lib.mt_exclusive_scan(A, B, S, N, I32, -1, None) == ARG
+    assert lib.mt_exclusive_scan(None, B, S, N, I32, 0, None) == ARG
+    assert lib.mt_exclusive_scan(A, B, None, N, I32, 0, None) == ARG
+    assert lib.mt_exclusive_scan(A, B, S, None, I32, 0, None) == ARG
+    assert lib.mt_exclusive_scan(A, A, S, N, I32, 0, None) == ALIAS
+    assert lib.mt_exclusive_scan(A + 4, B, S, N, I64, 0, None) == ALIGN
+    assert lib.mt_exclusive_scan(A, B, S + 8, N, I32, 0, None) == ALIGN
+    assert lib.mt_exclusive_scan(A, B, S, N + 2, I32, 0, None) == ALIGN
+
+
+def test_select_host_checks(lib):
+    assert lib.mt_select(None, A, B, N, S, N, None) == ARG
+    assert lib.mt_select(A, B, A, N, S, N, None) == ALIAS
+    assert lib.mt_select(A + 2, B, S, N, S, N, None) == ALIGN
+    assert lib.mt_select(A, B, S, N + 1, S, N, None) == ALIGN
+
+
+def test_scratch_slots(lib):
+    f = lib.mt_scan_scratch_slots
+    assert f(0, I32, 1) == 4
+    assert f(-1, I32, 1) == -1
+    assert f(10, BF16, 1) == -1
+    assert f(10, I32, 7) == -1
+    # 4096 elements per tile for 4-byte types, one 8-byte record each; up to
+    # three elements of head misalignment
+    assert f(4096, I32, 1) == 4 + 2
+    assert f(4093, F32, 1) == 4 + 1
+    assert f(1 << 28, I32, 1) == 4 + (1 << 16) + 1
+    # 2048 elements per tile for i64, three 8-byte words per record
+    assert f(2048, I64, 1) == 4 + 3 * 2
+    assert f(2047, I64, 1) == 4 + 3
+    # select: 8192 flags per tile, one record each
+    assert f(1 << 28, I32, 2) == 4 + (1 << 15)
+    assert f(1, I32, 2) == 4 + 1
+
+
+def test_strerror_and_counter(lib):
+    assert lib.mt_scan_strerror(0) == b"ok"
+    assert b"look-back" in lib.mt_scan_strerror(TIMEOUT)
+    assert lib.mt_scan_strerror(12345) == b"unknown status"
+    assert lib.mt_scan_launches() == 0  # nothing was launched on the CPU
+
+
+def test_package_fails_loudly_without_library():
+    """With the shared library absent the package refuses to import (no fallback)."""
+    with tempfile.TemporaryDirectory() as d:
+        pkg = os.path.join(d, "prefix_scan_row_gb300")
+        os.makedirs(pkg)
+        shutil.copy(os.path.join(ROOT, "prefix_scan_row_gb300", "__init__.py"), pkg)
+        r = subprocess.run([sys.executable, "-c", "import prefix_scan_row_gb300"], cwd=d,
+                           capture_output=True, text=True)
+        assert r.returncode != 0
+        assert "no CPU fallback" in r.stderr
+
+
+def test_product_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "prefix_scan_row_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read().lower()
+                assert "oracle" not in text, f
