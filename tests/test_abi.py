@@ -17,8 +17,8 @@ HEADER = os.path.join(ROOT, "include", "mt_scan.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from prefix_scan_row_gb300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     L = ctypes.CDLL(path)
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.mt_scan_rows.argtypes = [p, p, i64, i64, i32, i32, p]
