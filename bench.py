@@ -208,3 +208,297 @@ def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
         dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the --impl reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(host, frac):
+    """Scan the first `frac` of the rows of each of the step's tensors with the
+    single-threaded CPU oracle. Returns (seconds, algorithmic bytes, elements)."""
+    import oracle
+    secs = nbytes = elems = 0
+    for (name, r, n, d, inc), x in zip(CALLS, host):
+        rows = max(1, int(round(r * frac)))
+        xs = x[:rows]
+        t = time.perf_counter()
+        oracle.scan_rows(xs, d, inc)
+        secs += time.perf_counter() - t
+        nbytes += call_bytes(rows, n, d)
+        elems += rows * n
+    return secs, nbytes, elems
+
+
+def calibrate_oracle(host):
+    """Seconds one full step takes on the oracle, from a small sample."""
+    secs, nbytes, _ = oracle_sample(host, 16 / 4096)
+    return secs * STEP_BYTES / nbytes
+
+
+def cpu_baseline(host, target_s=12.0):
+    per_step = calibrate_oracle(host)
+    frac = min(1.0, target_s / per_step)
+    secs, nbytes, elems = oracle_sample(host, frac)
+    return {"value": nbytes / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "elements_per_s": elems / secs, "seconds": round(secs, 3),
+            "sample": f"first {frac:.4f} of the rows of each of the 4 tensors of one step "
+                      f"({elems} elements, {nbytes} algorithmic bytes), plain C, 1 thread"}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def make_host_inputs():
+    return [workloads.rows_half(r, n, d) for _, r, n, d, _ in CALLS]
+
+
+def run_ours(args, world, rank, local):
+    import prefix_scan_row_gb300 as mt
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    host = make_host_inputs()
+    xs = [h.to(dev) for h in host]
+    outs = [torch.empty_like(x) for x in xs]
+    incl = [c[4] for c in CALLS]
+
+    def step(ev=None):
+        for i in range(len(CALLS)):
+            if i == 0 and ev is not None:
+                ev[0].record(stream)
+            mt.mt_scan_rows(xs[i], outs[i], incl[i], stream)
+            if i == 0 and ev is not None:
+                ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mt.mt_scan_status(stream) == 0
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    dom = [(ev(), ev()) for _ in range(args.steps)]
+    start, end = ev(), ev()
+    sampler = ClockSampler(local).start()
+    time.sleep(0.05)
+    barrier()
+    torch.cuda.synchronize()
+    l0 = mt.mt_scan_launches()
+    th0 = time.perf_counter()
+    start.record(stream)
+    for k in range(args.steps):
+        step(dom[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    th1 = time.perf_counter()
+    barrier()
+    launches = mt.mt_scan_launches() - l0
+    time.sleep(0.05)
+    sampler.stop()
+    assert mt.mt_scan_status(stream) == 0, "device error word set during the timed region"
+    ms_local = start.elapsed_time(end)
+    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom)
+    ms, nbytes = aggregate(ms_local, STEP_BYTES * args.steps, dev if world > 1 else None)
+
+    # End to end through the C ABI with host buffers: every step copies its
+    # inputs from pinned host memory, runs the four calls, and copies the
+    # results back to pinned host memory.
+    pin_in = [h.pin_memory() for h in host]
+    pin_out = [torch.empty(h.shape, dtype=h.dtype).pin_memory() for h in host]
+
+    def e2e_step():
+        for i in range(len(CALLS)):
+            xs[i].copy_(pin_in[i], non_blocking=True)
+        for i in range(len(CALLS)):
+            mt.mt_scan_rows(xs[i], outs[i], incl[i], stream)
+        for i in range(len(CALLS)):
+            pin_out[i].copy_(outs[i], non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 100))
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms, e2e_bytes = aggregate(e0.elapsed_time(e1), STEP_BYTES * e2e_steps,
+                                  dev if world > 1 else None)
+    h2d = sum(h.numel() * h.element_size() for h in host)
+
+    peak, peak_src = measured_peak()
+    value = nbytes / (ms / 1e3) / 1e9
+    achieved = DOM_BYTES / (dom_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "storage": "bf16+f16", "accumulate": "f32",
+                   "calls_per_step": [c[0] for c in CALLS], "bytes_per_step": STEP_BYTES,
+                   "elements_per_step": STEP_ELEMS,
+                   "l2": f"inputs larger than L2: {STEP_BYTES/1e6:.0f} MB moved per step vs "
+                         f"{L2_BYTES/1e6:.0f} MB L2, no buffer touched twice within a step",
+                   "parallelism": f"replicas x{world} (rows shard with no exchange)"},
+        "elements_per_s": round(STEP_ELEMS * world * args.steps / (ms / 1e3), 1),
+        "frac_of_peak": {"measured": round(value / world / peak, 4), "peak_gbs": peak,
+                         "peak_source": peak_src, "datasheet_8000_gbs": round(value / world / 8000.0, 4)},
+        "e2e": {"value": round(e2e_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d, "steps": e2e_steps,
+                "how": "pinned host -> device copy, 4 mt_scan_rows calls, device -> pinned host "
+                       "copy, all on one stream, CUDA events around the steps"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
+                     "kernel": "k_scan_rows<__nv_bfloat16,4> on [8192,8192] exclusive",
+                     "bytes_per_launch": DOM_BYTES, "avg_launch_ms": round(dom_ms, 5),
+                     "peak_of": peak_src},
+        "clocks": sampler.summary(th0, th1),
+        "gpu_launches": int(launches),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle, as it stands, on the same workload.
+# ---------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    if rank != 0:
+        return  # rank 0 alone runs the CPU reference
+    host = make_host_inputs()
+    per_step = calibrate_oracle(host)
+    budget = 150.0  # seconds for the whole --warmup W --steps K run
+    frac = min(1.0, budget / max(1, args.steps + args.warmup) / per_step)
+    for _ in range(args.warmup):
+        oracle_sample(host, frac)
+    secs = nbytes = elems = 0
+    for _ in range(args.steps):
+        s, b, e = oracle_sample(host, frac)
+        secs, nbytes, elems = secs + s, nbytes + b, elems + e
+    value = nbytes / secs / 1e9
+    sample = (f"each step: the first {frac:.5f} of the rows of each of the 4 tensors "
+              f"({elems // max(1, args.steps)} elements), plain C oracle, 1 thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "storage": "bf16+f16", "accumulate": "f64 (oracle)"},
+        "elements_per_s": round(elems / secs, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# --suite: each kernel on each configured shape (not the bench line; a table
+# for the design notes). Calls are timed one by one with CUDA events; L2 is
+# flushed before every timed call whose buffers would fit in it.
+# ---------------------------------------------------------------------------
+def run_suite(args):
+    import prefix_scan_row_gb300 as mt
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, src = measured_peak()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    rows_out = []
+
+    def timeit(name, fn, nbytes, elems, reps=20):
+        small = nbytes < 2 * L2_BYTES
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            if small:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        assert mt.mt_scan_status() == 0
+        med = statistics.median(times)
+        gbs = nbytes / (med / 1e3) / 1e9
+        r = {"config": name, "ms": round(med, 4), "GB/s": round(gbs, 1),
+             "frac_measured": round(gbs / peak, 3), "Gelem/s": round(elems / (med / 1e3) / 1e9, 2),
+             "l2_flushed": small}
+        rows_out.append(r)
+        print(json.dumps(r), flush=True)
+
+    for name, (r, n, d), incs in [
+            ("rows f32 [1024,4096]", (1024, 4096, "f32"), (True, False)),
+            ("rows bf16 [8192,8192]", (8192, 8192, "bf16"), (False,)),
+            ("rows f16 [8192,8192]", (8192, 8192, "f16"), (False,)),
+            ("rows bf16 [4096,4099]", (4096, 4099, "bf16"), (True,)),
+            ("rows f16 [4096,4099]", (4096, 4099, "f16"), (True,)),
+            ("rows f32 [4,2^24]", (4, 1 << 24, "f32"), (True, False))]:
+        x = (workloads.rows_f32(r, n) if d == "f32" else workloads.rows_half(r, n, d)).to(dev)
+        o = torch.empty_like(x)
+        for inc in incs:
+            timeit(f"{name} {'incl' if inc else 'excl'}", lambda: mt.mt_scan_rows(x, o, inc),
+                   call_bytes(r, n, d), r * n)
+        del x, o
+    cap, n = workloads.SCAN1D_CAPACITY, workloads.SCAN1D_LIVE
+    n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
+    for d, tdt, s in (("i32", torch.int32, 4), ("f32", torch.float32, 4), ("i64", torch.int64, 8)):
+        a = workloads.scan1d(d).to(dev)
+        o = torch.empty_like(a)
+        scr = mt.alloc_scratch(cap, tdt, mt.MT_SCRATCH_SCAN, device=dev)
+        for op in ("add", "min", "max"):
+            timeit(f"exclusive_scan {d} {op} n=2^28-12345",
+                   lambda: mt.mt_exclusive_scan(a, o, scr, n_dev, op), 2 * s * n, n)
+        del a, o, scr
+    ns = workloads.SELECT_N
+    nd = torch.tensor([ns], dtype=torch.int32, device=dev)
+    for p in (0.5, 0.01):
+        v, f = workloads.select_inputs(ns, p)
+        k = int(f.sum())
+        v, f = v.to(dev), f.to(dev)
+        o = torch.empty_like(v)
+        num = torch.zeros(1, dtype=torch.int32, device=dev)
+        scr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_SELECT, device=dev)
+        timeit(f"select f32 n=2^28 p={p}", lambda: mt.mt_select(v, f, o, num, scr, nd),
+               5 * ns + 4 * k, ns)
+        del v, f, o, scr
+    if args.suite_out:
+        with open(args.suite_out, "w") as fh:
+            json.dump({"peak_gbs": peak, "peak_source": src, "rows": rows_out}, fh, indent=1)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the CPU-oracle baseline (profiling runs)")
+    ap.add_argument("--suite", action="store_true", help="time every kernel on every configured shape")
+    ap.add_argument("--suite-out", default=None)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_env()
+    if args.suite:
+        run_suite(args)
+    elif args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()
