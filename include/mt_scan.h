@@ -51,7 +51,8 @@ typedef enum {
     MT_ERR_ALIAS = -3,            /* out == arr where in-place is forbidden */
     MT_ERR_CUDA = -4,             /* a CUDA runtime call or launch failed */
     MT_ERR_LOOKBACK_TIMEOUT = -5, /* device: a tile waited too long for a predecessor */
-    MT_ERR_ALIGN = -6             /* pointer not aligned to its element size */
+    MT_ERR_ALIGN = -6,            /* pointer not aligned to its element size */
+    MT_ERR_TOO_LARGE = -7         /* needs more than the fixed no-allocation scratch */
 } mt_status;
 
 /*
@@ -170,6 +171,32 @@ const char *mt_scan_strerror(int code);
  * Every wait stays bounded. Not for production use.
  */
 int mt_scan_debug_lookback(int64_t skip_publish_tile, uint32_t spin_limit);
+
+/*
+ * mt_scan_rows_noalloc -- the row scan of mt_scan_rows, for callers that may
+ * not allocate device memory. The pages have no counterpart: it exists for
+ * programs whose device memory is all reserved up front by another
+ * allocator, for loops where an allocation call could take a driver lock or
+ * wait on the device, and for hosts that forbid device allocations after
+ * start-up. mt_scan_rows takes the look-back records of long rows from a
+ * memory pool; this variant takes them from one fixed array inside the
+ * library instead, and calls no allocating routine.
+ *
+ * Arguments, results and the other errors are those of mt_scan_rows.
+ * Limit: the array holds MT_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that
+ * loads the library, for the life of the process, which covers
+ * rows * tiles_per_row <= 131068 tiles (a tile is 4096 f32 or 8192 bf16/f16
+ * elements of a row; rows of at most 8192 elements use no tiles of it). A
+ * larger call returns MT_ERR_TOO_LARGE and launches nothing.
+ * The first call on each device looks up the array's device address (a
+ * cudaGetSymbolAddress call), so make that first call before any stream
+ * capture. Every call uses the same array and clears the part it needs
+ * first; calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on it and must not be made.
+ */
+#define MT_NOALLOC_SCRATCH_BYTES (1 << 20)
+int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
+                         int inclusive, void *stream);
 
 #ifdef __cplusplus
 }

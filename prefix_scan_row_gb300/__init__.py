@@ -31,13 +31,16 @@ MT_SCRATCH_SCAN, MT_SCRATCH_SELECT = 1, 2
 MT_OK = 0
 MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_LOOKBACK_TIMEOUT, MT_ERR_ALIGN = (
     -1, -2, -3, -4, -5, -6)
+MT_ERR_TOO_LARGE = -7
+MT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_F16,
               torch.int32: MT_I32, torch.int64: MT_I64}
 OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX}
 
 EXPORTS = ("mt_scan_rows", "mt_exclusive_scan", "mt_select", "mt_scan_scratch_slots",
-           "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback")
+           "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback",
+           "mt_scan_rows_noalloc")
 
 
 class ScanError(RuntimeError):
@@ -69,6 +72,8 @@ def _load():
     L.mt_scan_strerror.restype = ctypes.c_char_p
     L.mt_scan_debug_lookback.argtypes = [i64, u32]
     L.mt_scan_debug_lookback.restype = i32
+    L.mt_scan_rows_noalloc.argtypes = [p, p, i64, i64, i32, i32, p]
+    L.mt_scan_rows_noalloc.restype = i32
     return L
 
 
@@ -159,3 +164,22 @@ def mt_scan_launches() -> int:
 
 def mt_scan_debug_lookback(skip_publish_tile: int = -1, spin_limit: int = 0) -> None:
     lib.mt_scan_debug_lookback(int(skip_publish_tile), int(spin_limit))
+
+
+def mt_scan_rows_noalloc(inp: torch.Tensor, out: torch.Tensor, inclusive: bool, stream=None) -> None:
+    """mt_scan_rows without any device allocation, for callers that may not
+    allocate: the look-back records of long rows live in a fixed 1 MiB array
+    inside the library. Raises ScanError(MT_ERR_TOO_LARGE) for a shape that
+    needs more. The first call on a device looks up that array's address;
+    calls that overlap on the GPU must not be made."""
+    if inp.dim() == 1:
+        rows, n = 1, inp.shape[0]
+    else:
+        rows, n = inp.shape
+    if out.shape != inp.shape or out.dtype != inp.dtype:
+        raise ValueError("out must match inp in shape and dtype")
+    if not (inp.is_contiguous() and out.is_contiguous()):
+        raise ValueError("inp and out must be contiguous")
+    code = DTYPE_CODE.get(inp.dtype, -99)
+    _check(lib.mt_scan_rows_noalloc(_ptr(inp), _ptr(out), rows, n, code, int(bool(inclusive)),
+                                    _stream(stream)), "mt_scan_rows_noalloc")

@@ -249,6 +249,7 @@ extern "C" const char *mt_scan_strerror(int code) {
     case MT_ERR_CUDA: return "CUDA error";
     case MT_ERR_LOOKBACK_TIMEOUT: return "look-back wait gave up (results invalid)";
     case MT_ERR_ALIGN: return "pointer misaligned";
+    case MT_ERR_TOO_LARGE: return "needs more than the fixed no-allocation scratch (MT_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
     }
 }
