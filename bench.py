@@ -416,7 +416,12 @@ def run_suite(args):
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     rows_out = []
 
+    def wanted(name):
+        return args.only is None or args.only in name
+
     def timeit(name, fn, nbytes, elems, reps=20):
+        if not wanted(name):
+            return
         small = nbytes < 2 * L2_BYTES
         for _ in range(3):
             fn()
@@ -446,32 +451,39 @@ def run_suite(args):
             ("rows bf16 [4096,4099]", (4096, 4099, "bf16"), (True,)),
             ("rows f16 [4096,4099]", (4096, 4099, "f16"), (True,)),
             ("rows f32 [4,2^24]", (4, 1 << 24, "f32"), (True, False))]:
+        if not any(wanted(f"{name} {'incl' if i else 'excl'}") for i in incs):
+            continue
         x = (workloads.rows_f32(r, n) if d == "f32" else workloads.rows_half(r, n, d)).to(dev)
         o = torch.empty_like(x)
         for inc in incs:
             timeit(f"{name} {'incl' if inc else 'excl'}", lambda: mt.mt_scan_rows(x, o, inc),
                    call_bytes(r, n, d), r * n)
         del x, o
-    cap, n = workloads.SCAN1D_CAPACITY, workloads.SCAN1D_LIVE
+    cap, n = workloads.SCAN1D_CAPACITY // args.scale, workloads.SCAN1D_LIVE // args.scale
+    tag = "n=2^28-12345" if args.scale == 1 else f"n=(2^28-12345)/{args.scale}"
     n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
     for d, tdt, s in (("i32", torch.int32, 4), ("f32", torch.float32, 4), ("i64", torch.int64, 8)):
-        a = workloads.scan1d(d).to(dev)
+        if not any(wanted(f"exclusive_scan {d} {op} {tag}") for op in ("add", "min", "max")):
+            continue
+        a = workloads.scan1d(d, capacity=cap).to(dev)
         o = torch.empty_like(a)
         scr = mt.alloc_scratch(cap, tdt, mt.MT_SCRATCH_SCAN, device=dev)
         for op in ("add", "min", "max"):
-            timeit(f"exclusive_scan {d} {op} n=2^28-12345",
+            timeit(f"exclusive_scan {d} {op} {tag}",
                    lambda: mt.mt_exclusive_scan(a, o, scr, n_dev, op), 2 * s * n, n)
         del a, o, scr
-    ns = workloads.SELECT_N
+    ns = workloads.SELECT_N // args.scale
     nd = torch.tensor([ns], dtype=torch.int32, device=dev)
     for p in (0.5, 0.01):
+        if not wanted(f"select f32 n={ns} p={p}"):
+            continue
         v, f = workloads.select_inputs(ns, p)
         k = int(f.sum())
         v, f = v.to(dev), f.to(dev)
         o = torch.empty_like(v)
         num = torch.zeros(1, dtype=torch.int32, device=dev)
         scr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_SELECT, device=dev)
-        timeit(f"select f32 n=2^28 p={p}", lambda: mt.mt_select(v, f, o, num, scr, nd),
+        timeit(f"select f32 n={ns} p={p}", lambda: mt.mt_select(v, f, o, num, scr, nd),
                5 * ns + 4 * k, ns)
         del v, f, o, scr
     if args.suite_out:
@@ -489,6 +501,8 @@ def main():
                     help="skip the CPU-oracle baseline (profiling runs)")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every configured shape")
     ap.add_argument("--suite-out", default=None)
+    ap.add_argument("--only", default=None, help="suite: run only configs whose name contains this")
+    ap.add_argument("--scale", type=int, default=1, help="suite: divide the 1-D sizes by this")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()
