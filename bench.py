@@ -417,7 +417,7 @@ def run_suite(args):
     rows_out = []
 
     def wanted(name):
-        return args.only is None or args.only in name
+        return args.only is None or any(o in name for o in args.only.split("|"))
 
     def timeit(name, fn, nbytes, elems, reps=20):
         if not wanted(name):

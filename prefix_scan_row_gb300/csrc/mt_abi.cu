@@ -140,7 +140,7 @@ extern "C" int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n,
         return MT_ERR_CUDA;
     uint64_t *ws = nullptr;
     if (p.tiles_per_row > 1) {
-        const int64_t nwords = kHeaderSlots + rows * p.tiles_per_row;
+        const int64_t nwords = kHeaderSlots + rows * p.tiles_per_row * rows_rec_slots();
         cudaMemPool_t pool;
         if (device_pool(dev, &pool) != cudaSuccess)
             return MT_ERR_CUDA;
@@ -197,7 +197,8 @@ extern "C" int mt_select(const void *arr, const uint8_t *flags, void *out, int32
     if (!make_launch(stream, &L, nullptr))
         return MT_ERR_CUDA;
     uint64_t *sw = static_cast<uint64_t *>(scratch);
-    if (launch_reset(sw, 0, n_dev, select_tile_elems(), 1, 0, 1, num_out, L) != cudaSuccess)
+    if (launch_reset(sw, 0, n_dev, select_tile_elems(), 1, 0, select_rec_slots(), num_out, L) !=
+        cudaSuccess)
         return MT_ERR_CUDA;
     const bool aligned = ((uintptr_t)arr % 16 == 0) && ((uintptr_t)flags % 16 == 0);
     return select_launch(arr, flags, out, num_out, sw, n_dev, aligned, L) == cudaSuccess
@@ -218,7 +219,7 @@ extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) 
     }
     if (kind == MT_SCRATCH_SELECT) {
         const int64_t te = select_tile_elems();
-        return kHeaderSlots + (capacity + te - 1) / te;
+        return kHeaderSlots + (capacity + te - 1) / te * select_rec_slots();
     }
     return -1;
 }

@@ -21,15 +21,17 @@ void note_launch();
 
 // ---- row-wise scan (mt_rows.cu) -------------------------------------------
 struct RowPlan {
+    bool staged;             // row longer than one CTA tile: persistent staged kernel
     int items;               // 16-byte chunks per thread
     int64_t tile_elems;      // virtual elements per tile
-    int64_t tiles_per_row;   // 1: no look-back
+    int64_t tiles_per_row;   // 1: no look-back (and no workspace)
 };
 RowPlan rows_plan(int dtype, int64_t n, bool heads_zero);
 cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int dtype,
                         const RowPlan &p, bool inclusive, bool aligned_io, uint64_t *ws,
                         const Launch &L);
 cudaError_t rows_take_error(int *code);
+int rows_rec_slots();  // 8-byte slots per look-back record of a long row
 
 // ---- device-wide exclusive scan (mt_scan1d.cu) ----------------------------
 int64_t scan1d_tile_elems(int dtype);
@@ -40,6 +42,7 @@ cudaError_t scan1d_take_error(int *code);
 
 // ---- select (mt_select.cu) ------------------------------------------------
 int64_t select_tile_elems();
+int select_rec_slots();
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                           uint64_t *scratch, const int32_t *n_dev, bool aligned, const Launch &L);
 cudaError_t select_take_error(int *code);

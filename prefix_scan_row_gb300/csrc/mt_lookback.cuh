@@ -21,6 +21,14 @@
 
 namespace mt {
 
+#ifndef MT_REC_SLOTS
+#define MT_REC_SLOTS 4  // 8-byte slots per record: one 32-byte sector each, so the
+                        // records near the look-back front spread over L2 slices
+#endif
+#if MT_REC_SLOTS < 3
+#error "a record needs at least three 8-byte slots for 8-byte values"
+#endif
+
 // Tile status records.
 template <class Acc, bool kPacked = (sizeof(Acc) == 4)> struct Status;
 
@@ -28,7 +36,7 @@ template <class Acc, bool kPacked = (sizeof(Acc) == 4)> struct Status;
 // low half. A 64-bit store or load is single-copy atomic, and the value needs
 // no other data, so relaxed gpu-scope order is enough.
 template <class Acc> struct Status<Acc, true> {
-    static constexpr int kSlots = 1;
+    static constexpr int kSlots = MT_REC_SLOTS;
     __device__ __forceinline__ static void publish(uint64_t *rec, uint32_t flag, Acc v) {
         st_relaxed_u64(rec, ((uint64_t)flag << 32) | bits32<Acc>(v));
     }
@@ -43,7 +51,7 @@ template <class Acc> struct Status<Acc, true> {
 // written before the flag (release) and read after it (acquire); each value
 // word is written once per call, so a reader never sees it change.
 template <class Acc> struct Status<Acc, false> {
-    static constexpr int kSlots = 3;
+    static constexpr int kSlots = MT_REC_SLOTS;
     __device__ __forceinline__ static void publish(uint64_t *rec, uint32_t flag, Acc v) {
         st_relaxed_u64(rec + (flag == kAgg ? 1 : 2), (uint64_t)v);
         st_release_u64(rec, (uint64_t)flag);
@@ -63,28 +71,55 @@ struct LookBack {
     uint32_t spin_limit; // polls before a waiter gives up
 };
 
+#ifndef MT_LB_PER_LANE
+#define MT_LB_PER_LANE 1
+#endif
+// Predecessors read by each lane per poll: the window is 32 * kLbPerLane tiles.
+// The inclusive-prefix front advances by at most one window per L2 round trip,
+// so the window bounds the scan's throughput at window x tile bytes / latency.
+constexpr int kLbPerLane = MT_LB_PER_LANE;
+
 // Called by all 32 lanes of warp 0. Returns the exclusive prefix of `tile`
 // (the combine of every earlier tile of the segment [first, tile)).
+// Lane l reads tiles pos - l*K - i, i = 0..K-1 (i = 0 newest), so lanes hold
+// consecutive groups and a higher lane always holds older tiles.
 template <class Acc, class Op>
 __device__ __forceinline__ Acc warp_lookback(const uint64_t *recs, int64_t tile, int64_t first,
                                              uint32_t spin_limit) {
     using St = Status<Acc>;
+    constexpr int K = kLbPerLane;
     const int lane = threadIdx.x & 31;
     const Acc ident = Op::template identity<Acc>();
     Acc excl = ident;
     int64_t pos = tile - 1;  // the newest predecessor not yet folded
     uint32_t polls = 0;
     for (;;) {
-        const int64_t t = pos - lane;  // lane 0: newest, lane 31: oldest of the window
-        uint32_t flag = kIncl;         // before the segment start: an inclusive identity
-        Acc val = ident;
-        if (t >= first)
-            St::read(recs + t * St::kSlots, flag, val);
-        const unsigned empty = __ballot_sync(kFull, flag == kEmpty);
-        const unsigned incl = __ballot_sync(kFull, flag == kIncl);
-        const unsigned low = incl & (0u - incl);                  // nearest inclusive predecessor
+        uint32_t f[K];
+        Acc v[K];
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int64_t t = pos - (int64_t)lane * K - i;
+            f[i] = kIncl;  // before the segment start: an inclusive identity
+            v[i] = ident;
+            if (t >= first)
+                St::read(recs + t * St::kSlots, f[i], v[i]);
+        }
+        // Nearest inclusive predecessor within this lane's group (K: none),
+        // and whether a tile this lane must fold is still empty.
+        int inc_i = K;
+#pragma unroll
+        for (int i = K - 1; i >= 0; --i)
+            if (f[i] == kIncl)
+                inc_i = i;
+        bool blocked = false;
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+            if (i <= inc_i && f[i] == kEmpty)
+                blocked = true;
+        const unsigned incl = __ballot_sync(kFull, inc_i < K);
+        const unsigned low = incl & (0u - incl);                  // lane of the nearest inclusive
         const unsigned need = incl ? (low | (low - 1u)) : kFull;  // lanes that must be folded
-        if (empty & need) {
+        if (__ballot_sync(kFull, blocked) & need) {
             ++polls;
             bool give_up = polls >= spin_limit;
             if (!give_up && (polls & 63u) == 0)
@@ -98,9 +133,15 @@ __device__ __forceinline__ Acc warp_lookback(const uint64_t *recs, int64_t tile,
                 __nanosleep(polls < 64 ? 64 : 256);
             continue;
         }
-        // Ordered fold of lanes [0, last needed]: a higher lane holds an
-        // earlier tile, so it goes on the left.
-        Acc c = ((need >> lane) & 1u) ? val : ident;
+        // Fold this lane's group, oldest first, stopping at its inclusive one.
+        Acc c = ident;
+        if ((need >> lane) & 1u) {
+#pragma unroll
+            for (int i = K - 1; i >= 0; --i)
+                if (i <= inc_i)
+                    c = Op::apply(c, v[i]);
+        }
+        // Ordered fold across lanes: a higher lane holds older tiles (left).
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const Acc o = __shfl_down_sync(kFull, c, d);
@@ -111,39 +152,50 @@ __device__ __forceinline__ Acc warp_lookback(const uint64_t *recs, int64_t tile,
         excl = Op::apply(c, excl);
         if (incl)
             return excl;
-        pos -= 32;
+        pos -= 32 * K;
     }
 }
 
-// Block-wide: publish this tile's aggregate, look back, publish the inclusive
-// prefix, and return the tile's exclusive prefix to every thread.
-// `tile` and `first` are block-uniform.
+// Thread 0 publishes this tile's aggregate: as the inclusive prefix for the
+// first tile of a segment, as an aggregate otherwise.
 template <class Acc, class Op>
-__device__ __forceinline__ Acc tile_prefix(const LookBack &lb, int64_t tile, int64_t first, Acc agg,
-                                           Acc *sm_prefix) {
+__device__ __forceinline__ void publish_aggregate(const LookBack &lb, int64_t tile, int64_t first,
+                                                  Acc agg) {
+    using St = Status<Acc>;
+    if (lb.recs == nullptr || threadIdx.x != 0 || tile == lb.skip_tile)
+        return;
+    St::publish(lb.recs + tile * St::kSlots, tile == first ? kIncl : kAgg, agg);
+}
+
+// Block-wide, after publish_aggregate: warp 0 looks back, thread 0 publishes
+// the inclusive prefix; every thread gets the tile's exclusive prefix.
+// `tile` and `first` are block-uniform; `agg` is needed in thread 0 only.
+template <class Acc, class Op>
+__device__ __forceinline__ Acc lookback_prefix(const LookBack &lb, int64_t tile, int64_t first,
+                                               Acc agg, Acc *sm_prefix) {
     using St = Status<Acc>;
     const Acc ident = Op::template identity<Acc>();
-    if (lb.recs == nullptr)
+    if (lb.recs == nullptr || tile == first)
         return ident;
-    uint64_t *rec = lb.recs + tile * St::kSlots;
-    const bool publish = tile != lb.skip_tile;
-    if (tile == first) {
-        if (threadIdx.x == 0 && publish)
-            St::publish(rec, kIncl, agg);
-        return ident;
-    }
     if (threadIdx.x < 32) {
-        if (threadIdx.x == 0 && publish)
-            St::publish(rec, kAgg, agg);
         const Acc ex = warp_lookback<Acc, Op>(lb.recs, tile, first, lb.spin_limit);
         if (threadIdx.x == 0) {
-            if (publish)
-                St::publish(rec, kIncl, Op::apply(ex, agg));
+            if (tile != lb.skip_tile)
+                St::publish(lb.recs + tile * St::kSlots, kIncl, Op::apply(ex, agg));
             *sm_prefix = ex;
         }
     }
     __syncthreads();
     return *sm_prefix;
+}
+
+// Both steps at once: publish the aggregate, look back, publish the inclusive
+// prefix, and return the tile's exclusive prefix to every thread.
+template <class Acc, class Op>
+__device__ __forceinline__ Acc tile_prefix(const LookBack &lb, int64_t tile, int64_t first, Acc agg,
+                                           Acc *sm_prefix) {
+    publish_aggregate<Acc, Op>(lb, tile, first, agg);
+    return lookback_prefix<Acc, Op>(lb, tile, first, agg, sm_prefix);
 }
 
 }  // namespace mt

@@ -79,7 +79,8 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
     const RowPlan p = rows_plan(dtype, n, heads_zero);
     if (p.tiles_per_row > INT32_MAX / rows)
         return MT_ERR_ARG;
-    const int64_t nwords = (p.tiles_per_row > 1) ? kHeaderSlots + rows * p.tiles_per_row : 0;
+    const int64_t nwords =
+        (p.tiles_per_row > 1) ? kHeaderSlots + rows * p.tiles_per_row * rows_rec_slots() : 0;
     if (nwords > kNoAllocSlots)
         return MT_ERR_TOO_LARGE;
 
@@ -88,7 +89,10 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
         return MT_ERR_CUDA;
     Launch L;
     L.stream = static_cast<cudaStream_t>(stream);
-    L.sm_count = 0;  // unused by the row launcher
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&L.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MT_ERR_CUDA;
     L.skip_tile = -1;
     L.spin_limit = kDefaultSpin;
     if (nwords > 0) {

@@ -6,10 +6,11 @@
 // out[i] = sum_{j<i} inp[j] with out[0] = 0, f32 loads and accumulation and
 // one cast at the store). The page runs one threadgroup per row that walks
 // the row in 1024-element chunks with a serial carry; here a row that fits
-// in one tile is one CTA, and a longer row is split over several CTAs whose
-// carries are chained by the decoupled look-back, so every row -- short or
-// 2^24 long -- is read once and written once.
-#include "mt_tilescan.cuh"
+// in one tile is one CTA (k_scan_rows), and a longer row is split over tiles
+// of a persistent pipelined kernel (mt_pipe.cuh) whose carries are chained by
+// the decoupled look-back, so every row -- short or 2^24 long -- is read once
+// and written once.
+#include "mt_staged.cuh"
 
 namespace mt {
 
@@ -18,30 +19,16 @@ struct RowArgs {
     char *out;
     int64_t rows;
     int64_t n;
-    int64_t tpr;                  // tiles per row
     int inclusive;
-    int aligned_io;               // output rows have the input rows' 16-byte phase
-    unsigned long long *counter;  // dynamic tile ids (multi-tile rows only)
-    LookBack lb;
+    int aligned_io;  // output rows have the input rows' 16-byte phase
 };
 
+// One CTA per row; the whole row is one tile.
 template <class S, int ITEMS>
 __global__ void __launch_bounds__(kThreads) k_scan_rows(RowArgs a) {
     using T = TileScan<S, OpAdd, ITEMS>;
     __shared__ typename T::Smem sm;
-    int64_t g;
-    if (a.lb.recs == nullptr) {
-        g = blockIdx.x;  // one tile per row: no ordering needed
-    } else {
-        // Tile ids in the order CTAs start, so every tile a CTA waits on has
-        // already been taken by a running CTA.
-        if (threadIdx.x == 0)
-            sm.tile = atomicAdd(a.counter, 1ull);
-        __syncthreads();
-        g = (int64_t)sm.tile;
-    }
-    const int64_t row = g / a.tpr;
-    const int64_t k = g - row * a.tpr;
+    const int64_t row = blockIdx.x;
     if (row >= a.rows)
         return;
     constexpr int64_t s = sizeof(S);
@@ -49,16 +36,57 @@ __global__ void __launch_bounds__(kThreads) k_scan_rows(RowArgs a) {
     const int64_t head = (int64_t)(((uintptr_t)in_row & 15u) / s);
     const uint4 *vin = reinterpret_cast<const uint4 *>(in_row - head * s);
     S *eout = reinterpret_cast<S *>(a.out + row * a.n * s) - head;
-    const int64_t t0 = k * T::kTE;
-    const int64_t hi = head + a.n;
-    if (t0 >= hi)
-        return;  // an empty trailing tile: nothing to do, and nobody waits on it
-    T::run(vin, eout, a.aligned_io != 0, t0, head, hi, a.inclusive != 0, a.lb, g, row * a.tpr, sm);
+    const LookBack none{nullptr, -1, 0};
+    T::run(vin, eout, a.aligned_io != 0, 0, head, head + a.n, a.inclusive != 0, none, row, row, sm);
 }
 
 // Chunks per thread tried for rows that fit in one tile; longer rows use
-// kMultiItems per tile (16 KB of input per tile).
+// kMultiItems per tile (16 KB of input per tile) and kRowStages tiles in
+// flight per CTA.
+#ifndef MT_ROWS_KIND
+#define MT_ROWS_KIND 2  // long rows: 0 direct loads, 1 bulk-copy ring, 2 staged super-tiles
+#endif
+#ifndef MT_ROWS_SUB_WIDE
+#define MT_ROWS_SUB_WIDE 3  // sub-tiles per super-tile, 4-byte storage
+#endif
+#ifndef MT_ROWS_SUB_HALF
+#define MT_ROWS_SUB_HALF 2  // 2-byte storage (its f32 prefixes take two planes)
+#endif
+#ifndef MT_ROWS_THREADS
+#define MT_ROWS_THREADS 256
+#endif
+#ifndef MT_ROWS_STAGES
+#define MT_ROWS_STAGES 2
+#endif
 constexpr int kMultiItems = 4;
+constexpr int kMultiThreads = MT_ROWS_THREADS;
+
+template <class S>
+static constexpr int sub_of() {
+    return sizeof(S) == 2 ? MT_ROWS_SUB_HALF : MT_ROWS_SUB_WIDE;
+}
+
+template <class S>
+static cudaError_t launch_long(const SegArgs &a, int64_t tiles, const Launch &L) {
+#if MT_ROWS_KIND == 2
+    return launch_staged<S, OpAdd, kMultiItems, sub_of<S>(), kMultiThreads>(a, tiles, L);
+#elif MT_ROWS_KIND == 1
+    return launch_pipe<S, OpAdd, kMultiItems, MT_ROWS_STAGES, kMultiThreads>(a, tiles, L);
+#else
+    return launch_direct<S, OpAdd, kMultiItems, kMultiThreads>(a, tiles, L);
+#endif
+}
+
+// Virtual elements per tile of a long row.
+static int64_t long_tile_elems(int dtype) {
+#if MT_ROWS_KIND == 2
+    if (dtype == 0)
+        return Staged<float, OpAdd, kMultiItems, sub_of<float>(), kMultiThreads>::kTE;
+    return Staged<__half, OpAdd, kMultiItems, sub_of<__half>(), kMultiThreads>::kTE;
+#else
+    return (int64_t)kMultiThreads * kMultiItems * (dtype == 0 ? 4 : 8);
+#endif
+}
 
 RowPlan rows_plan(int dtype, int64_t n, bool heads_zero) {
     const int E = (dtype == 0) ? 4 : 8;
@@ -67,10 +95,10 @@ RowPlan rows_plan(int dtype, int64_t n, bool heads_zero) {
     for (int items = 1; items <= max_items; items *= 2) {
         const int64_t te = (int64_t)kThreads * items * E;
         if (head_max + n <= te)
-            return RowPlan{items, te, 1};
+            return RowPlan{false, items, te, 1};
     }
-    const int64_t te = (int64_t)kThreads * kMultiItems * E;
-    return RowPlan{kMultiItems, te, (head_max + n + te - 1) / te};
+    const int64_t te = long_tile_elems(dtype);
+    return RowPlan{true, kMultiItems, te, (head_max + n + te - 1) / te};
 }
 
 template <class S, int ITEMS>
@@ -91,32 +119,51 @@ static void launch_items(int items, const RowArgs &a, int64_t grid, cudaStream_t
 cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int dtype,
                         const RowPlan &p, bool inclusive, bool aligned_io, uint64_t *ws,
                         const Launch &L) {
+    if (p.staged) {
+        // One super-tile per row needs neither tile ordering nor look-back.
+        const bool chained = p.tiles_per_row > 1;
+        SegArgs a;
+        a.in = static_cast<const char *>(in);
+        a.out = static_cast<char *>(out);
+        a.nseg = rows;
+        a.n = n;
+        a.tpr = p.tiles_per_row;
+        a.n_dev = nullptr;
+        a.counter = chained ? reinterpret_cast<unsigned long long *>(ws) : nullptr;
+        a.inclusive = inclusive ? 1 : 0;
+        a.aligned_io = aligned_io ? 1 : 0;
+        a.lb.recs = chained ? ws + kHeaderSlots : nullptr;
+        a.lb.skip_tile = L.skip_tile;
+        a.lb.spin_limit = L.spin_limit;
+        const int64_t tiles = rows * p.tiles_per_row;
+        if (dtype == 0)
+            return launch_long<float>(a, tiles, L);
+        if (dtype == 1)
+            return launch_long<__nv_bfloat16>(a, tiles, L);
+        return launch_long<__half>(a, tiles, L);
+    }
     RowArgs a;
     a.in = static_cast<const char *>(in);
     a.out = static_cast<char *>(out);
     a.rows = rows;
     a.n = n;
-    a.tpr = p.tiles_per_row;
     a.inclusive = inclusive ? 1 : 0;
     a.aligned_io = aligned_io ? 1 : 0;
-    a.counter = reinterpret_cast<unsigned long long *>(ws);
-    a.lb.recs = (p.tiles_per_row > 1) ? ws + kHeaderSlots : nullptr;
-    a.lb.skip_tile = L.skip_tile;
-    a.lb.spin_limit = L.spin_limit;
-    const int64_t grid = rows * p.tiles_per_row;
     if (dtype == 0) {
         if (p.items == 8)
-            launch_one<float, 8>(a, grid, L.stream);
+            launch_one<float, 8>(a, rows, L.stream);
         else
-            launch_items<float>(p.items, a, grid, L.stream);
+            launch_items<float>(p.items, a, rows, L.stream);
     } else if (dtype == 1) {
-        launch_items<__nv_bfloat16>(p.items, a, grid, L.stream);
+        launch_items<__nv_bfloat16>(p.items, a, rows, L.stream);
     } else {
-        launch_items<__half>(p.items, a, grid, L.stream);
+        launch_items<__half>(p.items, a, rows, L.stream);
     }
     note_launch();
     return cudaGetLastError();
 }
+
+int rows_rec_slots() { return Status<float>::kSlots; }
 
 cudaError_t rows_take_error(int *code) {
     const int zero = 0;

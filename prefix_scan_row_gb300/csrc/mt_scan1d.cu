@@ -6,52 +6,50 @@
 // the identity of "Semantics > Common conventions > Identity value". The
 // page's realisation is a three-pass scan (tile reduce, scan of partials,
 // re-read and scan); here one persistent kernel reads every element once and
-// writes it once, chaining tiles with the decoupled look-back. The grid is
+// writes it once, chaining tiles with the decoupled look-back; tiles reach
+// shared memory by bulk copies a few tiles ahead (mt_pipe.cuh). The grid is
 // sized from the SM count and occupancy, not from n, so the host never needs
 // the live count.
-#include "mt_tilescan.cuh"
+#include "mt_staged.cuh"
 
 namespace mt {
 
-constexpr int kScanItems = 4;  // 16 KB of input per tile for every dtype
-
-struct ScanArgs {
-    const char *in;
-    char *out;
-    const int32_t *n_dev;
-    unsigned long long *counter;
-    int aligned_io;
-    LookBack lb;
-};
+#ifndef MT_SCAN1D_KIND
+#define MT_SCAN1D_KIND 2  // 0: direct loads, 1: bulk-copy ring, 2: staged super-tiles
+#endif
+#ifndef MT_SCAN1D_SUB
+#define MT_SCAN1D_SUB 3   // sub-tiles per staged super-tile
+#endif
+#ifndef MT_SCAN1D_ITEMS
+#define MT_SCAN1D_ITEMS 4
+#endif
+#ifndef MT_SCAN1D_THREADS
+#define MT_SCAN1D_THREADS 256
+#endif
+#ifndef MT_SCAN1D_STAGES
+#define MT_SCAN1D_STAGES 2
+#endif
+constexpr int kScanItems = MT_SCAN1D_ITEMS;      // 16-byte chunks per thread per tile
+constexpr int kScanThreads = MT_SCAN1D_THREADS;  // threads per CTA
 
 template <class S, class Op>
-__global__ void __launch_bounds__(kThreads) k_exclusive_scan(ScanArgs a) {
-    using T = TileScan<S, Op, kScanItems>;
-    __shared__ typename T::Smem sm;
-    constexpr int64_t s = sizeof(S);
-    const int32_t n32 = *a.n_dev;
-    const int64_t n = n32 > 0 ? n32 : 0;
-    const int64_t head = (int64_t)(((uintptr_t)a.in & 15u) / s);
-    const uint4 *vin = reinterpret_cast<const uint4 *>(a.in - head * s);
-    S *eout = reinterpret_cast<S *>(a.out) - head;
-    const int64_t hi = head + n;
-    const int64_t ntiles = n > 0 ? (hi + T::kTE - 1) / T::kTE : 0;
-    for (;;) {
-        if (threadIdx.x == 0)
-            sm.tile = atomicAdd(a.counter, 1ull);
-        __syncthreads();
-        const int64_t g = (int64_t)sm.tile;
-        if (g >= ntiles)
-            break;
-        // run() contains a block barrier before any thread can come back
-        // here and overwrite sm.tile.
-        T::run(vin, eout, a.aligned_io != 0, g * T::kTE, head, hi, false, a.lb, g, 0, sm);
-    }
+static cudaError_t launch_scan(const SegArgs &a, const Launch &L) {
+#if MT_SCAN1D_KIND == 2
+    return launch_staged<S, Op, kScanItems, MT_SCAN1D_SUB, kScanThreads>(a, 0, L);
+#elif MT_SCAN1D_KIND == 1
+    return launch_pipe<S, Op, kScanItems, MT_SCAN1D_STAGES, kScanThreads>(a, 0, L);
+#else
+    return launch_direct<S, Op, kScanItems, kScanThreads>(a, 0, L);
+#endif
 }
 
 template <class S>
 static constexpr int64_t tile_elems_of() {
-    return TileScan<S, OpAdd, kScanItems>::kTE;
+#if MT_SCAN1D_KIND == 2
+    return Staged<S, OpAdd, kScanItems, MT_SCAN1D_SUB, kScanThreads>::kTE;
+#else
+    return TileScan<S, OpAdd, kScanItems, kScanThreads>::kTE;
+#endif
 }
 
 int64_t scan1d_tile_elems(int dtype) {
@@ -67,39 +65,27 @@ int scan1d_rec_slots(int dtype) {
     return dtype == 4 ? Status<int64_t>::kSlots : Status<int32_t>::kSlots;
 }
 
-template <class S, class Op>
-static cudaError_t launch(const ScanArgs &a, const Launch &L) {
-    static int per_sm = 0;  // resident CTAs per SM for this instance
-    if (per_sm == 0) {
-        int b = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_exclusive_scan<S, Op>,
-                                                                      kThreads, 0);
-        if (e != cudaSuccess)
-            return e;
-        per_sm = b > 0 ? b : 1;
-    }
-    k_exclusive_scan<S, Op><<<(unsigned)(L.sm_count * per_sm), kThreads, 0, L.stream>>>(a);
-    note_launch();
-    return cudaGetLastError();
-}
-
 template <class S>
-static cudaError_t launch_op(int op, const ScanArgs &a, const Launch &L) {
+static cudaError_t launch_op(int op, const SegArgs &a, const Launch &L) {
     switch (op) {
-    case 0: return launch<S, OpAdd>(a, L);
-    case 1: return launch<S, OpMin>(a, L);
-    case 2: return launch<S, OpMax>(a, L);
+    case 0: return launch_scan<S, OpAdd>(a, L);
+    case 1: return launch_scan<S, OpMin>(a, L);
+    case 2: return launch_scan<S, OpMax>(a, L);
     default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t scan1d_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
                           int dtype, int op, bool aligned_io, const Launch &L) {
-    ScanArgs a;
+    SegArgs a;
     a.in = static_cast<const char *>(arr);
     a.out = static_cast<char *>(out);
+    a.nseg = 1;
+    a.n = 0;
+    a.tpr = 0;
     a.n_dev = n_dev;
     a.counter = reinterpret_cast<unsigned long long *>(scratch);
+    a.inclusive = 0;
     a.aligned_io = aligned_io ? 1 : 0;
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;

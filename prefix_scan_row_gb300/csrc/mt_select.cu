@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
 }
 
 int64_t select_tile_elems() { return kSelTE; }
+int select_rec_slots() { return Status<uint32_t>::kSlots; }
 
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                           uint64_t *scratch, const int32_t *n_dev, bool aligned, const Launch &L) {

@@ -7,57 +7,92 @@
 // the segment's valid range [lo, hi) are loaded (the aligned 16-byte chunk
 // around a valid element lies in the same page) but enter the scan as the
 // identity and are never stored.
+//
+// A tile is scanned in two phases: a load phase (from global memory, or from
+// a shared-memory stage filled by a bulk copy) into `raw` registers, and
+// scan_store(), which scans, obtains the tile prefix and stores the outputs.
 #pragma once
 
 #include "mt_lookback.cuh"
 
 namespace mt {
 
-template <class S, class Op, int ITEMS>
+struct NoHook {
+    __device__ __forceinline__ void operator()() const {}
+};
+
+template <class S, class Op, int ITEMS, int THREADS = kThreads>
 struct TileScan {
     using C = Codec<S>;
     using Acc = typename C::Acc;
     static constexpr int E = C::E;
-    static constexpr int kChunks = kThreads * ITEMS;
+    static constexpr int kNW = THREADS / 32;                // warps per CTA
+    static constexpr int kChunks = THREADS * ITEMS;
     static constexpr int64_t kTE = (int64_t)kChunks * E;  // virtual elements per tile
+    static_assert(THREADS % 32 == 0 && THREADS <= 1024, "block size");
 
     struct Smem {
-        Acc warp_tot[kWarps];
-        Acc prefix;
+        Acc warp_tot[2][kNW];  // double-buffered: consecutive tiles of a persistent CTA
+        Acc warp_pre[2][kNW];  // exclusive warp prefixes (more than 8 warps)
+        Acc agg[2];
+        Acc prefix[2];
         unsigned long long tile;
     };
 
-    __device__ __forceinline__ static int64_t chunk_v(int64_t t0, int j) {
+    // Index of chunk j of this thread inside the tile.
+    __device__ __forceinline__ static int chunk_of(int j) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        return t0 + (int64_t)(warp * 32 * ITEMS + j * 32 + lane) * E;
+        return warp * 32 * ITEMS + j * 32 + lane;
     }
 
-    // Scan the tile covering virtual [t0, t0 + kTE) of a segment.
-    //   vin       : 16-byte aligned address of virtual element 0 of the input
-    //   eout      : address of virtual element 0 of the output (element pointer)
-    //   aligned_io: eout is 16-byte aligned too (same phase as the input)
-    //   [lo, hi)  : valid virtual range of the segment
-    //   tile/first: global tile id and the id of the segment's first tile
-    __device__ __forceinline__ static void run(const uint4 *vin, S *eout, bool aligned_io, int64_t t0,
-                                               int64_t lo, int64_t hi, bool inclusive,
-                                               const LookBack &lb, int64_t tile, int64_t first,
-                                               Smem &sm) {
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        const Acc ident = Op::template identity<Acc>();
-
-        // 1. Issue every load of the tile before using any of them.
-        uint4 raw[ITEMS];
+    // Loads straight from global memory; every load is issued before any is used.
+    __device__ __forceinline__ static void load_global(const uint4 *vin, int64_t t0, int64_t lo,
+                                                       int64_t hi, uint4 (&raw)[ITEMS]) {
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
-            const int64_t v = chunk_v(t0, j);
+            const int64_t v = t0 + (int64_t)chunk_of(j) * E;
             raw[j] = make_uint4(0u, 0u, 0u, 0u);
             if (v < hi && v + E > lo)
                 raw[j] = ld_stream(vin + v / E);
         }
+    }
+
+    // Loads from a shared-memory stage holding the tile's chunks in order
+    // (chunk c at stage[c]); conflict-free (consecutive lanes, consecutive 16 B).
+    __device__ __forceinline__ static void load_stage(const uint4 *stage, int64_t t0, int64_t lo,
+                                                      int64_t hi, uint4 (&raw)[ITEMS]) {
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) {
+            const int c = chunk_of(j);
+            const int64_t v = t0 + (int64_t)c * E;
+            raw[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (v < hi && v + E > lo)
+                raw[j] = stage[c];
+        }
+    }
+
+    // Scan the tile covering virtual [t0, t0 + kTE) of a segment and store it.
+    //   eout      : address of virtual element 0 of the output (element pointer)
+    //   aligned_io: eout is 16-byte aligned (same phase as the input)
+    //   [lo, hi)  : valid virtual range of the segment
+    //   tile/first: global tile id and the id of the segment's first tile
+    //   buf       : which half of the double-buffered shared state to use
+    //   hook      : run by every thread right after the block barrier that
+    //               follows the last read of `raw`'s source (a stage may be
+    //               refilled from there on)
+    template <class Hook>
+    __device__ __forceinline__ static void scan_store(uint4 (&raw)[ITEMS], S *eout, bool aligned_io,
+                                                      int64_t t0, int64_t lo, int64_t hi,
+                                                      bool inclusive, const LookBack &lb,
+                                                      int64_t tile, int64_t first, Smem &sm, int buf,
+                                                      const Hook &hook) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const Acc ident = Op::template identity<Acc>();
+
         Acc x[ITEMS][E];
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
-            const int64_t v = chunk_v(t0, j);
+            const int64_t v = t0 + (int64_t)chunk_of(j) * E;
             C::unpack(raw[j], x[j]);
             if (!(v >= lo && v + E <= hi)) {
 #pragma unroll
@@ -67,7 +102,7 @@ struct TileScan {
             }
         }
 
-        // 2. Inclusive scan of each chunk in registers.
+        // Inclusive scan of each chunk in registers.
         Acc inc[ITEMS];
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
@@ -77,7 +112,7 @@ struct TileScan {
             inc[j] = x[j][E - 1];
         }
 
-        // 3. Inclusive warp scans of the chunk totals (one per j, interleaved).
+        // Inclusive warp scans of the chunk totals (one per j, interleaved).
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
 #pragma unroll
@@ -88,7 +123,7 @@ struct TileScan {
             }
         }
 
-        // 4. Prefix of each chunk inside the warp's run; the warp total.
+        // Prefix of each chunk inside the warp's run; the warp total.
         Acc pre[ITEMS];
         Acc run = ident;
 #pragma unroll
@@ -100,26 +135,50 @@ struct TileScan {
             run = Op::apply(run, __shfl_sync(kFull, inc[j], 31));
         }
         if (lane == 0)
-            sm.warp_tot[warp] = run;
+            sm.warp_tot[buf][warp] = run;
         __syncthreads();
+        hook();
 
-        // 5. Block: this warp's exclusive prefix and the tile aggregate.
+        // Block: this warp's exclusive prefix and the tile aggregate.
         Acc wpre = ident, agg = ident;
+        if constexpr (kNW <= 8) {
+            // few warps: every thread folds the warp totals itself
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const Acc t = sm.warp_tot[w];
-            if (w < warp)
-                wpre = Op::apply(wpre, t);
-            agg = Op::apply(agg, t);
+            for (int w = 0; w < kNW; ++w) {
+                const Acc t = sm.warp_tot[buf][w];
+                if (w < warp)
+                    wpre = Op::apply(wpre, t);
+                agg = Op::apply(agg, t);
+            }
+        } else {
+            // many warps: warp 0 scans the totals, one more barrier
+            if (warp == 0) {
+                Acc t = lane < kNW ? sm.warp_tot[buf][lane] : ident;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const Acc y = __shfl_up_sync(kFull, t, d);
+                    if (lane >= d)
+                        t = Op::apply(y, t);
+                }
+                Acc e = __shfl_up_sync(kFull, t, 1);
+                if (lane == 0)
+                    e = ident;
+                if (lane < kNW)
+                    sm.warp_pre[buf][lane] = e;
+                if (lane == 31)
+                    sm.agg[buf] = t;
+            }
+            __syncthreads();
+            wpre = sm.warp_pre[buf][warp];
+            agg = sm.agg[buf];
         }
 
-        // 6. Tile prefix from the look-back (identity for a segment's first tile).
-        const Acc tp = tile_prefix<Acc, Op>(lb, tile, first, agg, &sm.prefix);
+        // Tile prefix from the look-back (identity for a segment's first tile).
+        const Acc tp = tile_prefix<Acc, Op>(lb, tile, first, agg, &sm.prefix[buf]);
         const Acc base0 = Op::apply(tp, wpre);
 
-        // 7. Outputs: inclusive base + s_k, or exclusive base + s_{k-1} with
-        //    base itself at k = 0 (the one-slot shift of scan.rs's exclusive
-        //    kernel).
+        // Outputs: inclusive base + s_k, or exclusive base + s_{k-1} with base
+        // itself at k = 0 (the one-slot shift of scan.rs's exclusive kernel).
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
             const Acc base = Op::apply(base0, pre[j]);
@@ -133,7 +192,7 @@ struct TileScan {
                     x[j][k] = Op::apply(base, x[j][k - 1]);
                 x[j][0] = base;
             }
-            const int64_t v = chunk_v(t0, j);
+            const int64_t v = t0 + (int64_t)chunk_of(j) * E;
             if (aligned_io && v >= lo && v + E <= hi) {
                 st_v4(reinterpret_cast<uint4 *>(eout) + v / E, C::pack(x[j]));
             } else if (v < hi && v + E > lo) {
@@ -143,6 +202,16 @@ struct TileScan {
                         C::store1(eout + v + k, x[j][k]);
             }
         }
+    }
+
+    // One tile read straight from global memory (single-tile rows).
+    __device__ __forceinline__ static void run(const uint4 *vin, S *eout, bool aligned_io, int64_t t0,
+                                               int64_t lo, int64_t hi, bool inclusive,
+                                               const LookBack &lb, int64_t tile, int64_t first,
+                                               Smem &sm) {
+        uint4 raw[ITEMS];
+        load_global(vin, t0, lo, hi, raw);
+        scan_store(raw, eout, aligned_io, t0, lo, hi, inclusive, lb, tile, first, sm, 0, NoHook());
     }
 };
 
