@@ -25,6 +25,7 @@ struct RowPlan {
     int items;               // 16-byte chunks per thread
     int64_t tile_elems;      // virtual elements per tile
     int64_t tiles_per_row;   // 1: no look-back (and no workspace)
+    int warps;               // single-tile rows: warps per CTA
 };
 RowPlan rows_plan(int dtype, int64_t n, bool heads_zero);
 cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int dtype,

@@ -23,10 +23,11 @@ struct RowArgs {
     int aligned_io;  // output rows have the input rows' 16-byte phase
 };
 
-// One CTA per row; the whole row is one tile.
+// One CTA per row; the whole row is one tile of blockDim.x * ITEMS chunks
+// (the block size is chosen per row length, up to 16 warps).
 template <class S, int ITEMS>
-__global__ void __launch_bounds__(kThreads) k_scan_rows(RowArgs a) {
-    using T = TileScan<S, OpAdd, ITEMS>;
+__global__ void __launch_bounds__(512) k_scan_rows(RowArgs a) {
+    using T = TileScan<S, OpAdd, ITEMS, 0>;
     __shared__ typename T::Smem sm;
     const int64_t row = blockIdx.x;
     if (row >= a.rows)
@@ -40,9 +41,6 @@ __global__ void __launch_bounds__(kThreads) k_scan_rows(RowArgs a) {
     T::run(vin, eout, a.aligned_io != 0, 0, head, head + a.n, a.inclusive != 0, none, row, row, sm);
 }
 
-// Chunks per thread tried for rows that fit in one tile; longer rows use
-// kMultiItems per tile (16 KB of input per tile) and kRowStages tiles in
-// flight per CTA.
 #ifndef MT_ROWS_KIND
 #define MT_ROWS_KIND 2  // long rows: 0 direct loads, 1 bulk-copy ring, 2 staged super-tiles
 #endif
@@ -88,30 +86,47 @@ static int64_t long_tile_elems(int dtype) {
 #endif
 }
 
+// Single-tile rows: the (warps, chunks per thread) pair that covers the row
+// with the least idle chunks, at most 16 warps and 4 chunks per thread (8 for
+// f32); ties go to more chunks per thread. Longer rows take the staged path.
 RowPlan rows_plan(int dtype, int64_t n, bool heads_zero) {
     const int E = (dtype == 0) ? 4 : 8;
     const int64_t head_max = heads_zero ? 0 : E - 1;
+    const int64_t chunks = (head_max + n + E - 1) / E;
     const int max_items = (dtype == 0) ? 8 : 4;
-    for (int items = 1; items <= max_items; items *= 2) {
-        const int64_t te = (int64_t)kThreads * items * E;
-        if (head_max + n <= te)
-            return RowPlan{false, items, te, 1};
+    int best_items = 0, best_warps = 0;
+    int64_t best_waste = -1;
+    for (int items = 1; items <= max_items; ++items) {
+        if (items > 4 && items != 8)
+            continue;
+        const int64_t warps = (chunks + 32 * items - 1) / (32 * items);
+        if (warps > 16)
+            continue;
+        const int64_t waste = warps * 32 * items - chunks;
+        if (best_waste < 0 || waste <= best_waste) {
+            best_waste = waste;
+            best_items = items;
+            best_warps = (int)warps;
+        }
     }
+    if (best_items > 0)
+        return RowPlan{false, best_items, (int64_t)best_warps * 32 * best_items * E, 1, best_warps};
     const int64_t te = long_tile_elems(dtype);
-    return RowPlan{true, kMultiItems, te, (head_max + n + te - 1) / te};
+    return RowPlan{true, kMultiItems, te, (head_max + n + te - 1) / te, 0};
 }
 
 template <class S, int ITEMS>
-static void launch_one(const RowArgs &a, int64_t grid, cudaStream_t st) {
-    k_scan_rows<S, ITEMS><<<(unsigned)grid, kThreads, 0, st>>>(a);
+static void launch_one(const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
+    k_scan_rows<S, ITEMS><<<(unsigned)grid, 32 * warps, 0, st>>>(a);
 }
 
 template <class S>
-static void launch_items(int items, const RowArgs &a, int64_t grid, cudaStream_t st) {
+static void launch_items(int items, const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
     switch (items) {
-    case 1: launch_one<S, 1>(a, grid, st); break;
-    case 2: launch_one<S, 2>(a, grid, st); break;
-    case 4: launch_one<S, 4>(a, grid, st); break;
+    case 1: launch_one<S, 1>(a, grid, warps, st); break;
+    case 2: launch_one<S, 2>(a, grid, warps, st); break;
+    case 3: launch_one<S, 3>(a, grid, warps, st); break;
+    case 4: launch_one<S, 4>(a, grid, warps, st); break;
     default: break;
     }
 }
@@ -151,13 +166,13 @@ cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int 
     a.aligned_io = aligned_io ? 1 : 0;
     if (dtype == 0) {
         if (p.items == 8)
-            launch_one<float, 8>(a, rows, L.stream);
+            launch_one<float, 8>(a, rows, p.warps, L.stream);
         else
-            launch_items<float>(p.items, a, rows, L.stream);
+            launch_items<float>(p.items, a, rows, p.warps, L.stream);
     } else if (dtype == 1) {
-        launch_items<__nv_bfloat16>(p.items, a, rows, L.stream);
+        launch_items<__nv_bfloat16>(p.items, a, rows, p.warps, L.stream);
     } else {
-        launch_items<__half>(p.items, a, rows, L.stream);
+        launch_items<__half>(p.items, a, rows, p.warps, L.stream);
     }
     note_launch();
     return cudaGetLastError();

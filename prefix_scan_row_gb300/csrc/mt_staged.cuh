@@ -71,67 +71,71 @@ struct Staged {
         }
     }
 
-    // The super-tile's aggregate (valid in thread 0). Adds may be grouped
-    // freely (exact for integers, a rounding difference for floats); min/max
-    // combine in element order so that ties keep the earliest element.
+    // The super-tile's aggregate (valid in thread 0). Any grouping gives the
+    // same result for adds of integers, for integer min/max, and for float
+    // min/max unless the result is a zero (which of +0/-0 comes first then
+    // matters): those take the quick unordered reduction, and a float min/max
+    // whose quick result is zero is redone in element order. Float adds take
+    // the quick one too (only rounding differs, within the stated tolerance).
     __device__ __forceinline__ static Acc reduce(Smem &sm, int64_t t0, int64_t lo, int64_t hi) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const Acc ident = Op::template identity<Acc>();
-        if constexpr (std::is_same<Op, OpAdd>::value) {
-            Acc acc = ident;
+        Acc acc = ident;
 #pragma unroll 1
-            for (int sub = 0; sub < SUB; ++sub) {
+        for (int sub = 0; sub < SUB; ++sub) {
 #pragma unroll
-                for (int j = 0; j < ITEMS; ++j) {
-                    Acc x[E];
-                    load_chunk(sm, chunk_of(sub, j), t0, lo, hi, x);
+            for (int j = 0; j < ITEMS; ++j) {
+                Acc x[E];
+                load_chunk(sm, chunk_of(sub, j), t0, lo, hi, x);
 #pragma unroll
-                    for (int k = 0; k < E; ++k)
-                        acc = Op::apply(acc, x[k]);
-                }
+                for (int k = 0; k < E; ++k)
+                    acc = Op::apply(acc, x[k]);
             }
+        }
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1)
-                acc = Op::apply(acc, __shfl_xor_sync(kFull, acc, d));
-            if (lane == 0)
-                sm.red[0][warp] = acc;
-            __syncthreads();
-            Acc agg = ident;
-            if (threadIdx.x == 0)
-                for (int w = 0; w < kNW; ++w)
-                    agg = Op::apply(agg, sm.red[0][w]);
-            return agg;
-        } else {
+        for (int d = 16; d > 0; d >>= 1)
+            acc = Op::apply(acc, __shfl_xor_sync(kFull, acc, d));
+        if (lane == 0)
+            sm.red[0][warp] = acc;
+        __syncthreads();
+        Acc agg = ident;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w)
+            agg = Op::apply(agg, sm.red[0][w]);
+        constexpr bool kOrderFree = std::is_same<Op, OpAdd>::value || !std::is_same<Acc, float>::value;
+        if constexpr (!kOrderFree) {
+            if (agg == Acc(0)) {  // block-uniform: every thread folded the same totals
+                __syncthreads();  // all reads of sm.red are done
 #pragma unroll 1
-            for (int sub = 0; sub < SUB; ++sub) {
-                Acc r = ident;
+                for (int sub = 0; sub < SUB; ++sub) {
+                    Acc r = ident;
 #pragma unroll
-                for (int j = 0; j < ITEMS; ++j) {
-                    Acc x[E];
-                    load_chunk(sm, chunk_of(sub, j), t0, lo, hi, x);
-                    Acc c = x[0];
+                    for (int j = 0; j < ITEMS; ++j) {
+                        Acc x[E];
+                        load_chunk(sm, chunk_of(sub, j), t0, lo, hi, x);
+                        Acc c = x[0];
 #pragma unroll
-                    for (int k = 1; k < E; ++k)
-                        c = Op::apply(c, x[k]);
+                        for (int k = 1; k < E; ++k)
+                            c = Op::apply(c, x[k]);
 #pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {  // lane order: lower lanes are earlier
-                        const Acc o = __shfl_down_sync(kFull, c, d);
-                        if (lane + d < 32)
-                            c = Op::apply(c, o);
+                        for (int d = 1; d < 32; d <<= 1) {  // lane order: lower lanes are earlier
+                            const Acc o = __shfl_down_sync(kFull, c, d);
+                            if (lane + d < 32)
+                                c = Op::apply(c, o);
+                        }
+                        r = Op::apply(r, c);
                     }
-                    r = Op::apply(r, c);
+                    if (lane == 0)
+                        sm.red[sub][warp] = r;
                 }
-                if (lane == 0)
-                    sm.red[sub][warp] = r;
-            }
-            __syncthreads();
-            Acc agg = ident;
-            if (threadIdx.x == 0)
+                __syncthreads();
+                agg = ident;
                 for (int sub = 0; sub < SUB; ++sub)
                     for (int w = 0; w < kNW; ++w)
                         agg = Op::apply(agg, sm.red[sub][w]);
-            return agg;
+            }
         }
+        return agg;
     }
 
     __device__ __forceinline__ static uint4 *plane(Smem &sm, int p, int c) {

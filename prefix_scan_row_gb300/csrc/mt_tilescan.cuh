@@ -21,12 +21,15 @@ struct NoHook {
     __device__ __forceinline__ void operator()() const {}
 };
 
+// THREADS == 0: the block size is taken from blockDim at run time (at most
+// 16 warps); kChunks and kTE are then not meaningful.
 template <class S, class Op, int ITEMS, int THREADS = kThreads>
 struct TileScan {
     using C = Codec<S>;
     using Acc = typename C::Acc;
     static constexpr int E = C::E;
-    static constexpr int kNW = THREADS / 32;                // warps per CTA
+    static constexpr bool kDyn = THREADS == 0;
+    static constexpr int kNW = kDyn ? 16 : THREADS / 32;    // warps per CTA (the maximum when dynamic)
     static constexpr int kChunks = THREADS * ITEMS;
     static constexpr int64_t kTE = (int64_t)kChunks * E;  // virtual elements per tile
     static_assert(THREADS % 32 == 0 && THREADS <= 1024, "block size");
@@ -141,7 +144,15 @@ struct TileScan {
 
         // Block: this warp's exclusive prefix and the tile aggregate.
         Acc wpre = ident, agg = ident;
-        if constexpr (kNW <= 8) {
+        if constexpr (kDyn) {
+            const int nw = blockDim.x >> 5;
+            for (int w = 0; w < nw; ++w) {
+                const Acc t = sm.warp_tot[buf][w];
+                if (w < warp)
+                    wpre = Op::apply(wpre, t);
+                agg = Op::apply(agg, t);
+            }
+        } else if constexpr (kNW <= 8) {
             // few warps: every thread folds the warp totals itself
 #pragma unroll
             for (int w = 0; w < kNW; ++w) {

@@ -139,3 +139,19 @@ def test_scan_full_size(mt, dtype):
         assert mt.mt_scan_status() == 0
         assert torch.all(out[n:] == SENTINEL[dtype]).item()
         assert_scan_matches(out, arr_cpu, n, dtype, op)
+
+
+@pytest.mark.parametrize("op", ["min", "max"])
+def test_scan_f32_signed_zeros_bit_exact(mt, op):
+    """Both zeros present: which one a min/max keeps depends on element order
+    (the earlier one wins), so tiles whose extreme is a zero must combine in
+    order. Bit-exact against the oracle."""
+    n = 300001
+    u = workloads.uniform((n,), 21, 0.0, 1.0, "f32")
+    arr = u if op == "min" else -u
+    g = torch.Generator().manual_seed(22)
+    pos = torch.randperm(n, generator=g)[:400]
+    arr[pos[:200]] = 0.0
+    arr[pos[200:]] = -0.0
+    out = run_scan(mt, arr, n, "f32", op)
+    assert_scan_matches(out, arr, n, "f32", op)
