@@ -77,7 +77,7 @@ typedef enum {
  *
  * Rows longer than one tile are split across CTAs that chain their carries
  * with a single-pass decoupled look-back. Those calls take a small status
- * workspace (32 bytes per tile of 12288 f32 / 16384 bf16 elements, plus 32
+ * workspace (128 bytes per tile of 12288 f32 / 16384 bf16 elements, plus 32
  * bytes) from a stream-ordered memory
  * pool owned by the library (cudaMallocFromPoolAsync / cudaFreeAsync on
  * `stream`); rows that fit in one tile use none.
@@ -186,7 +186,7 @@ int mt_scan_debug_lookback(int64_t skip_publish_tile, uint32_t spin_limit);
  * Arguments, results and the other errors are those of mt_scan_rows.
  * Limit: the array holds MT_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that
  * loads the library, for the life of the process, which covers
- * rows * tiles_per_row <= 32767 tiles (a tile is 12288 f32 or 16384
+ * rows * tiles_per_row <= 8191 tiles (a tile is 12288 f32 or 16384
  * bf16/f16 elements of a row; rows of at most 8192 elements use no tiles of
  * it). A larger call returns MT_ERR_TOO_LARGE and launches nothing.
  * The first call on each device looks up the array's device address (a

@@ -22,8 +22,8 @@
 namespace mt {
 
 #ifndef MT_REC_SLOTS
-#define MT_REC_SLOTS 4  // 8-byte slots per record: one 32-byte sector each, so the
-                        // records near the look-back front spread over L2 slices
+#define MT_REC_SLOTS 16  // 8-byte slots per record: one 128-byte line each, so the
+                         // records near the look-back front spread over L2 slices
 #endif
 #if MT_REC_SLOTS < 3
 #error "a record needs at least three 8-byte slots for 8-byte values"

@@ -10,11 +10,23 @@
 // selected words in shared memory and writes them out as one contiguous run.
 // A value word is only read when one of its four flags is set, so sparse
 // flags skip most of the value bytes.
-#include "mt_tilescan.cuh"
+//
+// When flags and values are 16-byte aligned, k_select_staged instead brings
+// each tile's flags and values into shared memory with two bulk copies and
+// publishes the tile's count as soon as they land. Each warp then packs its
+// selected words in place at the start of its own range of the tile, walking
+// its elements 32 at a time (lane i reads element i of each step, a ballot
+// ranks the selected lanes, so the writes are consecutive: no bank
+// conflicts). The look-back comes last, then each warp copies its packed run
+// out with coalesced stores. k_select serves the other alignments.
+#include "mt_pipe.cuh"
 
 namespace mt {
 
-constexpr int kSelItems = 2;                          // flag chunks (16 flags) per thread
+#ifndef MT_SEL_ITEMS
+#define MT_SEL_ITEMS 2
+#endif
+constexpr int kSelItems = MT_SEL_ITEMS;  // flag chunks (16 flags) per thread
 constexpr int kSelChunks = kThreads * kSelItems;
 constexpr int64_t kSelTE = (int64_t)kSelChunks * 16;  // elements per tile (8192)
 
@@ -174,12 +186,158 @@ __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
     }
 }
 
+// ---- staged variant (16-byte aligned flags and values) ----------------------
+struct SelStagedSmem {
+    uint4 flags[kSelChunks];  // 16 flags per chunk
+    uint32_t vals[kSelTE];    // the tile's values; each warp packs its selected ones in place
+    uint64_t bar;
+    int64_t tile;
+    uint32_t red[kWarps];
+    uint32_t prefix;
+};
+
+__global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    SelStagedSmem &sm = *reinterpret_cast<SelStagedSmem *>(dsm);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t n32 = *a.n_dev;
+    const int64_t n = n32 > 0 ? n32 : 0;
+    const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    uint32_t phase = 0;
+    for (;;) {
+        if (threadIdx.x == 0)
+            sm.tile = (int64_t)atomicAdd(a.counter, 1ull);
+        __syncthreads();  // tile id visible; everyone is done with the last tile
+        const int64_t g = sm.tile;
+        if (g >= ntiles)
+            break;
+        const int64_t t0 = g * kSelTE;
+        const int64_t elems = (n - t0 < kSelTE) ? n - t0 : kSelTE;
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            const uint32_t fb = (uint32_t)((elems + 15) / 16 * 16);
+            const uint32_t vb = (uint32_t)((elems * 4 + 15) / 16 * 16);
+            mbar_arrive_expect_tx(&sm.bar, fb + vb);
+            bulk_g2s(&sm.flags[0], a.flags + t0, fb, &sm.bar);
+            bulk_g2s(&sm.vals[0], a.arr + t0, vb, &sm.bar);
+        }
+        const bool ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0)
+                atomicCAS(&g_mt_err, 0, kErrTimeout);
+            mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copies before leaving
+            return;
+        }
+        phase ^= 1u;
+
+        // Count: popcounts of this thread's 16-flag chunks (flags past n are 0).
+        uint32_t mine = 0u;
+#pragma unroll
+        for (int j = 0; j < kSelItems; ++j) {
+            const int c = warp * 32 * kSelItems + j * 32 + lane;
+            const int64_t valid = elems - (int64_t)c * 16;
+            if (valid > 0) {
+                uint4 f = sm.flags[c];
+                f.x = keep_low_bytes(f.x, valid);
+                f.y = keep_low_bytes(f.y, valid - 4);
+                f.z = keep_low_bytes(f.z, valid - 8);
+                f.w = keep_low_bytes(f.w, valid - 12);
+                mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
+            }
+        }
+        // The tile's count, published as soon as the flags are in.
+        uint32_t wsum = mine;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1)
+            wsum += __shfl_xor_sync(kFull, wsum, d);
+        if (lane == 0)
+            sm.red[warp] = wsum;
+        __syncthreads();
+        uint32_t agg = 0u, wpre = 0u;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t t = sm.red[w];
+            if (w < warp)
+                wpre += t;
+            agg += t;
+        }
+        publish_aggregate<uint32_t, OpAdd>(a.lb, g, 0, agg);
+
+        // Pack this warp's selected words in place, in element order. A write
+        // goes to a slot at or before every element this warp reads later, and
+        // a warp step reads all its lanes before any of them writes.
+        const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
+        const int wstart = warp * 32 * kSelItems * 16;
+        const unsigned lt = (1u << lane) - 1u;
+        uint32_t cnt = 0u;
+#pragma unroll
+        for (int step = 0; step < kSelItems * 16; ++step) {
+            const int e = wstart + step * 32 + lane;
+            const bool sel = (e < elems) && fb[e] != 0;
+            const unsigned bal = __ballot_sync(kFull, sel);
+            const uint32_t val = sm.vals[e];
+            if (sel)
+                sm.vals[wstart + cnt + __popc(bal & lt)] = val;
+            cnt += __popc(bal);
+        }
+        __syncwarp();
+        const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
+        uint32_t *dst = a.out + G + wpre;
+        for (uint32_t i = lane; i < cnt; i += 32)
+            dst[i] = sm.vals[wstart + i];
+        if (g == ntiles - 1 && threadIdx.x == 0)
+            *a.num_out = (int32_t)(G + agg);
+    }
+}
+
 int64_t select_tile_elems() { return kSelTE; }
 int select_rec_slots() { return Status<uint32_t>::kSlots; }
+
+static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
+    static int per_sm[128] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 128)
+        return cudaErrorInvalidDevice;
+    const int bytes = (int)sizeof(SelStagedSmem);
+    if (per_sm[dev] == 0) {
+        e = cudaFuncSetAttribute(k_select_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess)
+            return e;
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_staged, kThreads, bytes);
+        if (e != cudaSuccess)
+            return e;
+        per_sm[dev] = b > 0 ? b : 1;
+    }
+    k_select_staged<<<(unsigned)(L.sm_count * per_sm[dev]), kThreads, bytes, L.stream>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                           uint64_t *scratch, const int32_t *n_dev, bool aligned, const Launch &L) {
     static int per_sm = 0;
+    if (aligned) {
+        SelArgs a;
+        a.arr = static_cast<const uint32_t *>(arr);
+        a.flags = flags;
+        a.out = static_cast<uint32_t *>(out);
+        a.num_out = num_out;
+        a.n_dev = n_dev;
+        a.counter = reinterpret_cast<unsigned long long *>(scratch);
+        a.aligned = 1;
+        a.lb.recs = scratch + kHeaderSlots;
+        a.lb.skip_tile = L.skip_tile;
+        a.lb.spin_limit = L.spin_limit;
+        return launch_staged_select(a, L);
+    }
     if (per_sm == 0) {
         int b = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select, kThreads, 0);

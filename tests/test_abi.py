@@ -99,17 +99,17 @@ def test_scratch_slots(lib):
     assert f(-1, I32, 1) == -1
     assert f(10, BF16, 1) == -1
     assert f(10, I32, 7) == -1
-    # 12288 elements per super-tile for 4-byte types; every record is four
-    # 8-byte slots (one 32-byte sector); up to three elements of head misalignment
-    assert f(12288, I32, 1) == 4 + 4 * 2
-    assert f(12285, F32, 1) == 4 + 4 * 1
-    assert f(1 << 28, I32, 1) == 4 + 4 * 21846
+    # 12288 elements per super-tile for 4-byte types; every record is sixteen
+    # 8-byte slots (one 128-byte line); up to three elements of head misalignment
+    assert f(12288, I32, 1) == 4 + 16 * 2
+    assert f(12285, F32, 1) == 4 + 16 * 1
+    assert f(1 << 28, I32, 1) == 4 + 16 * 21846
     # 6144 elements per super-tile for i64
-    assert f(6144, I64, 1) == 4 + 4 * 2
-    assert f(6143, I64, 1) == 4 + 4 * 1
+    assert f(6144, I64, 1) == 4 + 16 * 2
+    assert f(6143, I64, 1) == 4 + 16 * 1
     # select: 8192 flags per tile
-    assert f(1 << 28, I32, 2) == 4 + 4 * (1 << 15)
-    assert f(1, I32, 2) == 4 + 4 * 1
+    assert f(1 << 28, I32, 2) == 4 + 16 * (1 << 15)
+    assert f(1, I32, 2) == 4 + 16 * 1
 
 
 def test_strerror_and_counter(lib):

@@ -36,10 +36,10 @@ def test_noalloc_refuses_too_large_before_launching():
     """Host-side check only: fake, aligned pointers are never touched."""
     L = _lib()
     f32 = 0
-    # rows of 32767 tiles of 12288 f32 elements fit (4 header words plus four
+    # rows of 8191 tiles of 12288 f32 elements fit (4 header words plus sixteen
     # words per tile); one tile more does not
-    assert L.mt_scan_rows_noalloc(0x10000, 0x20000, 1, 32768 * 12288, f32, 1, None) == -7
-    assert L.mt_scan_rows_noalloc(0x10000, 0x20000, 2, 16400 * 12288, f32, 0, None) == -7
+    assert L.mt_scan_rows_noalloc(0x10000, 0x20000, 1, 8192 * 12288, f32, 1, None) == -7
+    assert L.mt_scan_rows_noalloc(0x10000, 0x20000, 2, 4100 * 12288, f32, 0, None) == -7
     assert L.mt_scan_rows_noalloc(0x10000, 0x20000, -1, 5, f32, 1, None) == -1
     assert L.mt_scan_rows_noalloc(0x10000, 0x20000, 0, 5, f32, 1, None) == 0
 
