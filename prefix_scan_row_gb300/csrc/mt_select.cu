@@ -310,6 +310,10 @@ static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
         e = cudaFuncSetAttribute(k_select_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
+        e = cudaFuncSetAttribute(k_select_staged, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
         int b = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_staged, kThreads, bytes);
         if (e != cudaSuccess)

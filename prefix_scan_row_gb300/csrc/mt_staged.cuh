@@ -24,18 +24,26 @@
 
 namespace mt {
 
-template <class S, class Op, int ITEMS, int SUB, int THREADS>
+#ifndef MT_STAGED_EARLY_LOOKBACK
+#define MT_STAGED_EARLY_LOOKBACK 0  // 1: look back before the scan (one scan+store pass)
+#endif
+
+// A thread's group = V adjacent 16-byte chunks (V * E contiguous elements),
+// scanned serially before the warp scan; V > 1 cuts the warp-scan work per
+// element for wide element types.
+template <class S, class Op, int ITEMS, int SUB, int THREADS, int V = 1>
 struct Staged {
-    using T = TileScan<S, Op, ITEMS, THREADS>;
     using C = Codec<S>;
     using Acc = typename C::Acc;
     static constexpr int E = C::E;
+    static constexpr int EG = E * V;                            // elements per group
     static constexpr int kNW = THREADS / 32;
-    static constexpr int kSubChunks = THREADS * ITEMS;          // chunks per sub-tile
+    static constexpr int kSubGroups = THREADS * ITEMS;          // groups per sub-tile
+    static constexpr int kSubChunks = kSubGroups * V;           // chunks per sub-tile
     static constexpr int kChunks = SUB * kSubChunks;            // chunks per super-tile
     static constexpr int64_t kTE = (int64_t)kChunks * E;        // virtual elements per super-tile
     // local prefixes of one chunk, in 16-byte planes: 1 when Acc is as wide as S
-    static constexpr int kPlanes = (E * (int)sizeof(Acc) + 15) / 16;
+    static constexpr int kPlanes = MT_STAGED_EARLY_LOOKBACK ? 1 : (E * (int)sizeof(Acc) + 15) / 16;
     static constexpr int kPerPlane = 16 / (int)sizeof(Acc);     // Acc values per plane
 
     struct Smem {
@@ -49,23 +57,33 @@ struct Staged {
     };
     static constexpr size_t kSmemBytes = sizeof(Smem);
 
+    // Group index of this thread's j-th group of sub-tile `sub`; its chunks
+    // are group * V ... group * V + V - 1.
     __device__ __forceinline__ static int chunk_of(int sub, int j) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        return sub * kSubChunks + warp * 32 * ITEMS + j * 32 + lane;
+        return sub * kSubGroups + warp * 32 * ITEMS + j * 32 + lane;
     }
-    // Chunk c of the staged input, widened, with elements outside [lo, hi)
+    // Group gi of the staged input, widened, with elements outside [lo, hi)
     // replaced by the identity.
-    __device__ __forceinline__ static void load_chunk(const Smem &sm, int c, int64_t t0, int64_t lo,
-                                                      int64_t hi, Acc (&x)[E]) {
+    __device__ __forceinline__ static void load_chunk(const Smem &sm, int gi, int64_t t0, int64_t lo,
+                                                      int64_t hi, Acc (&x)[EG]) {
         const Acc ident = Op::template identity<Acc>();
-        const int64_t v = t0 + (int64_t)c * E;
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (v < hi && v + E > lo)
-            raw = sm.stage[c];
-        C::unpack(raw, x);
-        if (!(v >= lo && v + E <= hi)) {
+        const int64_t v = t0 + (int64_t)gi * EG;
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+            const int64_t vq = v + q * E;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (vq < hi && vq + E > lo)
+                raw = sm.stage[gi * V + q];
+            Acc part[E];
+            C::unpack(raw, part);
 #pragma unroll
             for (int k = 0; k < E; ++k)
+                x[q * E + k] = part[k];
+        }
+        if (!(v >= lo && v + EG <= hi)) {
+#pragma unroll
+            for (int k = 0; k < EG; ++k)
                 if (v + k < lo || v + k >= hi)
                     x[k] = ident;
         }
@@ -85,10 +103,10 @@ struct Staged {
         for (int sub = 0; sub < SUB; ++sub) {
 #pragma unroll
             for (int j = 0; j < ITEMS; ++j) {
-                Acc x[E];
+                Acc x[EG];
                 load_chunk(sm, chunk_of(sub, j), t0, lo, hi, x);
 #pragma unroll
-                for (int k = 0; k < E; ++k)
+                for (int k = 0; k < EG; ++k)
                     acc = Op::apply(acc, x[k]);
             }
         }
@@ -111,11 +129,11 @@ struct Staged {
                     Acc r = ident;
 #pragma unroll
                     for (int j = 0; j < ITEMS; ++j) {
-                        Acc x[E];
+                        Acc x[EG];
                         load_chunk(sm, chunk_of(sub, j), t0, lo, hi, x);
                         Acc c = x[0];
 #pragma unroll
-                        for (int k = 1; k < E; ++k)
+                        for (int k = 1; k < EG; ++k)
                             c = Op::apply(c, x[k]);
 #pragma unroll
                         for (int d = 1; d < 32; d <<= 1) {  // lane order: lower lanes are earlier
@@ -141,36 +159,65 @@ struct Staged {
     __device__ __forceinline__ static uint4 *plane(Smem &sm, int p, int c) {
         return p == 0 ? &sm.stage[c] : &sm.extra[(p - 1) * kChunks + c];
     }
-    __device__ __forceinline__ static void put(Smem &sm, int c, const Acc (&x)[E]) {
+    __device__ __forceinline__ static void put(Smem &sm, int gi, const Acc (&x)[EG]) {
 #pragma unroll
-        for (int p = 0; p < kPlanes; ++p) {
-            uint4 w;
-            Acc *d = reinterpret_cast<Acc *>(&w);
+        for (int q = 0; q < V; ++q) {
+            const int c = gi * V + q;
 #pragma unroll
-            for (int q = 0; q < kPerPlane; ++q)
-                d[q] = (p * kPerPlane + q < E) ? x[p * kPerPlane + q] : Acc(0);
-            *plane(sm, p, c) = w;
+            for (int p = 0; p < kPlanes; ++p) {
+                uint4 w;
+                Acc *d = reinterpret_cast<Acc *>(&w);
+#pragma unroll
+                for (int r = 0; r < kPerPlane; ++r)
+                    d[r] = (p * kPerPlane + r < E) ? x[q * E + p * kPerPlane + r] : Acc(0);
+                *plane(sm, p, c) = w;
+            }
         }
     }
-    __device__ __forceinline__ static void get(Smem &sm, int c, Acc (&x)[E]) {
+    __device__ __forceinline__ static void get(Smem &sm, int gi, Acc (&x)[EG]) {
 #pragma unroll
-        for (int p = 0; p < kPlanes; ++p) {
-            const uint4 w = *plane(sm, p, c);
-            const Acc *d = reinterpret_cast<const Acc *>(&w);
+        for (int q = 0; q < V; ++q) {
+            const int c = gi * V + q;
 #pragma unroll
-            for (int q = 0; q < kPerPlane; ++q)
-                if (p * kPerPlane + q < E)
-                    x[p * kPerPlane + q] = d[q];
+            for (int p = 0; p < kPlanes; ++p) {
+                const uint4 w = *plane(sm, p, c);
+                const Acc *d = reinterpret_cast<const Acc *>(&w);
+#pragma unroll
+                for (int r = 0; r < kPerPlane; ++r)
+                    if (p * kPerPlane + r < E)
+                        x[q * E + p * kPerPlane + r] = d[r];
+            }
+        }
+    }
+    // Store a group's outputs: 16-byte stores for whole aligned chunks.
+    __device__ __forceinline__ static void store_group(S *eout, bool aligned_io, int64_t v, int64_t lo,
+                                                       int64_t hi, const Acc (&x)[EG]) {
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+            const int64_t vq = v + q * E;
+            Acc part[E];
+#pragma unroll
+            for (int k = 0; k < E; ++k)
+                part[k] = x[q * E + k];
+            if (aligned_io && vq >= lo && vq + E <= hi) {
+                st_v4(reinterpret_cast<uint4 *>(eout) + vq / E, C::pack(part));
+            } else if (vq < hi && vq + E > lo) {
+#pragma unroll
+                for (int k = 0; k < E; ++k)
+                    if (vq + k >= lo && vq + k < hi)
+                        C::store1(eout + vq + k, part[k]);
+            }
         }
     }
 };
 
-template <class S, class Op, int ITEMS, int SUB, int THREADS>
+template <class S, class Op, int ITEMS, int SUB, int THREADS, int V>
 __global__ void __launch_bounds__(THREADS) k_scan_staged(SegArgs a) {
-    using G = Staged<S, Op, ITEMS, SUB, THREADS>;
+    using G = Staged<S, Op, ITEMS, SUB, THREADS, V>;
     using Acc = typename G::Acc;
     using C = typename G::C;
     constexpr int E = G::E;
+    constexpr int EG = G::EG;
     extern __shared__ __align__(128) unsigned char dsm[];
     typename G::Smem &sm = *reinterpret_cast<typename G::Smem *>(dsm);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -239,35 +286,27 @@ __global__ void __launch_bounds__(THREADS) k_scan_staged(SegArgs a) {
         // that later tiles' look-backs find it as early as possible.
         const Acc agg_total = G::reduce(sm, t0, lo, hi);
         publish_aggregate<Acc, Op>(a.lb, g, first, agg_total);
+#if MT_STAGED_EARLY_LOOKBACK
+        // The prefix right away; the scan below then stores final outputs.
+        const Acc tp = lookback_prefix<Acc, Op>(a.lb, g, first, agg_total, &sm.prefix[it & 1]);
+#endif
 
         // Pass 1: scan the sub-tiles in order with a running carry; keep each
         // element's super-tile-local prefix in shared memory.
         Acc carry = ident;
 #pragma unroll 1
         for (int sub = 0; sub < SUB; ++sub) {
-            Acc x[ITEMS][E];
+            Acc x[ITEMS][EG];
 #pragma unroll
-            for (int j = 0; j < ITEMS; ++j) {
-                const int c = G::chunk_of(sub, j);
-                const int64_t v = t0 + (int64_t)c * E;
-                uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-                if (v < hi && v + E > lo)
-                    raw = sm.stage[c];
-                C::unpack(raw, x[j]);
-                if (!(v >= lo && v + E <= hi)) {
-#pragma unroll
-                    for (int k = 0; k < E; ++k)
-                        if (v + k < lo || v + k >= hi)
-                            x[j][k] = ident;
-                }
-            }
+            for (int j = 0; j < ITEMS; ++j)
+                G::load_chunk(sm, G::chunk_of(sub, j), t0, lo, hi, x[j]);
             Acc inc[ITEMS];
 #pragma unroll
             for (int j = 0; j < ITEMS; ++j) {
 #pragma unroll
-                for (int k = 1; k < E; ++k)
+                for (int k = 1; k < EG; ++k)
                     x[j][k] = Op::apply(x[j][k - 1], x[j][k]);
-                inc[j] = x[j][E - 1];
+                inc[j] = x[j][EG - 1];
             }
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -299,27 +338,36 @@ __global__ void __launch_bounds__(THREADS) k_scan_staged(SegArgs a) {
                     wpre = Op::apply(wpre, t);
                 agg = Op::apply(agg, t);
             }
+#if MT_STAGED_EARLY_LOOKBACK
+            const Acc base0 = Op::apply(Op::apply(tp, carry), wpre);
+#else
             const Acc base0 = Op::apply(carry, wpre);
+#endif
 #pragma unroll
             for (int j = 0; j < ITEMS; ++j) {
                 const Acc base = Op::apply(base0, pre[j]);
                 if (a.inclusive) {
 #pragma unroll
-                    for (int k = 0; k < E; ++k)
+                    for (int k = 0; k < EG; ++k)
                         x[j][k] = Op::apply(base, x[j][k]);
                 } else {
 #pragma unroll
-                    for (int k = E - 1; k > 0; --k)
+                    for (int k = EG - 1; k > 0; --k)
                         x[j][k] = Op::apply(base, x[j][k - 1]);
                     x[j][0] = base;
                 }
-                const int c = G::chunk_of(sub, j);
-                const int64_t v = t0 + (int64_t)c * E;
-                if (v < hi && v + E > lo)
-                    G::put(sm, c, x[j]);
+                const int gi = G::chunk_of(sub, j);
+                const int64_t v = t0 + (int64_t)gi * EG;
+#if MT_STAGED_EARLY_LOOKBACK
+                G::store_group(eout, a.aligned_io != 0, v, lo, hi, x[j]);
+#else
+                if (v < hi && v + EG > lo)
+                    G::put(sm, gi, x[j]);
+#endif
             }
             carry = Op::apply(carry, agg);
         }
+#if !MT_STAGED_EARLY_LOOKBACK
 
         // The super-tile's prefix (publishes its aggregate, looks back, and
         // publishes its inclusive prefix; identity for a segment's first one).
@@ -330,32 +378,26 @@ __global__ void __launch_bounds__(THREADS) k_scan_staged(SegArgs a) {
         for (int sub = 0; sub < SUB; ++sub) {
 #pragma unroll
             for (int j = 0; j < ITEMS; ++j) {
-                const int c = G::chunk_of(sub, j);
-                const int64_t v = t0 + (int64_t)c * E;
-                if (!(v < hi && v + E > lo))
+                const int gi = G::chunk_of(sub, j);
+                const int64_t v = t0 + (int64_t)gi * EG;
+                if (!(v < hi && v + EG > lo))
                     continue;
-                Acc x[E];
-                G::get(sm, c, x);
+                Acc x[EG];
+                G::get(sm, gi, x);
 #pragma unroll
-                for (int k = 0; k < E; ++k)
+                for (int k = 0; k < EG; ++k)
                     x[k] = Op::apply(tp, x[k]);
-                if (a.aligned_io && v >= lo && v + E <= hi) {
-                    st_v4(reinterpret_cast<uint4 *>(eout) + v / E, C::pack(x));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < E; ++k)
-                        if (v + k >= lo && v + k < hi)
-                            C::store1(eout + v + k, x[k]);
-                }
+                G::store_group(eout, a.aligned_io != 0, v, lo, hi, x);
             }
         }
+#endif
         fence_proxy_async_smem();  // this thread's shared writes precede the next bulk copy
     }
 }
 
-template <class S, class Op, int ITEMS, int SUB, int THREADS>
+template <class S, class Op, int ITEMS, int SUB, int THREADS, int V = 1>
 static cudaError_t launch_staged(const SegArgs &a, int64_t max_ctas, const Launch &L) {
-    using G = Staged<S, Op, ITEMS, SUB, THREADS>;
+    using G = Staged<S, Op, ITEMS, SUB, THREADS, V>;
     static int per_sm[128] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -364,12 +406,19 @@ static cudaError_t launch_staged(const SegArgs &a, int64_t max_ctas, const Launc
     if (dev < 0 || dev >= 128)
         return cudaErrorInvalidDevice;
     if (per_sm[dev] == 0) {
-        e = cudaFuncSetAttribute(k_scan_staged<S, Op, ITEMS, SUB, THREADS>,
+        e = cudaFuncSetAttribute(k_scan_staged<S, Op, ITEMS, SUB, THREADS, V>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmemBytes);
         if (e != cudaSuccess)
             return e;
+        // the whole unified L1/shared array as shared memory, so that as many
+        // super-tiles as registers allow are in flight on each SM
+        e = cudaFuncSetAttribute(k_scan_staged<S, Op, ITEMS, SUB, THREADS, V>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
         int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_scan_staged<S, Op, ITEMS, SUB, THREADS>,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_scan_staged<S, Op, ITEMS, SUB, THREADS, V>,
                                                           THREADS, G::kSmemBytes);
         if (e != cudaSuccess)
             return e;
@@ -380,7 +429,7 @@ static cudaError_t launch_staged(const SegArgs &a, int64_t max_ctas, const Launc
         grid = max_ctas;
     if (grid < 1)
         grid = 1;
-    k_scan_staged<S, Op, ITEMS, SUB, THREADS><<<(unsigned)grid, THREADS, G::kSmemBytes, L.stream>>>(a);
+    k_scan_staged<S, Op, ITEMS, SUB, THREADS, V><<<(unsigned)grid, THREADS, G::kSmemBytes, L.stream>>>(a);
     note_launch();
     return cudaGetLastError();
 }
