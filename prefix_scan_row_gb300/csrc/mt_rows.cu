@@ -6,11 +6,12 @@
 // out[i] = sum_{j<i} inp[j] with out[0] = 0, f32 loads and accumulation and
 // one cast at the store). The page runs one threadgroup per row that walks
 // the row in 1024-element chunks with a serial carry; here a row that fits
-// in one tile is one CTA (k_scan_rows), and a longer row is split over tiles
-// of a persistent pipelined kernel (mt_pipe.cuh) whose carries are chained by
-// the decoupled look-back, so every row -- short or 2^24 long -- is read once
-// and written once.
+// in one tile is one CTA (k_scan_rows, mt_tilescan.cuh), and a longer row is
+// split over the super-tiles of the persistent staged kernel (mt_staged.cuh)
+// whose carries are chained by the decoupled look-back, so every row --
+// short or 2^24 long -- is read once and written once.
 #include "mt_staged.cuh"
+#include "mt_tilescan.cuh"
 
 namespace mt {
 
@@ -27,23 +28,23 @@ struct RowArgs {
 // (the block size is chosen per row length, up to 16 warps).
 template <class S, int ITEMS>
 __global__ void __launch_bounds__(512) k_scan_rows(RowArgs a) {
-    using T = TileScan<S, OpAdd, ITEMS, 0>;
+    using T = RowTile<S, OpAdd, ITEMS>;
     __shared__ typename T::Smem sm;
     const int64_t row = blockIdx.x;
     if (row >= a.rows)
         return;
     constexpr int64_t s = sizeof(S);
     const char *in_row = a.in + row * a.n * s;
-    const int64_t head = (int64_t)(((uintptr_t)in_row & 15u) / s);
+    const int head = (int)(((uintptr_t)in_row & 15u) / s);
     const uint4 *vin = reinterpret_cast<const uint4 *>(in_row - head * s);
     S *eout = reinterpret_cast<S *>(a.out + row * a.n * s) - head;
-    const LookBack none{nullptr, -1, 0};
-    T::run(vin, eout, a.aligned_io != 0, 0, head, head + a.n, a.inclusive != 0, none, row, row, sm);
+    const int lo = head, hi = head + (int)a.n;
+    if (lo == 0 && hi == (int)blockDim.x * ITEMS * T::E)  // the row fills the tile
+        T::template run<true>(vin, eout, a.aligned_io != 0, lo, hi, a.inclusive != 0, sm);
+    else
+        T::template run<false>(vin, eout, a.aligned_io != 0, lo, hi, a.inclusive != 0, sm);
 }
 
-#ifndef MT_ROWS_KIND
-#define MT_ROWS_KIND 2  // long rows: 0 direct loads, 1 bulk-copy ring, 2 staged super-tiles
-#endif
 #ifndef MT_ROWS_SUB_WIDE
 #define MT_ROWS_SUB_WIDE 3  // sub-tiles per super-tile, 4-byte storage
 #endif
@@ -52,9 +53,6 @@ __global__ void __launch_bounds__(512) k_scan_rows(RowArgs a) {
 #endif
 #ifndef MT_ROWS_THREADS
 #define MT_ROWS_THREADS 256
-#endif
-#ifndef MT_ROWS_STAGES
-#define MT_ROWS_STAGES 2
 #endif
 constexpr int kMultiItems = 4;
 constexpr int kMultiThreads = MT_ROWS_THREADS;
@@ -66,24 +64,14 @@ static constexpr int sub_of() {
 
 template <class S>
 static cudaError_t launch_long(const SegArgs &a, int64_t tiles, const Launch &L) {
-#if MT_ROWS_KIND == 2
     return launch_staged<S, OpAdd, kMultiItems, sub_of<S>(), kMultiThreads>(a, tiles, L);
-#elif MT_ROWS_KIND == 1
-    return launch_pipe<S, OpAdd, kMultiItems, MT_ROWS_STAGES, kMultiThreads>(a, tiles, L);
-#else
-    return launch_direct<S, OpAdd, kMultiItems, kMultiThreads>(a, tiles, L);
-#endif
 }
 
 // Virtual elements per tile of a long row.
 static int64_t long_tile_elems(int dtype) {
-#if MT_ROWS_KIND == 2
     if (dtype == 0)
         return Staged<float, OpAdd, kMultiItems, sub_of<float>(), kMultiThreads>::kTE;
     return Staged<__half, OpAdd, kMultiItems, sub_of<__half>(), kMultiThreads>::kTE;
-#else
-    return (int64_t)kMultiThreads * kMultiItems * (dtype == 0 ? 4 : 8);
-#endif
 }
 
 // Single-tile rows: the (warps, chunks per thread) pair that covers the row

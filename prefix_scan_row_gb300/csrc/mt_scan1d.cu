@@ -6,25 +6,16 @@
 // the identity of "Semantics > Common conventions > Identity value". The
 // page's realisation is a three-pass scan (tile reduce, scan of partials,
 // re-read and scan); here one persistent kernel reads every element once and
-// writes it once, chaining tiles with the decoupled look-back; tiles reach
-// shared memory by bulk copies a few tiles ahead (mt_pipe.cuh). The grid is
+// writes it once, chaining super-tiles with the decoupled look-back; each
+// super-tile reaches shared memory by one bulk copy (mt_staged.cuh). The grid is
 // sized from the SM count and occupancy, not from n, so the host never needs
 // the live count.
 #include "mt_staged.cuh"
 
 namespace mt {
 
-#ifndef MT_SCAN1D_KIND
-#define MT_SCAN1D_KIND 2  // 0: direct loads, 1: bulk-copy ring, 2: staged super-tiles
-#endif
 #ifndef MT_SCAN1D_SUB
 #define MT_SCAN1D_SUB 3   // sub-tiles per staged super-tile
-#endif
-#ifndef MT_SCAN1D_V4
-#define MT_SCAN1D_V4 1    // adjacent 16-byte chunks per thread group, 4-byte types
-#endif
-#ifndef MT_SCAN1D_V8
-#define MT_SCAN1D_V8 1    // the same for 8-byte types
 #endif
 #ifndef MT_SCAN1D_ITEMS
 #define MT_SCAN1D_ITEMS 4
@@ -32,41 +23,17 @@ namespace mt {
 #ifndef MT_SCAN1D_THREADS
 #define MT_SCAN1D_THREADS 256
 #endif
-#ifndef MT_SCAN1D_STAGES
-#define MT_SCAN1D_STAGES 2
-#endif
 constexpr int kScanItems = MT_SCAN1D_ITEMS;      // 16-byte chunks per thread per tile
 constexpr int kScanThreads = MT_SCAN1D_THREADS;  // threads per CTA
 
-template <class S>
-static constexpr int vec_of() {
-    return sizeof(S) == 8 ? MT_SCAN1D_V8 : MT_SCAN1D_V4;
-}
-
-// Groups per thread per sub-tile: a sub-tile stays kScanItems chunks per thread.
-template <class S>
-static constexpr int items_of() {
-    return kScanItems / vec_of<S>() > 0 ? kScanItems / vec_of<S>() : 1;
-}
-
 template <class S, class Op>
 static cudaError_t launch_scan(const SegArgs &a, const Launch &L) {
-#if MT_SCAN1D_KIND == 2
-    return launch_staged<S, Op, items_of<S>(), MT_SCAN1D_SUB, kScanThreads, vec_of<S>()>(a, 0, L);
-#elif MT_SCAN1D_KIND == 1
-    return launch_pipe<S, Op, kScanItems, MT_SCAN1D_STAGES, kScanThreads>(a, 0, L);
-#else
-    return launch_direct<S, Op, kScanItems, kScanThreads>(a, 0, L);
-#endif
+    return launch_staged<S, Op, kScanItems, MT_SCAN1D_SUB, kScanThreads>(a, 0, L);
 }
 
 template <class S>
 static constexpr int64_t tile_elems_of() {
-#if MT_SCAN1D_KIND == 2
-    return Staged<S, OpAdd, items_of<S>(), MT_SCAN1D_SUB, kScanThreads, vec_of<S>()>::kTE;
-#else
-    return TileScan<S, OpAdd, kScanItems, kScanThreads>::kTE;
-#endif
+    return Staged<S, OpAdd, kScanItems, MT_SCAN1D_SUB, kScanThreads>::kTE;
 }
 
 int64_t scan1d_tile_elems(int dtype) {

@@ -19,7 +19,7 @@
 // ranks the selected lanes, so the writes are consecutive: no bank
 // conflicts). The look-back comes last, then each warp copies its packed run
 // out with coalesced stores. k_select serves the other alignments.
-#include "mt_pipe.cuh"
+#include "mt_lookback.cuh"
 
 namespace mt {
 

@@ -37,6 +37,7 @@ constexpr uint32_t kAgg = 1;    // the tile's own aggregate is published
 constexpr uint32_t kIncl = 2;   // the inclusive prefix through this tile is published
 
 constexpr int kErrTimeout = -5;  // same value as MT_ERR_LOOKBACK_TIMEOUT
+constexpr uint32_t kCopyWaitLimit = 1u << 26;  // mbarrier polls before a copy is given up
 
 // Per translation unit device error word; written when a look-back wait gives up.
 static __device__ int g_mt_err;
