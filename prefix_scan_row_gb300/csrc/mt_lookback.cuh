@@ -25,8 +25,8 @@ namespace mt {
 #define MT_REC_SLOTS 16  // 8-byte slots per record: one 128-byte line each, so the
                          // records near the look-back front spread over L2 slices
 #endif
-#if MT_REC_SLOTS < 3
-#error "a record needs at least three 8-byte slots for 8-byte values"
+#if MT_REC_SLOTS < 2
+#error "a record needs at least two 8-byte slots for 8-byte values"
 #endif
 
 // Tile status records.
@@ -47,21 +47,28 @@ template <class Acc> struct Status<Acc, true> {
     }
 };
 
-// 8-byte values: three words [flag, aggregate, inclusive]. The value word is
-// written before the flag (release) and read after it (acquire); each value
-// word is written once per call, so a reader never sees it change.
+// 8-byte values: two words, each [flag:32 | one 32-bit half of the value]
+// (low half first). Every word is written by one single-copy-atomic 64-bit
+// store and carries the flag of the state it belongs to, so a reader that
+// loads both words (two independent loads: one round trip) and finds the
+// same flag in both has both halves of that state's value. A reader that
+// finds two different flags caught the record between the two stores of an
+// update and sees it as empty, which only makes it poll again. States only
+// move forward (empty, aggregate, inclusive), so no fence is needed.
 template <class Acc> struct Status<Acc, false> {
     static constexpr int kSlots = MT_REC_SLOTS;
     __device__ __forceinline__ static void publish(uint64_t *rec, uint32_t flag, Acc v) {
-        st_relaxed_u64(rec + (flag == kAgg ? 1 : 2), (uint64_t)v);
-        st_release_u64(rec, (uint64_t)flag);
+        const uint64_t u = (uint64_t)v;
+        const uint64_t f = (uint64_t)flag << 32;
+        st_relaxed_u64(rec, f | (u & 0xffffffffull));
+        st_relaxed_u64(rec + 1, f | (u >> 32));
     }
     __device__ __forceinline__ static void read(const uint64_t *rec, uint32_t &flag, Acc &v) {
-        flag = (uint32_t)ld_acquire_u64(rec);
-        if (flag == kAgg)
-            v = (Acc)ld_relaxed_u64(rec + 1);
-        else if (flag == kIncl)
-            v = (Acc)ld_relaxed_u64(rec + 2);
+        const uint64_t w0 = ld_relaxed_u64(rec);
+        const uint64_t w1 = ld_relaxed_u64(rec + 1);
+        const uint32_t f0 = (uint32_t)(w0 >> 32), f1 = (uint32_t)(w1 >> 32);
+        flag = (f0 == f1) ? f0 : kEmpty;
+        v = (Acc)((w1 << 32) | (w0 & 0xffffffffull));
     }
 };
 

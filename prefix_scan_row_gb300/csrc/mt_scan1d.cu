@@ -17,6 +17,9 @@ namespace mt {
 #ifndef MT_SCAN1D_SUB
 #define MT_SCAN1D_SUB 3   // sub-tiles per staged super-tile
 #endif
+#ifndef MT_SCAN1D_SUB8
+#define MT_SCAN1D_SUB8 MT_SCAN1D_SUB  // the same for 8-byte types
+#endif
 #ifndef MT_SCAN1D_ITEMS
 #define MT_SCAN1D_ITEMS 4
 #endif
@@ -26,14 +29,19 @@ namespace mt {
 constexpr int kScanItems = MT_SCAN1D_ITEMS;      // 16-byte chunks per thread per tile
 constexpr int kScanThreads = MT_SCAN1D_THREADS;  // threads per CTA
 
+template <class S>
+static constexpr int sub_of() {
+    return sizeof(S) == 8 ? MT_SCAN1D_SUB8 : MT_SCAN1D_SUB;
+}
+
 template <class S, class Op>
 static cudaError_t launch_scan(const SegArgs &a, const Launch &L) {
-    return launch_staged<S, Op, kScanItems, MT_SCAN1D_SUB, kScanThreads>(a, 0, L);
+    return launch_staged<S, Op, kScanItems, sub_of<S>(), kScanThreads>(a, 0, L);
 }
 
 template <class S>
 static constexpr int64_t tile_elems_of() {
-    return Staged<S, OpAdd, kScanItems, MT_SCAN1D_SUB, kScanThreads>::kTE;
+    return Staged<S, OpAdd, kScanItems, sub_of<S>(), kScanThreads>::kTE;
 }
 
 int64_t scan1d_tile_elems(int dtype) {

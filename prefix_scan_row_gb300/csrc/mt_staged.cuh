@@ -39,6 +39,13 @@ struct SegArgs {
     LookBack lb;                  // lb.recs == nullptr: no tile waits on another
 };
 
+#ifndef MT_STAGED_EARLY_W4
+#define MT_STAGED_EARLY_W4 1  // early aggregate for 4-byte accumulators
+#endif
+#ifndef MT_STAGED_EARLY_W8
+#define MT_STAGED_EARLY_W8 1  // the same for 8-byte accumulators
+#endif
+
 template <class S, class Op, int ITEMS, int SUB, int THREADS>
 struct Staged {
     using C = Codec<S>;
@@ -193,8 +200,12 @@ struct Staged {
         const Acc ident = Op::template identity<Acc>();
 
         // Pass 0: the aggregate, published before the scan.
-        const Acc agg_total = reduce<FULL>(sm, llo, lhi);
-        publish_aggregate<Acc, Op>(a.lb, g, first, agg_total);
+        constexpr bool kEarly = sizeof(Acc) == 8 ? MT_STAGED_EARLY_W8 : MT_STAGED_EARLY_W4;
+        Acc agg_total = ident;
+        if constexpr (kEarly) {
+            agg_total = reduce<FULL>(sm, llo, lhi);
+            publish_aggregate<Acc, Op>(a.lb, g, first, agg_total);
+        }
 
         // Pass 1: sub-tiles in order with a running carry; keep each
         // element's super-tile-local prefix in shared memory.
@@ -260,6 +271,11 @@ struct Staged {
                 put(sm, chunk_of(sub, j), x[j]);
             }
             carry = Op::apply(carry, agg);
+        }
+
+        if constexpr (!kEarly) {
+            agg_total = carry;
+            publish_aggregate<Acc, Op>(a.lb, g, first, agg_total);
         }
 
         // The super-tile's prefix: look back, publish the inclusive prefix
