@@ -8,8 +8,8 @@
 //      publishes it at once, so that later tiles' look-backs wait less;
 //   3. scans it in SUB sub-tiles of THREADS x ITEMS 16-byte chunks (registers,
 //      warp shuffles, block totals) with a running carry across sub-tiles, and
-//      writes each element's super-tile-local prefix back to shared memory --
-//      every thread rereads only the chunks it wrote, so this needs no barrier;
+//      writes each element's super-tile-local prefix back to shared memory
+//      in place;
 //   4. looks back for the super-tile's prefix (one look-back per SUB
 //      sub-tiles), combines it with the local prefixes and stores the outputs.
 // The super-tile makes look-backs SUB times rarer per byte, and the input in
@@ -39,6 +39,15 @@ struct SegArgs {
     LookBack lb;                  // lb.recs == nullptr: no tile waits on another
 };
 
+#ifndef MT_STAGED_WAIT_WARP0
+#define MT_STAGED_WAIT_WARP0 1  // only warp 0 polls the copy's mbarrier
+#endif
+#ifndef MT_STAGED_PAIR_W4
+#define MT_STAGED_PAIR_W4 1  // scan 4-byte types two chunks per thread unit
+#endif
+#ifndef MT_STAGED_PAIR_W8
+#define MT_STAGED_PAIR_W8 1  // the same for 8-byte types
+#endif
 #ifndef MT_STAGED_EARLY_W4
 #define MT_STAGED_EARLY_W4 1  // early aggregate for 4-byte accumulators
 #endif
@@ -58,6 +67,13 @@ struct Staged {
     // local prefixes of one chunk, in 16-byte planes: 1 when Acc is as wide as S
     static constexpr int kPlanes = (E * (int)sizeof(Acc) + 15) / 16;
     static constexpr int kPerPlane = 16 / (int)sizeof(Acc);  // Acc values per plane
+    // Pass 1 scans units of V adjacent chunks per thread: a longer serial
+    // run per thread and V times fewer warp scans per element. V = 2 needs
+    // one plane (prefixes as wide as the input) and an even ITEMS.
+    static constexpr int V =
+        (kPlanes == 1 && ITEMS % 2 == 0 && (sizeof(Acc) == 8 ? MT_STAGED_PAIR_W8 : MT_STAGED_PAIR_W4)) ? 2 : 1;
+    static constexpr int kU = ITEMS / V;  // units per thread per sub-tile
+    static constexpr int EU = V * E;      // elements per unit
 
     struct Smem {
         uint4 stage[kChunks];                                    // input; plane 0 of the prefixes
@@ -81,7 +97,7 @@ struct Staged {
     // be stale: the copy only covers chunks that hold valid elements).
     template <bool FULL>
     __device__ __forceinline__ static void load(const Smem &sm, int c, int llo, int lhi, Acc (&x)[E]) {
-        C::unpack(sm.stage[c], x);
+        C::unpack(lds128(&sm.stage[c]), x);
         if (!FULL) {
             const int o = c * E;
             if (!(o >= llo && o + E <= lhi)) {
@@ -105,18 +121,77 @@ struct Staged {
 #pragma unroll
             for (int r = 0; r < kPerPlane; ++r)
                 d[r] = (p * kPerPlane + r < E) ? x[p * kPerPlane + r] : Acc(0);
-            *plane(sm, p, c) = w;
+            sts128(plane(sm, p, c), w);
         }
     }
     __device__ __forceinline__ static void get(Smem &sm, int c, Acc (&x)[E]) {
 #pragma unroll
         for (int p = 0; p < kPlanes; ++p) {
-            const uint4 w = *plane(sm, p, c);
+            const uint4 w = lds128(plane(sm, p, c));
             const Acc *d = reinterpret_cast<const Acc *>(&w);
 #pragma unroll
             for (int r = 0; r < kPerPlane; ++r)
                 if (p * kPerPlane + r < E)
                     x[p * kPerPlane + r] = d[r];
+        }
+    }
+
+    // Unit index of this thread's j-th unit of sub-tile `sub`; its chunks
+    // are V * unit ... V * unit + V - 1.
+    __device__ __forceinline__ static int unit_of(int sub, int j) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        return sub * (kSubChunks / V) + warp * 32 * kU + j * 32 + lane;
+    }
+    // With V = 2, lanes 4-7 of every group of 8 take their unit's second
+    // chunk first: the 8 lanes that share a shared-memory wavefront then
+    // touch 8 different 16-byte bank groups, for loads and stores alike.
+    __device__ __forceinline__ static int pair_swap() { return (threadIdx.x >> 2) & 1; }
+    __device__ __forceinline__ static uint4 pick(bool s, const uint4 &a, const uint4 &b) {
+        return make_uint4(s ? a.x : b.x, s ? a.y : b.y, s ? a.z : b.z, s ? a.w : b.w);
+    }
+    template <bool FULL>
+    __device__ __forceinline__ static void load_unit(const Smem &sm, int u, int llo, int lhi, Acc (&x)[EU]) {
+        if constexpr (V == 1) {
+            load<FULL>(sm, u, llo, lhi, x);
+        } else {
+            const bool s = pair_swap();
+            const uint4 p = lds128(&sm.stage[2 * u + (s ? 1 : 0)]);
+            const uint4 q = lds128(&sm.stage[2 * u + (s ? 0 : 1)]);
+            Acc lo[E], hi[E];
+            C::unpack(pick(s, q, p), lo);
+            C::unpack(pick(s, p, q), hi);
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                x[k] = lo[k];
+                x[E + k] = hi[k];
+            }
+            if (!FULL) {
+                const int o = u * EU;
+                if (!(o >= llo && o + EU <= lhi)) {
+                    const Acc ident = Op::template identity<Acc>();
+#pragma unroll
+                    for (int k = 0; k < EU; ++k)
+                        if (o + k < llo || o + k >= lhi)
+                            x[k] = ident;
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ static void put_unit(Smem &sm, int u, const Acc (&x)[EU]) {
+        if constexpr (V == 1) {
+            put(sm, u, x);
+        } else {
+            uint4 w[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                Acc *d = reinterpret_cast<Acc *>(&w[q]);
+#pragma unroll
+                for (int r = 0; r < E; ++r)
+                    d[r] = x[q * E + r];
+            }
+            const bool s = pair_swap();
+            sts128(&sm.stage[2 * u + (s ? 1 : 0)], pick(s, w[1], w[0]));
+            sts128(&sm.stage[2 * u + (s ? 0 : 1)], pick(s, w[0], w[1]));
         }
     }
 
@@ -212,31 +287,31 @@ struct Staged {
         Acc carry = ident;
 #pragma unroll 1
         for (int sub = 0; sub < SUB; ++sub) {
-            Acc x[ITEMS][E];
+            Acc x[kU][EU];
 #pragma unroll
-            for (int j = 0; j < ITEMS; ++j)
-                load<FULL>(sm, chunk_of(sub, j), llo, lhi, x[j]);
-            Acc inc[ITEMS];
+            for (int j = 0; j < kU; ++j)
+                load_unit<FULL>(sm, unit_of(sub, j), llo, lhi, x[j]);
+            Acc inc[kU];
 #pragma unroll
-            for (int j = 0; j < ITEMS; ++j) {
+            for (int j = 0; j < kU; ++j) {
 #pragma unroll
-                for (int k = 1; k < E; ++k)
+                for (int k = 1; k < EU; ++k)
                     x[j][k] = Op::apply(x[j][k - 1], x[j][k]);
-                inc[j] = x[j][E - 1];
+                inc[j] = x[j][EU - 1];
             }
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
 #pragma unroll
-                for (int j = 0; j < ITEMS; ++j) {
+                for (int j = 0; j < kU; ++j) {
                     const Acc y = __shfl_up_sync(kFull, inc[j], d);
                     if (lane >= d)
                         inc[j] = Op::apply(y, inc[j]);
                 }
             }
-            Acc pre[ITEMS];
+            Acc pre[kU];
             Acc run = ident;
 #pragma unroll
-            for (int j = 0; j < ITEMS; ++j) {
+            for (int j = 0; j < kU; ++j) {
                 Acc e = __shfl_up_sync(kFull, inc[j], 1);
                 if (lane == 0)
                     e = ident;
@@ -256,19 +331,19 @@ struct Staged {
             }
             const Acc base0 = Op::apply(carry, wpre);
 #pragma unroll
-            for (int j = 0; j < ITEMS; ++j) {
+            for (int j = 0; j < kU; ++j) {
                 const Acc base = Op::apply(base0, pre[j]);
                 if (a.inclusive) {
 #pragma unroll
-                    for (int k = 0; k < E; ++k)
+                    for (int k = 0; k < EU; ++k)
                         x[j][k] = Op::apply(base, x[j][k]);
                 } else {
 #pragma unroll
-                    for (int k = E - 1; k > 0; --k)
+                    for (int k = EU - 1; k > 0; --k)
                         x[j][k] = Op::apply(base, x[j][k - 1]);
                     x[j][0] = base;
                 }
-                put(sm, chunk_of(sub, j), x[j]);
+                put_unit(sm, unit_of(sub, j), x[j]);
             }
             carry = Op::apply(carry, agg);
         }
@@ -281,6 +356,11 @@ struct Staged {
         // The super-tile's prefix: look back, publish the inclusive prefix
         // (the identity for a segment's first super-tile).
         const Acc tp = lookback_prefix<Acc, Op>(a.lb, g, first, agg_total, &sm.prefix[buf]);
+        // Pass 2 reads chunks that other threads' units wrote when V > 1; the
+        // look-back ends with a block barrier except for a segment's first
+        // super-tile (or when no tile waits on another).
+        if (V > 1 && (a.lb.recs == nullptr || g == first))
+            __syncthreads();
 
         // Pass 2: prefix + local prefix, narrowed to S and stored; 16-byte
         // stores for whole chunks when the output has the input's phase.
@@ -311,7 +391,7 @@ struct Staged {
 };
 
 template <class S, class Op, int ITEMS, int SUB, int THREADS>
-__global__ void __launch_bounds__(THREADS) k_scan_staged(SegArgs a) {
+__global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) k_scan_staged(SegArgs a) {
     using G = Staged<S, Op, ITEMS, SUB, THREADS>;
     constexpr int E = G::E;
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -367,11 +447,16 @@ __global__ void __launch_bounds__(THREADS) k_scan_staged(SegArgs a) {
             mbar_arrive_expect_tx(&sm.bar, bytes);
             bulk_g2s(&sm.stage[0], vin + c0, bytes, &sm.bar);
         }
-        const bool ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
+        // Warp 0 waits for the copy; the block barrier then passes the
+        // completion (and the copied bytes) on to the other warps.
+        bool ok = true;
+        if (!MT_STAGED_WAIT_WARP0 || threadIdx.x < 32)
+            ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
         if (__syncthreads_or(!ok)) {
-            if (threadIdx.x == 0)
+            if (threadIdx.x == 0) {
                 atomicCAS(&g_mt_err, 0, kErrTimeout);
-            mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copy before leaving
+                mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copy before leaving
+            }
             return;
         }
         phase ^= 1u;

@@ -210,6 +210,18 @@ __device__ __forceinline__ int ld_relaxed_i32(const int *p) {
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
+// One 16-byte shared-memory access as a single instruction: a 16-byte chunk
+// read as two 8-byte halves costs a warp twice the wavefronts.
+__device__ __forceinline__ uint4 lds128(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(uint4 *p, const uint4 &v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "r"(smem_addr(p)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
 }
