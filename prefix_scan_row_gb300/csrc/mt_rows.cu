@@ -26,11 +26,10 @@ struct RowArgs {
 
 // One CTA per row; the whole row is one tile of blockDim.x * ITEMS chunks
 // (the block size is chosen per row length, up to 16 warps).
-#ifndef MT_ROWS_MINB
-#define MT_ROWS_MINB 1  // resident 512-thread CTAs per SM the register use must allow
-#endif
+// (A minimum-blocks bound, even 1, makes the compiler spend more registers
+// here and costs resident CTAs.)
 template <class S, int ITEMS>
-__global__ void __launch_bounds__(512, MT_ROWS_MINB) k_scan_rows(RowArgs a) {
+__global__ void __launch_bounds__(512) k_scan_rows(RowArgs a) {
     using T = RowTile<S, OpAdd, ITEMS>;
     __shared__ typename T::Smem sm;
     const int64_t row = blockIdx.x;

@@ -196,10 +196,81 @@ struct SelStagedSmem {
     uint32_t prefix;
 };
 
+// One staged tile: count and publish the count, pack each warp's selected
+// words in place, look back for the tile's output offset, copy the packed
+// runs out. FULL: the tile holds kSelTE elements, so no flag or element needs
+// a range check. (Looking back before the packing, overlapped with it, was
+// measured slower: the look-back then meets more predecessors that have
+// only published their counts.)
+template <bool FULL>
+__device__ __forceinline__ void select_tile(SelStagedSmem &sm, const SelArgs &a, int64_t g, int64_t ntiles,
+                                            int elems) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // Count: popcounts of this thread's 16-flag chunks (flags past n are 0).
+    uint32_t mine = 0u;
+#pragma unroll
+    for (int j = 0; j < kSelItems; ++j) {
+        const int c = warp * 32 * kSelItems + j * 32 + lane;
+        const int valid = elems - c * 16;
+        if (FULL || valid > 0) {
+            uint4 f = lds128(&sm.flags[c]);
+            if (!FULL) {
+                f.x = keep_low_bytes(f.x, valid);
+                f.y = keep_low_bytes(f.y, valid - 4);
+                f.z = keep_low_bytes(f.z, valid - 8);
+                f.w = keep_low_bytes(f.w, valid - 12);
+            }
+            mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
+        }
+    }
+    // The tile's count, published as soon as the flags are in.
+    uint32_t wsum = mine;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        wsum += __shfl_xor_sync(kFull, wsum, d);
+    if (lane == 0)
+        sm.red[warp] = wsum;
+    __syncthreads();
+    uint32_t agg = 0u, wpre = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t t = sm.red[w];
+        if (w < warp)
+            wpre += t;
+        agg += t;
+    }
+    publish_aggregate<uint32_t, OpAdd>(a.lb, g, 0, agg);
+
+    // Pack this warp's selected words in place, in element order. A write
+    // goes to a slot at or before every element this warp reads later, and
+    // a warp step reads all its lanes before any of them writes.
+    const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
+    const int wstart = warp * 32 * kSelItems * 16;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t cnt = 0u;
+#pragma unroll
+    for (int step = 0; step < kSelItems * 16; ++step) {
+        const int e = wstart + step * 32 + lane;
+        const bool sel = (FULL || e < elems) && fb[e] != 0;
+        const unsigned bal = __ballot_sync(kFull, sel);
+        const uint32_t val = sm.vals[e];
+        if (sel)
+            sm.vals[wstart + cnt + __popc(bal & lt)] = val;
+        cnt += __popc(bal);
+    }
+    __syncwarp();
+    // The tile's output offset (the look-back ends with a block barrier).
+    const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
+    uint32_t *dst = a.out + G + wpre;
+    for (uint32_t i = lane; i < cnt; i += 32)
+        dst[i] = sm.vals[wstart + i];
+    if (g == ntiles - 1 && threadIdx.x == 0)
+        *a.num_out = (int32_t)(G + agg);
+}
+
 __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
     extern __shared__ __align__(128) unsigned char dsm[];
     SelStagedSmem &sm = *reinterpret_cast<SelStagedSmem *>(dsm);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
     const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
@@ -216,81 +287,33 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
         if (g >= ntiles)
             break;
         const int64_t t0 = g * kSelTE;
-        const int64_t elems = (n - t0 < kSelTE) ? n - t0 : kSelTE;
+        const int elems = (int)((n - t0 < kSelTE) ? n - t0 : kSelTE);
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
             const uint32_t fb = (uint32_t)((elems + 15) / 16 * 16);
-            const uint32_t vb = (uint32_t)((elems * 4 + 15) / 16 * 16);
+            const uint32_t vb = (uint32_t)(((int64_t)elems * 4 + 15) / 16 * 16);
             mbar_arrive_expect_tx(&sm.bar, fb + vb);
             bulk_g2s(&sm.flags[0], a.flags + t0, fb, &sm.bar);
             bulk_g2s(&sm.vals[0], a.arr + t0, vb, &sm.bar);
         }
-        const bool ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
+        // Warp 0 waits for the copies; the block barrier passes the
+        // completion (and the copied bytes) on to the other warps.
+        bool ok = true;
+        if (threadIdx.x < 32)
+            ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
         if (__syncthreads_or(!ok)) {
-            if (threadIdx.x == 0)
+            if (threadIdx.x == 0) {
                 atomicCAS(&g_mt_err, 0, kErrTimeout);
-            mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copies before leaving
+                mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copies before leaving
+            }
             return;
         }
         phase ^= 1u;
-
-        // Count: popcounts of this thread's 16-flag chunks (flags past n are 0).
-        uint32_t mine = 0u;
-#pragma unroll
-        for (int j = 0; j < kSelItems; ++j) {
-            const int c = warp * 32 * kSelItems + j * 32 + lane;
-            const int64_t valid = elems - (int64_t)c * 16;
-            if (valid > 0) {
-                uint4 f = sm.flags[c];
-                f.x = keep_low_bytes(f.x, valid);
-                f.y = keep_low_bytes(f.y, valid - 4);
-                f.z = keep_low_bytes(f.z, valid - 8);
-                f.w = keep_low_bytes(f.w, valid - 12);
-                mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
-            }
-        }
-        // The tile's count, published as soon as the flags are in.
-        uint32_t wsum = mine;
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1)
-            wsum += __shfl_xor_sync(kFull, wsum, d);
-        if (lane == 0)
-            sm.red[warp] = wsum;
-        __syncthreads();
-        uint32_t agg = 0u, wpre = 0u;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const uint32_t t = sm.red[w];
-            if (w < warp)
-                wpre += t;
-            agg += t;
-        }
-        publish_aggregate<uint32_t, OpAdd>(a.lb, g, 0, agg);
-
-        // Pack this warp's selected words in place, in element order. A write
-        // goes to a slot at or before every element this warp reads later, and
-        // a warp step reads all its lanes before any of them writes.
-        const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
-        const int wstart = warp * 32 * kSelItems * 16;
-        const unsigned lt = (1u << lane) - 1u;
-        uint32_t cnt = 0u;
-#pragma unroll
-        for (int step = 0; step < kSelItems * 16; ++step) {
-            const int e = wstart + step * 32 + lane;
-            const bool sel = (e < elems) && fb[e] != 0;
-            const unsigned bal = __ballot_sync(kFull, sel);
-            const uint32_t val = sm.vals[e];
-            if (sel)
-                sm.vals[wstart + cnt + __popc(bal & lt)] = val;
-            cnt += __popc(bal);
-        }
-        __syncwarp();
-        const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
-        uint32_t *dst = a.out + G + wpre;
-        for (uint32_t i = lane; i < cnt; i += 32)
-            dst[i] = sm.vals[wstart + i];
-        if (g == ntiles - 1 && threadIdx.x == 0)
-            *a.num_out = (int32_t)(G + agg);
+        if (elems == kSelTE)
+            select_tile<true>(sm, a, g, ntiles, elems);
+        else
+            select_tile<false>(sm, a, g, ntiles, elems);
+        fence_proxy_async_smem();  // this thread's shared writes precede the next bulk copies
     }
 }
 
