@@ -413,7 +413,9 @@ def run_suite(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peak, src = measured_peak()
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    # L2 flush by a read of twice its size: the lines left behind are clean,
+    # so the timed call does not pay for writing back the flush's own data.
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     rows_out = []
 
     def wanted(name):
@@ -431,7 +433,7 @@ def run_suite(args):
             # larger than L2) while the host enqueues the call, so the events
             # time the call's kernels and not the host's launch latency.
             if small:
-                flush.fill_(1)
+                flush.sum()
             else:
                 torch.cuda._sleep(100_000)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

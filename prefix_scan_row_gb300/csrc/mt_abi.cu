@@ -20,6 +20,7 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 // so an empty input still reports a count.
 __global__ void k_reset(uint64_t *words, int64_t nwords, const int32_t *n_dev, int64_t tile_elems,
                         int elem_size, int head_bytes, int rec_slots, int32_t *num_out) {
+    pdl_prologue();
     int64_t total = nwords;
     if (n_dev != nullptr) {
         const int32_t n32 = *n_dev;
@@ -63,10 +64,10 @@ static cudaError_t launch_reset(uint64_t *words, int64_t nwords, const int32_t *
         grid = 1;
     if (grid > 8 * (int64_t)L.sm_count)
         grid = 8 * (int64_t)L.sm_count;
-    k_reset<<<(unsigned)grid, 256, 0, L.stream>>>(words, nwords, n_dev, tile_elems, elem_size,
-                                                   head_bytes, rec_slots, num_out);
+    const cudaError_t e = launch_pdl(k_reset, (unsigned)grid, 256, 0, L.stream, words, nwords, n_dev,
+                                     tile_elems, elem_size, head_bytes, rec_slots, num_out);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 // A stream-ordered pool per device for the look-back records of long rows.

@@ -19,6 +19,37 @@ struct Launch {
 
 void note_launch();
 
+// ---- launches with programmatic stream serialization ----------------------
+// Every kernel of the library is launched so that its CTAs may be scheduled
+// while the previous kernel in the stream is still finishing, and starts with
+// pdl_prologue(): it first waits until that kernel has completed and its
+// writes are visible (stream order is kept exactly), then lets the next
+// kernel be scheduled. Back-to-back calls thus lose the launch gap and the
+// ramp-up of each grid, not their ordering. Without the launch attribute
+// (or after a non-kernel stream operation) the wait returns at once.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_prologue() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class... KArgs, class... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+#endif
+
 // ---- row-wise scan (mt_rows.cu) -------------------------------------------
 struct RowPlan {
     bool staged;             // row longer than one CTA tile: persistent staged kernel

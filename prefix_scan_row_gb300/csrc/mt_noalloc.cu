@@ -26,6 +26,7 @@ static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocSlots];
 // Clears what the next scan reads before writing (the counter and the tile
 // records); the previous call leaves its values behind.
 __global__ void k_noalloc_clear(int64_t nwords) {
+    pdl_prologue();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nwords; i += stride)
         g_noalloc_scratch[i] = 0ull;
@@ -99,9 +100,9 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
         int64_t grid = (nwords + 255) / 256;
         if (grid > 1024)
             grid = 1024;
-        k_noalloc_clear<<<(unsigned)grid, 256, 0, L.stream>>>(nwords);
+        const cudaError_t e = launch_pdl(k_noalloc_clear, (unsigned)grid, 256, 0, L.stream, nwords);
         note_launch();
-        if (cudaGetLastError() != cudaSuccess)
+        if (e != cudaSuccess)
             return MT_ERR_CUDA;
     } else {
         ws = nullptr;  // rows fit in one tile: no look-back, no workspace

@@ -30,6 +30,7 @@ struct RowArgs {
 // here and costs resident CTAs.)
 template <class S, int ITEMS>
 __global__ void __launch_bounds__(512) k_scan_rows(RowArgs a) {
+    pdl_prologue();
     using T = RowTile<S, OpAdd, ITEMS>;
     __shared__ typename T::Smem sm;
     const int64_t row = blockIdx.x;
@@ -106,18 +107,18 @@ RowPlan rows_plan(int dtype, int64_t n, bool heads_zero) {
 }
 
 template <class S, int ITEMS>
-static void launch_one(const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
-    k_scan_rows<S, ITEMS><<<(unsigned)grid, 32 * warps, 0, st>>>(a);
+static cudaError_t launch_one(const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
+    return launch_pdl(k_scan_rows<S, ITEMS>, (unsigned)grid, 32 * warps, 0, st, a);
 }
 
 template <class S>
-static void launch_items(int items, const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
+static cudaError_t launch_items(int items, const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
     switch (items) {
-    case 1: launch_one<S, 1>(a, grid, warps, st); break;
-    case 2: launch_one<S, 2>(a, grid, warps, st); break;
-    case 3: launch_one<S, 3>(a, grid, warps, st); break;
-    case 4: launch_one<S, 4>(a, grid, warps, st); break;
-    default: break;
+    case 1: return launch_one<S, 1>(a, grid, warps, st);
+    case 2: return launch_one<S, 2>(a, grid, warps, st);
+    case 3: return launch_one<S, 3>(a, grid, warps, st);
+    case 4: return launch_one<S, 4>(a, grid, warps, st);
+    default: return cudaErrorInvalidValue;
     }
 }
 
@@ -154,18 +155,16 @@ cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int 
     a.n = n;
     a.inclusive = inclusive ? 1 : 0;
     a.aligned_io = aligned_io ? 1 : 0;
-    if (dtype == 0) {
-        if (p.items == 8)
-            launch_one<float, 8>(a, rows, p.warps, L.stream);
-        else
-            launch_items<float>(p.items, a, rows, p.warps, L.stream);
-    } else if (dtype == 1) {
-        launch_items<__nv_bfloat16>(p.items, a, rows, p.warps, L.stream);
-    } else {
-        launch_items<__half>(p.items, a, rows, p.warps, L.stream);
-    }
+    cudaError_t e;
+    if (dtype == 0)
+        e = p.items == 8 ? launch_one<float, 8>(a, rows, p.warps, L.stream)
+                         : launch_items<float>(p.items, a, rows, p.warps, L.stream);
+    else if (dtype == 1)
+        e = launch_items<__nv_bfloat16>(p.items, a, rows, p.warps, L.stream);
+    else
+        e = launch_items<__half>(p.items, a, rows, p.warps, L.stream);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 int rows_rec_slots() { return Status<float>::kSlots; }

@@ -61,6 +61,7 @@ __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
+    pdl_prologue();
     __shared__ SelSmem sm;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t n32 = *a.n_dev;
@@ -269,6 +270,7 @@ __device__ __forceinline__ void select_tile(SelStagedSmem &sm, const SelArgs &a,
 }
 
 __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
+    pdl_prologue();
     extern __shared__ __align__(128) unsigned char dsm[];
     SelStagedSmem &sm = *reinterpret_cast<SelStagedSmem *>(dsm);
     const int32_t n32 = *a.n_dev;
@@ -343,9 +345,9 @@ static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
             return e;
         per_sm[dev] = b > 0 ? b : 1;
     }
-    k_select_staged<<<(unsigned)(L.sm_count * per_sm[dev]), kThreads, bytes, L.stream>>>(a);
+    e = launch_pdl(k_select_staged, (unsigned)(L.sm_count * per_sm[dev]), kThreads, bytes, L.stream, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
@@ -383,9 +385,9 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
-    k_select<<<(unsigned)(L.sm_count * per_sm), kThreads, 0, L.stream>>>(a);
+    const cudaError_t e = launch_pdl(k_select, (unsigned)(L.sm_count * per_sm), kThreads, 0, L.stream, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t select_take_error(int *code) {

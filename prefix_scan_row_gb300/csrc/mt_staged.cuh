@@ -392,6 +392,7 @@ struct Staged {
 
 template <class S, class Op, int ITEMS, int SUB, int THREADS>
 __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) k_scan_staged(SegArgs a) {
+    pdl_prologue();
     using G = Staged<S, Op, ITEMS, SUB, THREADS>;
     constexpr int E = G::E;
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -508,9 +509,10 @@ static cudaError_t launch_staged(const SegArgs &a, int64_t max_ctas, const Launc
         grid = max_ctas;
     if (grid < 1)
         grid = 1;
-    k_scan_staged<S, Op, ITEMS, SUB, THREADS><<<(unsigned)grid, THREADS, G::kSmemBytes, L.stream>>>(a);
+    e = launch_pdl(k_scan_staged<S, Op, ITEMS, SUB, THREADS>, (unsigned)grid, THREADS, G::kSmemBytes,
+                   L.stream, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace mt
