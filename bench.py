@@ -71,8 +71,9 @@ STEP_BYTES = sum(call_bytes(r, n, d) for _, r, n, d, _ in CALLS)
 STEP_ELEMS = sum(r * n for _, r, n, _, _ in CALLS)
 DOM_BYTES = call_bytes(*CALLS[0][1:4])
 
-KERNEL_SOURCES = ["prefix_scan_row_gb300/csrc/mt_tile.cuh", "prefix_scan_row_gb300/csrc/mt_lookback.cuh",
-                  "prefix_scan_row_gb300/csrc/mt_tilescan.cuh", "prefix_scan_row_gb300/csrc/mt_rows.cu"]
+KERNEL_SOURCES = ["prefix_scan_row_gb300/csrc/mt_internal.h", "prefix_scan_row_gb300/csrc/mt_tile.cuh",
+                  "prefix_scan_row_gb300/csrc/mt_lookback.cuh", "prefix_scan_row_gb300/csrc/mt_tilescan.cuh",
+                  "prefix_scan_row_gb300/csrc/mt_rows.cu"]
 PROFILE = "profiles/rows_bf16_8192x8192_excl.md"
 
 
