@@ -52,7 +52,8 @@ typedef enum {
     MT_ERR_CUDA = -4,             /* a CUDA runtime call or launch failed */
     MT_ERR_LOOKBACK_TIMEOUT = -5, /* device: a tile waited too long for a predecessor */
     MT_ERR_ALIGN = -6,            /* pointer not aligned to its element size */
-    MT_ERR_TOO_LARGE = -7         /* needs more than the fixed no-allocation scratch */
+    MT_ERR_TOO_LARGE = -7,        /* needs more than the fixed no-allocation scratch */
+    MT_ERR_MEMORY = -8            /* a pointer the call's kernels cannot reach (see each call) */
 } mt_status;
 
 /*
@@ -69,9 +70,18 @@ typedef enum {
  * arithmetic precision"). The f32 additions may be grouped differently from
  * a left-to-right loop; the element order is never permuted.
  *
- * inp, out : device pointers to rows*n elements, each aligned to the element
- *            size (any 16-byte misalignment of a row start is handled).
- *            inp == out (in place) is allowed; other overlaps are not.
+ * inp, out : pointers to rows*n elements, each aligned to the element size
+ *            (any 16-byte misalignment of a row start is handled). inp == out
+ *            (in place) is allowed; other overlaps are not. Device memory,
+ *            or -- for rows that fit in one tile (up to about 16384
+ *            elements) -- host memory the GPU can reach: pinned host memory
+ *            mapped at the same address (cudaHostAlloc / cudaHostRegister
+ *            under unified addressing), or any host memory where the device
+ *            reads pageable memory (cudaDevAttrPageableMemoryAccess, as on
+ *            Grace hosts). The kernels then read and write the host buffers
+ *            directly over the host link, with no staging copy. Longer rows
+ *            need device memory (their kernel moves data with bulk copies);
+ *            other host pointers return MT_ERR_MEMORY.
  * rows, n  : >= 0. rows*n == 0 is a no-op that returns MT_OK.
  * inclusive: nonzero for the inclusive form.
  *
@@ -81,7 +91,7 @@ typedef enum {
  * bytes) from a stream-ordered memory
  * pool owned by the library (cudaMallocFromPoolAsync / cudaFreeAsync on
  * `stream`); rows that fit in one tile use none.
- * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIGN, MT_ERR_CUDA.
+ * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIGN, MT_ERR_MEMORY, MT_ERR_CUDA.
  */
 int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
                  int inclusive, void *stream);
@@ -111,7 +121,8 @@ int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
  *            undefined behaviour and is not checked (as on the page).
  * Only out[0:n] is written; out[n:] is left untouched.
  * Two kernels are launched: a status reset and the single-pass scan.
- * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_ALIGN, MT_ERR_CUDA.
+ * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_ALIGN, MT_ERR_MEMORY (a
+ * pointer not in device memory), MT_ERR_CUDA.
  */
 int mt_exclusive_scan(const void *arr, void *out, void *scratch, const int32_t *n_dev,
                       int dtype, int op, void *stream);
@@ -132,7 +143,8 @@ int mt_exclusive_scan(const void *arr, void *out, void *scratch, const int32_t *
  *            8-byte slots, 16-byte aligned, no initialisation needed; not
  *            shared by concurrent calls.
  * n_dev    : device pointer to the int32 live count (n < 0 treated as 0).
- * Errors: MT_ERR_ARG, MT_ERR_ALIAS, MT_ERR_ALIGN, MT_ERR_CUDA.
+ * Errors: MT_ERR_ARG, MT_ERR_ALIAS, MT_ERR_ALIGN, MT_ERR_MEMORY (a pointer not
+ * in device memory), MT_ERR_CUDA.
  */
 int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
               void *scratch, const int32_t *n_dev, void *stream);
@@ -187,8 +199,9 @@ int mt_scan_debug_lookback(int64_t skip_publish_tile, uint32_t spin_limit);
  * Limit: the array holds MT_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that
  * loads the library, for the life of the process, which covers
  * rows * tiles_per_row <= 8191 tiles (a tile is 12288 f32 or 16384
- * bf16/f16 elements of a row; rows of at most 8192 elements use no tiles of
- * it). A larger call returns MT_ERR_TOO_LARGE and launches nothing.
+ * bf16/f16 elements of a row; rows that fit one CTA, up to about 16384
+ * elements, use none of it). A larger call returns MT_ERR_TOO_LARGE and
+ * launches nothing.
  * The first call on each device looks up the array's device address (a
  * cudaGetSymbolAddress call), so make that first call before any stream
  * capture. Every call uses the same array and clears the part it needs

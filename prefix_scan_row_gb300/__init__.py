@@ -32,6 +32,7 @@ MT_OK = 0
 MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_LOOKBACK_TIMEOUT, MT_ERR_ALIGN = (
     -1, -2, -3, -4, -5, -6)
 MT_ERR_TOO_LARGE = -7
+MT_ERR_MEMORY = -8
 MT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_F16,

@@ -1,6 +1,7 @@
 // mt_abi.cu -- the exported C ABI (include/mt_scan.h): argument checks,
 // scratch layout and reset, workspace for long rows, launch dispatch.
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "mt_internal.h"
@@ -111,6 +112,53 @@ static int elem_size(int dtype) {
     }
 }
 
+// Whether the kernels can dereference p: memory of device `dev`, managed
+// memory, pinned host memory mapped at the same address, or -- on devices
+// that read pageable host memory -- any host address. `host` reports host
+// memory.
+bool ptr_reachable(const void *p, int dev, bool *host) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        *host = true;
+        return false;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+        *host = false;
+        return a.device == dev;
+    case cudaMemoryTypeManaged:
+        *host = false;
+        return true;
+    case cudaMemoryTypeHost:
+        *host = true;
+        return a.devicePointer == p;
+    default: {  // unregistered host memory
+        *host = true;
+        static int pageable[128] = {0};  // 0 unknown, 1 yes, 2 no
+        if (dev < 0 || dev >= 128)
+            return false;
+        if (pageable[dev] == 0) {
+            int v = 0;
+            if (cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess)
+                v = 0;
+            pageable[dev] = v ? 1 : 2;
+        }
+        return pageable[dev] == 1;
+    }
+    }
+}
+
+// All of `ps` in device (or managed) memory.
+static bool all_device(std::initializer_list<const void *> ps, int dev) {
+    for (const void *p : ps) {
+        bool host = false;
+        if (!ptr_reachable(p, dev, &host) || host)
+            return false;
+    }
+    return true;
+}
+
 }  // namespace mt
 
 using namespace mt;
@@ -139,6 +187,11 @@ extern "C" int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n,
     int dev = 0;
     if (!make_launch(stream, &L, &dev))
         return MT_ERR_CUDA;
+    bool in_host = false, out_host = false;
+    if (!ptr_reachable(inp, dev, &in_host) || !ptr_reachable(out, dev, &out_host))
+        return MT_ERR_MEMORY;
+    if (p.staged && (in_host || out_host))
+        return MT_ERR_MEMORY;  // the long-row kernel bulk-copies from device memory only
     uint64_t *ws = nullptr;
     if (p.tiles_per_row > 1) {
         const int64_t nwords = kHeaderSlots + rows * p.tiles_per_row * rows_rec_slots();
@@ -173,8 +226,11 @@ extern "C" int mt_exclusive_scan(const void *arr, void *out, void *scratch, cons
         ((uintptr_t)n_dev % 4) != 0)
         return MT_ERR_ALIGN;
     Launch L;
-    if (!make_launch(stream, &L, nullptr))
+    int dev = 0;
+    if (!make_launch(stream, &L, &dev))
         return MT_ERR_CUDA;
+    if (!all_device({arr, out, scratch, n_dev}, dev))
+        return MT_ERR_MEMORY;  // the kernel bulk-copies from, and polls, device memory
     uint64_t *sw = static_cast<uint64_t *>(scratch);
     if (launch_reset(sw, 0, n_dev, scan1d_tile_elems(dtype), s, (int)((uintptr_t)arr & 15u),
                      scan1d_rec_slots(dtype), nullptr, L) != cudaSuccess)
@@ -195,8 +251,11 @@ extern "C" int mt_select(const void *arr, const uint8_t *flags, void *out, int32
         ((uintptr_t)scratch % 16) != 0 || ((uintptr_t)n_dev % 4) != 0)
         return MT_ERR_ALIGN;
     Launch L;
-    if (!make_launch(stream, &L, nullptr))
+    int dev = 0;
+    if (!make_launch(stream, &L, &dev))
         return MT_ERR_CUDA;
+    if (!all_device({arr, flags, out, num_out, scratch, n_dev}, dev))
+        return MT_ERR_MEMORY;
     uint64_t *sw = static_cast<uint64_t *>(scratch);
     if (launch_reset(sw, 0, n_dev, select_tile_elems(), 1, 0, select_rec_slots(), num_out, L) !=
         cudaSuccess)
@@ -252,6 +311,7 @@ extern "C" const char *mt_scan_strerror(int code) {
     case MT_ERR_LOOKBACK_TIMEOUT: return "look-back wait gave up (results invalid)";
     case MT_ERR_ALIGN: return "pointer misaligned";
     case MT_ERR_TOO_LARGE: return "needs more than the fixed no-allocation scratch (MT_NOALLOC_SCRATCH_BYTES)";
+    case MT_ERR_MEMORY: return "a pointer the kernels cannot reach (host memory where device memory is needed)";
     default: return "unknown status";
     }
 }

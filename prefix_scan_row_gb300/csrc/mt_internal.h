@@ -19,6 +19,10 @@ struct Launch {
 
 void note_launch();
 
+// Whether the kernels can dereference p on device `dev` (mt_abi.cu); `host`
+// is set for host memory.
+bool ptr_reachable(const void *p, int dev, bool *host);
+
 // ---- launches with programmatic stream serialization ----------------------
 // Every kernel of the library is launched so that its CTAs may be scheduled
 // while the previous kernel in the stream is still finishing, and starts with

@@ -94,6 +94,10 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&L.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return MT_ERR_CUDA;
+    bool in_host = false, out_host = false;
+    if (!ptr_reachable(inp, dev, &in_host) || !ptr_reachable(out, dev, &out_host) ||
+        (p.staged && (in_host || out_host)))
+        return MT_ERR_MEMORY;  // as mt_scan_rows
     L.skip_tile = -1;
     L.spin_limit = kDefaultSpin;
     if (nwords > 0) {
