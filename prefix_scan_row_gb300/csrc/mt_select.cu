@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
 struct SelStagedSmem {
     uint4 flags[kSelChunks];  // 16 flags per chunk
     uint32_t vals[kSelTE];    // the tile's values; each warp packs its selected ones in place
-    uint64_t bar;
+    uint64_t bar_f;           // the flags' copy
+    uint64_t bar_v;           // the values' copy
     int64_t tile;
     uint32_t red[kWarps];
     uint32_t prefix;
@@ -203,9 +204,11 @@ struct SelStagedSmem {
 // a range check. (Looking back before the packing, overlapped with it, was
 // measured slower: the look-back then meets more predecessors that have
 // only published their counts.)
+// Returns false when the values' copy did not complete in time (the caller
+// records the error and drains it).
 template <bool FULL>
-__device__ __forceinline__ void select_tile(SelStagedSmem &sm, const SelArgs &a, int64_t g, int64_t ntiles,
-                                            int elems) {
+__device__ __forceinline__ bool select_tile(SelStagedSmem &sm, const SelArgs &a, int64_t g, int64_t ntiles,
+                                            int elems, uint32_t phase) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // Count: popcounts of this thread's 16-flag chunks (flags past n are 0).
     uint32_t mine = 0u;
@@ -242,6 +245,13 @@ __device__ __forceinline__ void select_tile(SelStagedSmem &sm, const SelArgs &a,
     }
     publish_aggregate<uint32_t, OpAdd>(a.lb, g, 0, agg);
 
+    // The values were copied alongside the flags; their copy is the larger one.
+    bool ok = true;
+    if (threadIdx.x < 32)
+        ok = mbar_wait(&sm.bar_v, phase, kCopyWaitLimit);
+    if (__syncthreads_or(!ok))
+        return false;
+
     // Pack this warp's selected words in place, in element order. A write
     // goes to a slot at or before every element this warp reads later, and
     // a warp step reads all its lanes before any of them writes.
@@ -267,6 +277,7 @@ __device__ __forceinline__ void select_tile(SelStagedSmem &sm, const SelArgs &a,
         dst[i] = sm.vals[wstart + i];
     if (g == ntiles - 1 && threadIdx.x == 0)
         *a.num_out = (int32_t)(G + agg);
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
@@ -277,7 +288,8 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
     const int64_t n = n32 > 0 ? n32 : 0;
     const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
     if (threadIdx.x == 0) {
-        mbar_init(&sm.bar, 1);
+        mbar_init(&sm.bar_f, 1);
+        mbar_init(&sm.bar_v, 1);
         fence_mbar_init();
     }
     uint32_t phase = 0;
@@ -294,27 +306,32 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
             fence_proxy_async_smem();
             const uint32_t fb = (uint32_t)((elems + 15) / 16 * 16);
             const uint32_t vb = (uint32_t)(((int64_t)elems * 4 + 15) / 16 * 16);
-            mbar_arrive_expect_tx(&sm.bar, fb + vb);
-            bulk_g2s(&sm.flags[0], a.flags + t0, fb, &sm.bar);
-            bulk_g2s(&sm.vals[0], a.arr + t0, vb, &sm.bar);
+            mbar_arrive_expect_tx(&sm.bar_f, fb);
+            bulk_g2s(&sm.flags[0], a.flags + t0, fb, &sm.bar_f);
+            mbar_arrive_expect_tx(&sm.bar_v, vb);
+            bulk_g2s(&sm.vals[0], a.arr + t0, vb, &sm.bar_v);
         }
-        // Warp 0 waits for the copies; the block barrier passes the
-        // completion (and the copied bytes) on to the other warps.
+        // Warp 0 waits for the flags; the block barrier passes the
+        // completion (and the copied bytes) on to the other warps. The
+        // tile's count is published before the values are waited for.
         bool ok = true;
         if (threadIdx.x < 32)
-            ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
-        if (__syncthreads_or(!ok)) {
+            ok = mbar_wait(&sm.bar_f, phase, kCopyWaitLimit);
+        if (__syncthreads_or(!ok))
+            ok = false;  // every thread: the flags did not arrive
+        else
+            ok = (elems == kSelTE) ? select_tile<true>(sm, a, g, ntiles, elems, phase)
+                                   : select_tile<false>(sm, a, g, ntiles, elems, phase);
+        if (!ok) {  // block-uniform
             if (threadIdx.x == 0) {
                 atomicCAS(&g_mt_err, 0, kErrTimeout);
-                mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copies before leaving
+                // drain both copies before leaving
+                mbar_wait(&sm.bar_f, phase, kCopyWaitLimit);
+                mbar_wait(&sm.bar_v, phase, kCopyWaitLimit);
             }
             return;
         }
         phase ^= 1u;
-        if (elems == kSelTE)
-            select_tile<true>(sm, a, g, ntiles, elems);
-        else
-            select_tile<false>(sm, a, g, ntiles, elems);
         fence_proxy_async_smem();  // this thread's shared writes precede the next bulk copies
     }
 }
