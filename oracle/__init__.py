@@ -50,6 +50,10 @@ def lib():
         L.oracle_scan_rows.restype = i32
         L.oracle_exclusive_scan.argtypes = [p, p, p, p, i64, i32, i32]
         L.oracle_exclusive_scan.restype = i32
+        L.oracle_inclusive_scan.argtypes = [p, p, p, p, i64, i32, i32]
+        L.oracle_inclusive_scan.restype = i32
+        L.oracle_reduce.argtypes = [p, p, p, p, i64, i32, i32]
+        L.oracle_reduce.restype = i32
         L.oracle_select.argtypes = [p, p, p, i64]
         L.oracle_select.restype = i64
         L.oracle_decode_half.argtypes = [p, p, i64, i32]
@@ -120,6 +124,39 @@ def exclusive_scan(arr, n: int, dtype: str, op: str, want_f64: bool = False):
     if rc != 0:
         raise ValueError("oracle_exclusive_scan rejected its arguments")
     return (out, p64, m64) if f64 else out
+
+
+def inclusive_scan(arr, n: int, dtype: str, op: str, want_f64: bool = False):
+    """Inclusive scan of arr[0:n]: out[i] = op(arr[0..=i]); returns out[0:n]
+    (and prefix64/abs64 for f32 add when ``want_f64``)."""
+    d, o = DTYPES[dtype], OPS[op]
+    a = np.ascontiguousarray(_np(arr)[:n])
+    out = np.empty((n,), dtype=_SCAN_NP[d])
+    f64 = want_f64 and d == F32 and o == ADD
+    p64 = np.empty((n,), dtype=np.float64) if f64 else None
+    m64 = np.empty((n,), dtype=np.float64) if f64 else None
+    rc = lib().oracle_inclusive_scan(_ptr(a), _ptr(out), _ptr(p64) if f64 else None,
+                                     _ptr(m64) if f64 else None, n, d, o)
+    if rc != 0:
+        raise ValueError("oracle_inclusive_scan rejected its arguments")
+    return (out, p64, m64) if f64 else out
+
+
+def reduce(arr, n: int, dtype: str, op: str, want_f64: bool = False):
+    """op(arr[0:n]) as a numpy scalar of the dtype (the identity for n == 0);
+    with ``want_f64`` for f32 add also the fp64 sum and the sum of |x|."""
+    d, o = DTYPES[dtype], OPS[op]
+    a = np.ascontiguousarray(_np(arr)[:n])
+    if a.size == 0:
+        a = np.zeros((1,), dtype=_SCAN_NP[d])
+    out = np.empty((1,), dtype=_SCAN_NP[d])
+    s64 = np.zeros((1,), dtype=np.float64)
+    m64 = np.zeros((1,), dtype=np.float64)
+    rc = lib().oracle_reduce(_ptr(a), _ptr(out), _ptr(s64), _ptr(m64), n, d, o)
+    if rc != 0:
+        raise ValueError("oracle_reduce rejected its arguments")
+    f64 = want_f64 and d == F32 and o == ADD
+    return (out[0], float(s64[0]), float(m64[0])) if f64 else out[0]
 
 
 def select(arr, flags, n: int):

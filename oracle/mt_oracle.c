@@ -325,6 +325,165 @@ int oracle_exclusive_scan(const void *arr, void *out, double *prefix64, double *
 }
 
 /* ------------------------------------------------------------------------
+ * Inclusive form of the device-wide scan: out[i] = op(arr[0..=i]), the left
+ * prefix lp[i+1] of the recurrence lp[0] = identity, lp[i+1] = op(lp[i],
+ * arr[i]) ([tile] "Why not just infer it from reduce?"; [algos]
+ * PrefixSumExecutor: arr[i] = sum(arr_original[0..=i])). Only out[0:n] is
+ * written. For f32 add, `out` gets the fp64 prefix rounded to f32 and, when
+ * non-null, `prefix64` / `abs64` the fp64 prefix and the running sum of |x_j|
+ * for j <= i. Returns 0, or -1 on a bad argument.
+ * ---------------------------------------------------------------------- */
+int oracle_inclusive_scan(const void *arr, void *out, double *prefix64, double *abs64,
+                          int64_t n, int dtype, int op)
+{
+    if (n < 0 || op < OR_ADD || op > OR_MAX)
+        return -1;
+    if (dtype == OR_I32) {
+        const int32_t *x = (const int32_t *)arr;
+        int32_t *y = (int32_t *)out;
+        if (op == OR_ADD) {
+            uint32_t lp = 0; /* unsigned: wraps modulo 2^32 */
+            for (int64_t i = 0; i < n; ++i) {
+                lp += (uint32_t)x[i];
+                int32_t v;
+                memcpy(&v, &lp, 4);
+                y[i] = v;
+            }
+        } else {
+            int32_t lp = (op == OR_MIN) ? INT32_MAX : INT32_MIN;
+            for (int64_t i = 0; i < n; ++i) {
+                if (op == OR_MIN)
+                    lp = (x[i] < lp) ? x[i] : lp;
+                else
+                    lp = (x[i] > lp) ? x[i] : lp;
+                y[i] = lp;
+            }
+        }
+        return 0;
+    }
+    if (dtype == OR_I64) {
+        const int64_t *x = (const int64_t *)arr;
+        int64_t *y = (int64_t *)out;
+        if (op == OR_ADD) {
+            uint64_t lp = 0; /* wraps modulo 2^64 */
+            for (int64_t i = 0; i < n; ++i) {
+                lp += (uint64_t)x[i];
+                int64_t v;
+                memcpy(&v, &lp, 8);
+                y[i] = v;
+            }
+        } else {
+            int64_t lp = (op == OR_MIN) ? INT64_MAX : INT64_MIN;
+            for (int64_t i = 0; i < n; ++i) {
+                if (op == OR_MIN)
+                    lp = (x[i] < lp) ? x[i] : lp;
+                else
+                    lp = (x[i] > lp) ? x[i] : lp;
+                y[i] = lp;
+            }
+        }
+        return 0;
+    }
+    if (dtype == OR_F32) {
+        const float *x = (const float *)arr;
+        float *y = (float *)out;
+        if (op == OR_ADD) {
+            double lp = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < n; ++i) {
+                lp += (double)x[i];
+                mag += fabs((double)x[i]);
+                if (y)
+                    y[i] = (float)lp;
+                if (prefix64)
+                    prefix64[i] = lp;
+                if (abs64)
+                    abs64[i] = mag;
+            }
+        } else {
+            float lp = (op == OR_MIN) ? INFINITY : -INFINITY;
+            for (int64_t i = 0; i < n; ++i) {
+                if (op == OR_MIN)
+                    lp = (x[i] < lp) ? x[i] : lp;
+                else
+                    lp = (x[i] > lp) ? x[i] : lp;
+                y[i] = lp;
+            }
+        }
+        return 0;
+    }
+    return -1;
+}
+
+/* ------------------------------------------------------------------------
+ * Device-wide reduction ([algos] reduce_{add,min,max}): out[0] =
+ * op(arr[0:n]), the identity of (op, dtype) when n == 0 -- the left prefix
+ * lp[n] of the same recurrence. For f32 add, out[0] is the fp64 sum rounded
+ * to f32 and, when non-null, *sum64 / *abs64 receive the fp64 sum and the sum
+ * of |x_j|. Returns 0, or -1 on a bad argument.
+ * ---------------------------------------------------------------------- */
+int oracle_reduce(const void *arr, void *out, double *sum64, double *abs64, int64_t n, int dtype,
+                  int op)
+{
+    if (n < 0 || op < OR_ADD || op > OR_MAX)
+        return -1;
+    if (dtype == OR_I32) {
+        const int32_t *x = (const int32_t *)arr;
+        int32_t r;
+        if (op == OR_ADD) {
+            uint32_t acc = 0;
+            for (int64_t i = 0; i < n; ++i)
+                acc += (uint32_t)x[i];
+            memcpy(&r, &acc, 4);
+        } else {
+            r = (op == OR_MIN) ? INT32_MAX : INT32_MIN;
+            for (int64_t i = 0; i < n; ++i)
+                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);
+        }
+        memcpy(out, &r, 4);
+        return 0;
+    }
+    if (dtype == OR_I64) {
+        const int64_t *x = (const int64_t *)arr;
+        int64_t r;
+        if (op == OR_ADD) {
+            uint64_t acc = 0;
+            for (int64_t i = 0; i < n; ++i)
+                acc += (uint64_t)x[i];
+            memcpy(&r, &acc, 8);
+        } else {
+            r = (op == OR_MIN) ? INT64_MAX : INT64_MIN;
+            for (int64_t i = 0; i < n; ++i)
+                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);
+        }
+        memcpy(out, &r, 8);
+        return 0;
+    }
+    if (dtype == OR_F32) {
+        const float *x = (const float *)arr;
+        float r;
+        if (op == OR_ADD) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < n; ++i) {
+                acc += (double)x[i];
+                mag += fabs((double)x[i]);
+            }
+            r = (float)acc;
+            if (sum64)
+                *sum64 = acc;
+            if (abs64)
+                *abs64 = mag;
+        } else {
+            r = (op == OR_MIN) ? INFINITY : -INFINITY;
+            for (int64_t i = 0; i < n; ++i)
+                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);
+        }
+        memcpy(out, &r, 4);
+        return 0;
+    }
+    return -1;
+}
+
+/* ------------------------------------------------------------------------
  * Stream compaction ([algos] select): every arr[i] whose flag is 1 goes to
  * the next slot of out, in input order; the count is returned. Elements are
  * copied as raw 4-byte words (the scatter ignores the element type).

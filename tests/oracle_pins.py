@@ -368,6 +368,124 @@ def pin_scan_brute_force():
                         assert got == want, (n, dt, op, i)
 
 
+def pin_inclusive_golden():
+    g = load_all()
+    ex = g["algos_inclusive_scan_add_i32"]
+    tile = g["tile_inclusive_order"]
+    for dt in ("i32", "i64", "f32"):
+        arr = np.array(ex["arr"], dtype=_NP[dt])
+        assert oracle.inclusive_scan(arr, len(arr), dt, "add").tolist() == ex["inclusive"], dt
+        assert oracle.inclusive_scan(arr, len(arr), dt, "min").tolist() == ex["inclusive_min"], dt
+        assert oracle.inclusive_scan(arr, len(arr), dt, "max").tolist() == ex["inclusive_max"], dt
+        for a, b in (("x_a", "inclusive_a"), ("x_b", "inclusive_b")):
+            x = np.array(tile[a], dtype=_NP[dt])
+            assert oracle.inclusive_scan(x, len(x), dt, "add").tolist() == tile[b], (dt, a)
+
+
+def pin_inclusive_brute_force():
+    rng = np.random.default_rng(29)
+    for n in (0, 1, 2, 5, 33, 64):
+        for dt in ("i32", "i64", "f32"):
+            if dt == "f32":
+                x = (rng.integers(-4096, 4096, n) / 1024.0).astype(np.float32)
+            else:
+                x = rng.integers(-1000, 1000, n).astype(_NP[dt])
+            for op in ("add", "min", "max"):
+                out = oracle.inclusive_scan(x, n, dt, op)
+                assert out.shape == (n,)
+                for i in range(n):
+                    head = [x[j].item() for j in range(i + 1)]
+                    if op == "add":
+                        assert Fraction(out[i].item()) == sum(Fraction(v) for v in head), (n, dt, i)
+                    elif op == "min":
+                        assert out[i].item() == min(head), (n, dt, i)
+                    else:
+                        assert out[i].item() == max(head), (n, dt, i)
+
+
+def pin_inclusive_library():
+    rng = np.random.default_rng(31)
+    n = 20000
+    for dt in ("i32", "i64", "f32"):
+        if dt == "i32":
+            x = rng.integers(-(2**31), 2**31, n, dtype=np.int64).astype(np.int32)
+        elif dt == "i64":
+            x = rng.integers(-(2**62), 2**62, n, dtype=np.int64)
+        else:
+            x = rng.uniform(-1, 1, n).astype(np.float32)
+        assert np.array_equal(oracle.inclusive_scan(x, n, dt, "min"), np.minimum.accumulate(x))
+        assert np.array_equal(oracle.inclusive_scan(x, n, dt, "max"), np.maximum.accumulate(x))
+        if dt == "i32":
+            want = (np.cumsum(x.astype(np.int64)) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
+            assert np.array_equal(oracle.inclusive_scan(x, n, dt, "add"), want)
+        elif dt == "i64":
+            with np.errstate(over="ignore"):
+                want = np.cumsum(x)
+            assert np.array_equal(oracle.inclusive_scan(x, n, dt, "add"), want)
+        else:
+            out, p64, mag = oracle.inclusive_scan(x, n, dt, "add", want_f64=True)
+            want = np.cumsum(x.astype(np.float64))
+            assert np.array_equal(p64, want)
+            assert np.array_equal(out, want.astype(np.float32))
+            assert np.allclose(mag, np.cumsum(np.abs(x.astype(np.float64))), rtol=1e-13, atol=0)
+
+
+def pin_reduce_golden_and_identities():
+    red = load_all()["algos_reduce_i32"]
+    for dt in ("i32", "i64", "f32"):
+        arr = np.array(red["arr"], dtype=_NP[dt])
+        for op in ("add", "min", "max"):
+            assert oracle.reduce(arr, len(arr), dt, op) == red[op], (dt, op)
+            assert oracle.reduce(arr, 0, dt, op) == _IDENT[(dt, op)], (dt, op)
+            assert oracle.reduce(arr, 1, dt, op) == red["arr"][0], (dt, op)
+    a = np.array([I32_MAX, 1], dtype=np.int32)
+    assert oracle.reduce(a, 2, "i32", "add") == I32_MIN  # wraps
+    b = np.array([I64_MAX, 1], dtype=np.int64)
+    assert oracle.reduce(b, 2, "i64", "add") == I64_MIN
+
+
+def pin_reduce_library():
+    rng = np.random.default_rng(37)
+    for n in (1, 7, 1000, 50001):
+        for dt in ("i32", "i64", "f32"):
+            if dt == "i32":
+                x = rng.integers(-(2**31), 2**31, n, dtype=np.int64).astype(np.int32)
+            elif dt == "i64":
+                x = rng.integers(-(2**62), 2**62, n, dtype=np.int64)
+            else:
+                x = rng.uniform(-1, 1, n).astype(np.float32)
+            assert oracle.reduce(x, n, dt, "min") == x.min()
+            assert oracle.reduce(x, n, dt, "max") == x.max()
+            if dt == "i32":
+                want = int(x.astype(np.int64).sum()) & 0xFFFFFFFF
+                want = want - 2**32 if want >= 2**31 else want
+                assert int(oracle.reduce(x, n, dt, "add")) == want
+            elif dt == "i64":
+                want = (int(sum(int(v) for v in x)) + 2**63) % 2**64 - 2**63
+                assert int(oracle.reduce(x, n, dt, "add")) == want
+            else:
+                r, s64, m64 = oracle.reduce(x, n, dt, "add", want_f64=True)
+                seq = np.cumsum(x.astype(np.float64))[-1]  # the same left-to-right order
+                assert s64 == seq and r == np.float32(seq)
+                assert abs(m64 - np.abs(x.astype(np.float64)).sum()) <= 1e-12 * m64
+
+
+def pin_reduce_signed_zero_ties():
+    """min/max keep the earliest of equal values: the sign of a zero result
+    is that of the first zero."""
+    pz, nz = np.float32(0.0), np.float32(-0.0)
+    for first, second in ((pz, nz), (nz, pz)):
+        x = np.array([1.0, first, 2.0, second], dtype=np.float32)
+        for op in ("min",):
+            r = oracle.reduce(x, 4, "f32", op)
+            assert r == 0 and np.signbit(r) == np.signbit(first)
+        y = np.array([-1.0, first, -2.0, second], dtype=np.float32)
+        r = oracle.reduce(y, 4, "f32", "max")
+        assert r == 0 and np.signbit(r) == np.signbit(first)
+        inc = oracle.inclusive_scan(x, 4, "f32", "min")
+        assert np.signbit(inc[3]) == np.signbit(first)
+
+
 # ---------------------------------------------------------------------------
 # Select
 # ---------------------------------------------------------------------------

@@ -31,6 +31,29 @@ MUTANTS = {
                                    "v = ldexp((double)m, -bias - f.frac_bits);"),
     "f32_store_perturbed": ("float f = (float)v;", "float f = (float)(v * (1.0 + 1e-7));"),
     "select_skips_first": ("if (flags[i] == 1) {", "if (flags[i] == 1 && i > 0) {"),
+    "inclusive_stores_before_update": (
+        "                lp += (uint32_t)x[i];\n                int32_t v;\n"
+        "                memcpy(&v, &lp, 4);\n                y[i] = v;",
+        "                int32_t v;\n                memcpy(&v, &lp, 4);\n"
+        "                y[i] = v;\n                lp += (uint32_t)x[i];"),
+    "inclusive_f32_min_keeps_later": (
+        "            float lp = (op == OR_MIN) ? INFINITY : -INFINITY;\n"
+        "            for (int64_t i = 0; i < n; ++i) {\n                if (op == OR_MIN)\n"
+        "                    lp = (x[i] < lp) ? x[i] : lp;\n                else\n"
+        "                    lp = (x[i] > lp) ? x[i] : lp;\n                y[i] = lp;",
+        "            float lp = (op == OR_MIN) ? INFINITY : -INFINITY;\n"
+        "            for (int64_t i = 0; i < n; ++i) {\n                if (op == OR_MIN)\n"
+        "                    lp = (x[i] <= lp) ? x[i] : lp;\n                else\n"
+        "                    lp = (x[i] > lp) ? x[i] : lp;\n                y[i] = lp;"),
+    "reduce_drops_last": ("            for (int64_t i = 0; i < n; ++i)\n                acc += (uint32_t)x[i];",
+                          "            for (int64_t i = 0; i + 1 < n; ++i)\n                acc += (uint32_t)x[i];"),
+    "reduce_f32_max_keeps_later": (
+        "            r = (op == OR_MIN) ? INFINITY : -INFINITY;\n            for (int64_t i = 0; i < n; ++i)\n"
+        "                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);",
+        "            r = (op == OR_MIN) ? INFINITY : -INFINITY;\n            for (int64_t i = 0; i < n; ++i)\n"
+        "                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] >= r) ? x[i] : r);"),
+    "reduce_wrong_min_identity": ("            r = (op == OR_MIN) ? INT64_MAX : INT64_MIN;",
+                                  "            r = (op == OR_MIN) ? INT64_MAX : 0;"),
 }
 
 
