@@ -487,7 +487,8 @@ def run_suite(args):
     tag = "n=2^28-12345" if args.scale == 1 else f"n=(2^28-12345)/{args.scale}"
     n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
     for d, tdt, s in (("i32", torch.int32, 4), ("f32", torch.float32, 4), ("i64", torch.int64, 8)):
-        if not any(wanted(f"exclusive_scan {d} {op} {tag}") for op in ("add", "min", "max")):
+        if not any(wanted(f"{k} {d} {op} {tag}") for op in ("add", "min", "max")
+                   for k in ("exclusive_scan", "inclusive_scan", "reduce")):
             continue
         a = workloads.scan1d(d, capacity=cap).to(dev)
         o = torch.empty_like(a)
@@ -495,7 +496,15 @@ def run_suite(args):
         for op in ("add", "min", "max"):
             timeit(f"exclusive_scan {d} {op} {tag}",
                    lambda: mt.mt_exclusive_scan(a, o, scr, n_dev, op), 2 * s * n, n)
-        del a, o, scr
+        for op in ("add", "min", "max"):
+            timeit(f"inclusive_scan {d} {op} {tag}",
+                   lambda: mt.mt_inclusive_scan(a, o, scr, n_dev, op), 2 * s * n, n)
+        rscr = mt.alloc_scratch(cap, tdt, mt.MT_SCRATCH_REDUCE, device=dev)
+        r1 = torch.empty(1, dtype=tdt, device=dev)
+        for op in ("add", "min", "max"):
+            timeit(f"reduce {d} {op} {tag}",
+                   lambda: mt.mt_reduce(a, r1, rscr, n_dev, op), s * n, n)
+        del a, o, scr, rscr, r1
     ns = workloads.SELECT_N // args.scale
     nd = torch.tensor([ns], dtype=torch.int32, device=dev)
     for p in (0.5, 0.01):

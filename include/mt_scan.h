@@ -41,7 +41,8 @@ typedef enum { MT_ADD = 0, MT_MIN = 1, MT_MAX = 2 } mt_op;
 
 typedef enum {
     MT_SCRATCH_SCAN = 1,   /* for mt_exclusive_scan */
-    MT_SCRATCH_SELECT = 2  /* for mt_select */
+    MT_SCRATCH_SELECT = 2, /* for mt_select */
+    MT_SCRATCH_REDUCE = 3  /* for mt_reduce */
 } mt_scratch_kind;
 
 typedef enum {
@@ -128,6 +129,41 @@ int mt_exclusive_scan(const void *arr, void *out, void *scratch, const int32_t *
                       int dtype, int op, void *stream);
 
 /*
+ * mt_inclusive_scan -- the inclusive form of mt_exclusive_scan:
+ *   out[i] = op(arr[0], ..., arr[i])
+ * (the left prefix lp[i+1] of [tile] "Why not just infer it from reduce?";
+ * [algos] "qd.algorithms.PrefixSumExecutor": arr[i] = sum(arr_original[0..=i]),
+ * there for i32 add only and in place). Same dtypes, ops, tie rule,
+ * identity, scratch (MT_SCRATCH_SCAN) and live-count rules as
+ * mt_exclusive_scan, except that out == arr (in place) is allowed: every
+ * tile is read into shared memory before any of it is written.
+ * Errors: as mt_exclusive_scan, without MT_ERR_ALIAS.
+ */
+int mt_inclusive_scan(const void *arr, void *out, void *scratch, const int32_t *n_dev,
+                      int dtype, int op, void *stream);
+
+/*
+ * mt_reduce -- device-wide reduction ([algos] "qd.algorithms.reduce_{add,min,max}"):
+ *   out[0] = op(arr[0], ..., arr[n-1]),  the identity of (op, dtype) for n <= 0.
+ * Same dtypes, ops, identities and tie rule as mt_exclusive_scan (for f32
+ * min/max the result is the earliest element equal to the extreme, so a zero
+ * result carries the sign of the first zero). f32 add is summed in f32 in a
+ * fixed grouping (the same bits on every call on the same GPU).
+ *
+ * arr      : device array of `dtype` (MT_I32, MT_I64 or MT_F32), aligned to
+ *            the element size.
+ * out      : device pointer to one element of `dtype`.
+ * scratch  : device memory of mt_scan_scratch_slots(capacity, dtype,
+ *            MT_SCRATCH_REDUCE) 8-byte slots (a fixed size: the header and one
+ *            partial per CTA), 8-byte aligned; no initialisation needed.
+ * n_dev    : device pointer to the int32 live count n, read on the device.
+ * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIGN, MT_ERR_MEMORY (a pointer not
+ * in device memory), MT_ERR_CUDA.
+ */
+int mt_reduce(const void *arr, void *out, void *scratch, const int32_t *n_dev, int dtype, int op,
+              void *stream);
+
+/*
  * mt_select -- stream compaction ([algos] "qd.algorithms.select"): every
  * arr[i] with flags[i] == 1 is copied, in input order, into a dense prefix of
  * out, and the number copied is written to *num_out. Elements are 4-byte
@@ -151,11 +187,12 @@ int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out
 
 /*
  * mt_scan_scratch_slots -- number of 8-byte scratch slots that
- * mt_exclusive_scan (kind MT_SCRATCH_SCAN, with its dtype) or mt_select
- * (kind MT_SCRATCH_SELECT, dtype ignored) needs for any live count up to
- * `capacity`. Plain host arithmetic, no device access ([algos] "Scratch
- * space": ask first, then allocate). Returns -1 for a negative capacity or
- * an unknown kind/dtype.
+ * mt_exclusive_scan / mt_inclusive_scan (kind MT_SCRATCH_SCAN, with their
+ * dtype), mt_select (kind MT_SCRATCH_SELECT, dtype ignored) or mt_reduce
+ * (kind MT_SCRATCH_REDUCE, with its dtype; the same size for every
+ * capacity) needs for any live count up to `capacity`. Plain host
+ * arithmetic, no device access ([algos] "Scratch space": ask first, then
+ * allocate). Returns -1 for a negative capacity or an unknown kind/dtype.
  */
 int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind);
 

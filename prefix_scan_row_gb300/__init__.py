@@ -12,6 +12,9 @@ Names and arguments follow the C ABI:
   [rows, n] f32/bf16/f16 CUDA tensor.
 * ``mt_exclusive_scan(arr, out, scratch, n_dev, op)`` -- device-wide exclusive
   add/min/max over i32/i64/f32 with the live count in a device int32.
+* ``mt_inclusive_scan(arr, out, scratch, n_dev, op)`` -- the inclusive form
+  (in place allowed).
+* ``mt_reduce(arr, out, scratch, n_dev, op)`` -- out[0] = op(arr[0:n]).
 * ``mt_select(arr, flags, out, num_out, scratch, n_dev)`` -- stream compaction.
 * ``mt_scan_scratch_slots(capacity, dtype, kind)`` -- scratch sizing.
 """
@@ -27,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "libmtscan.so")
 
 MT_F32, MT_BF16, MT_F16, MT_I32, MT_I64 = 0, 1, 2, 3, 4
 MT_ADD, MT_MIN, MT_MAX = 0, 1, 2
-MT_SCRATCH_SCAN, MT_SCRATCH_SELECT = 1, 2
+MT_SCRATCH_SCAN, MT_SCRATCH_SELECT, MT_SCRATCH_REDUCE = 1, 2, 3
 MT_OK = 0
 MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_LOOKBACK_TIMEOUT, MT_ERR_ALIGN = (
     -1, -2, -3, -4, -5, -6)
@@ -39,7 +42,8 @@ DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_
               torch.int32: MT_I32, torch.int64: MT_I64}
 OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX}
 
-EXPORTS = ("mt_scan_rows", "mt_exclusive_scan", "mt_select", "mt_scan_scratch_slots",
+EXPORTS = ("mt_scan_rows", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",
+           "mt_scan_scratch_slots",
            "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback",
            "mt_scan_rows_noalloc")
 
@@ -61,6 +65,10 @@ def _load():
     L.mt_scan_rows.restype = i32
     L.mt_exclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_exclusive_scan.restype = i32
+    L.mt_inclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
+    L.mt_inclusive_scan.restype = i32
+    L.mt_reduce.argtypes = [p, p, p, p, i32, i32, p]
+    L.mt_reduce.restype = i32
     L.mt_select.argtypes = [p, p, p, p, p, p, p]
     L.mt_select.restype = i32
     L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
@@ -127,6 +135,30 @@ def mt_exclusive_scan(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tenso
     code = DTYPE_CODE.get(arr.dtype, -99)
     _check(lib.mt_exclusive_scan(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code,
                                  OP_CODE[op], _stream(stream)), "mt_exclusive_scan")
+
+
+def mt_inclusive_scan(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor,
+                      n_dev: torch.Tensor, op: str, stream=None) -> None:
+    """Inclusive scan of arr[0:*n_dev] into out (out may be arr)."""
+    if out.dtype != arr.dtype:
+        raise ValueError("out must have arr's dtype")
+    if n_dev.dtype != torch.int32:
+        raise ValueError("n_dev must be an int32 device tensor")
+    code = DTYPE_CODE.get(arr.dtype, -99)
+    _check(lib.mt_inclusive_scan(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code,
+                                 OP_CODE[op], _stream(stream)), "mt_inclusive_scan")
+
+
+def mt_reduce(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor, n_dev: torch.Tensor,
+              op: str, stream=None) -> None:
+    """out[0] = op(arr[0:*n_dev]) (the identity for an empty input)."""
+    if out.dtype != arr.dtype:
+        raise ValueError("out must have arr's dtype")
+    if n_dev.dtype != torch.int32:
+        raise ValueError("n_dev must be an int32 device tensor")
+    code = DTYPE_CODE.get(arr.dtype, -99)
+    _check(lib.mt_reduce(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code, OP_CODE[op],
+                         _stream(stream)), "mt_reduce")
 
 
 def mt_select(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out: torch.Tensor,

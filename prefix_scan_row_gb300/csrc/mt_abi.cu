@@ -211,15 +211,16 @@ extern "C" int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n,
     return e == cudaSuccess ? MT_OK : MT_ERR_CUDA;
 }
 
-extern "C" int mt_exclusive_scan(const void *arr, void *out, void *scratch, const int32_t *n_dev,
-                                 int dtype, int op, void *stream) {
+// The exclusive and inclusive 1-D scans share their checks and kernel.
+static int scan1d_call(const void *arr, void *out, void *scratch, const int32_t *n_dev, int dtype,
+                       int op, bool inclusive, void *stream) {
     if (dtype != MT_F32 && dtype != MT_I32 && dtype != MT_I64)
         return MT_ERR_DTYPE;
     if (op < MT_ADD || op > MT_MAX)
         return MT_ERR_ARG;
     if (arr == nullptr || out == nullptr || scratch == nullptr || n_dev == nullptr)
         return MT_ERR_ARG;
-    if (arr == out)
+    if (arr == out && !inclusive)
         return MT_ERR_ALIAS;
     const int s = elem_size(dtype);
     if (((uintptr_t)arr % s) != 0 || ((uintptr_t)out % s) != 0 || ((uintptr_t)scratch % 16) != 0 ||
@@ -236,8 +237,43 @@ extern "C" int mt_exclusive_scan(const void *arr, void *out, void *scratch, cons
                      scan1d_rec_slots(dtype), nullptr, L) != cudaSuccess)
         return MT_ERR_CUDA;
     const bool aligned_io = (((uintptr_t)arr - (uintptr_t)out) % 16) == 0;
-    return scan1d_launch(arr, out, sw, n_dev, dtype, op, aligned_io, L) == cudaSuccess ? MT_OK
-                                                                                      : MT_ERR_CUDA;
+    return scan1d_launch(arr, out, sw, n_dev, dtype, op, inclusive, aligned_io, L) == cudaSuccess
+               ? MT_OK
+               : MT_ERR_CUDA;
+}
+
+extern "C" int mt_exclusive_scan(const void *arr, void *out, void *scratch, const int32_t *n_dev,
+                                 int dtype, int op, void *stream) {
+    return scan1d_call(arr, out, scratch, n_dev, dtype, op, false, stream);
+}
+
+extern "C" int mt_inclusive_scan(const void *arr, void *out, void *scratch, const int32_t *n_dev,
+                                 int dtype, int op, void *stream) {
+    return scan1d_call(arr, out, scratch, n_dev, dtype, op, true, stream);
+}
+
+extern "C" int mt_reduce(const void *arr, void *out, void *scratch, const int32_t *n_dev, int dtype,
+                         int op, void *stream) {
+    if (dtype != MT_F32 && dtype != MT_I32 && dtype != MT_I64)
+        return MT_ERR_DTYPE;
+    if (op < MT_ADD || op > MT_MAX)
+        return MT_ERR_ARG;
+    if (arr == nullptr || out == nullptr || scratch == nullptr || n_dev == nullptr)
+        return MT_ERR_ARG;
+    const int s = elem_size(dtype);
+    if (((uintptr_t)arr % s) != 0 || ((uintptr_t)out % s) != 0 || ((uintptr_t)scratch % 8) != 0 ||
+        ((uintptr_t)n_dev % 4) != 0)
+        return MT_ERR_ALIGN;
+    Launch L;
+    int dev = 0;
+    if (!make_launch(stream, &L, &dev))
+        return MT_ERR_CUDA;
+    if (!all_device({arr, out, scratch, n_dev}, dev))
+        return MT_ERR_MEMORY;
+    uint64_t *sw = static_cast<uint64_t *>(scratch);
+    if (launch_reset(sw, kHeaderSlots, nullptr, 0, 1, 0, 1, nullptr, L) != cudaSuccess)
+        return MT_ERR_CUDA;  // the ticket counter; the partials need no clearing
+    return reduce_launch(arr, out, sw, n_dev, dtype, op, L) == cudaSuccess ? MT_OK : MT_ERR_CUDA;
 }
 
 extern "C" int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
@@ -281,6 +317,8 @@ extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) 
         const int64_t te = select_tile_elems();
         return kHeaderSlots + (capacity + te - 1) / te * select_rec_slots();
     }
+    if (kind == MT_SCRATCH_REDUCE)
+        return elem_size(dtype) > 0 && dtype != MT_BF16 && dtype != MT_F16 ? reduce_scratch_slots() : -1;
     return -1;
 }
 

@@ -73,8 +73,13 @@ int rows_rec_slots();  // 8-byte slots per look-back record of a long row
 int64_t scan1d_tile_elems(int dtype);
 int scan1d_rec_slots(int dtype);
 cudaError_t scan1d_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
-                          int dtype, int op, bool aligned_io, const Launch &L);
+                          int dtype, int op, bool inclusive, bool aligned_io, const Launch &L);
 cudaError_t scan1d_take_error(int *code);
+
+// ---- device-wide reduction (mt_reduce.cu) ---------------------------------
+int64_t reduce_scratch_slots();  // fixed: header + one partial per CTA
+cudaError_t reduce_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
+                          int dtype, int op, const Launch &L);
 
 // ---- select (mt_select.cu) ------------------------------------------------
 int64_t select_tile_elems();

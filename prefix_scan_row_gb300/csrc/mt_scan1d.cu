@@ -1,5 +1,5 @@
-// mt_scan1d.cu -- device-wide exclusive scan (add / min / max over i32, i64
-// and f32) with the live count read on the device.
+// mt_scan1d.cu -- device-wide exclusive and inclusive scans (add / min / max
+// over i32, i64 and f32) with the live count read on the device.
 //
 // Semantics follow the Quadrants "Algorithms" user guide, section
 // "qd.algorithms.exclusive_scan_{add,min,max}": out[i] = op(arr[0:i]), out[0]
@@ -68,7 +68,7 @@ static cudaError_t launch_op(int op, const SegArgs &a, const Launch &L) {
 }
 
 cudaError_t scan1d_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
-                          int dtype, int op, bool aligned_io, const Launch &L) {
+                          int dtype, int op, bool inclusive, bool aligned_io, const Launch &L) {
     SegArgs a;
     a.in = static_cast<const char *>(arr);
     a.out = static_cast<char *>(out);
@@ -77,7 +77,7 @@ cudaError_t scan1d_launch(const void *arr, void *out, uint64_t *scratch, const i
     a.tpr = 0;
     a.n_dev = n_dev;
     a.counter = reinterpret_cast<unsigned long long *>(scratch);
-    a.inclusive = 0;
+    a.inclusive = inclusive ? 1 : 0;
     a.aligned_io = aligned_io ? 1 : 0;
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;

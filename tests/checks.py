@@ -53,20 +53,36 @@ def assert_rows_close(gpu_out: torch.Tensor, x_cpu: torch.Tensor, dtype: str, in
                              f"err {err[i]} bound {bound[i]}")
 
 
-def assert_scan_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dtype: str, op: str):
-    """1-D exclusive scan of arr[0:n]: bit-exact except f32 add (tolerance)."""
+def assert_scan_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dtype: str, op: str,
+                        inclusive: bool = False):
+    """1-D exclusive (or inclusive) scan of arr[0:n]: bit-exact except f32 add
+    (tolerance)."""
+    scan = oracle.inclusive_scan if inclusive else oracle.exclusive_scan
     got = gpu_out[:n].detach().to("cpu").numpy()
     if dtype == "f32" and op == "add":
-        _, p64, mag = oracle.exclusive_scan(arr_cpu, n, dtype, op, want_f64=True)
+        _, p64, mag = scan(arr_cpu, n, dtype, op, want_f64=True)
         err = np.abs(got.astype(np.float64) - p64)
         bound = REL * mag + ABS
         bad = np.nonzero(~(err <= bound))[0]
         assert bad.size == 0, f"{bad.size} out of tolerance; first {bad[0]}: {got[bad[0]]} vs {p64[bad[0]]}"
         return
-    ref = oracle.exclusive_scan(arr_cpu, n, dtype, op)
+    ref = scan(arr_cpu, n, dtype, op)
     w = {"i32": np.uint32, "f32": np.uint32, "i64": np.uint64}[dtype]
     bad = np.nonzero(got.view(w) != ref.view(w))[0]
     assert bad.size == 0, f"{bad.size} mismatches; first at {bad[0]}: {got[bad[0]]} vs {ref[bad[0]]}"
+
+
+def assert_reduce_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dtype: str, op: str):
+    """out[0] of a reduction: bit-exact except f32 add, which must lie within
+    REL * sum|x| + ABS of the fp64 sum."""
+    got = gpu_out[:1].detach().to("cpu").numpy()[0]
+    if dtype == "f32" and op == "add":
+        _, s64, m64 = oracle.reduce(arr_cpu, n, dtype, op, want_f64=True)
+        assert abs(float(got) - s64) <= REL * m64 + ABS, f"{got} vs {s64} (sum|x| {m64})"
+        return
+    ref = oracle.reduce(arr_cpu, n, dtype, op)
+    w = {"i32": np.uint32, "f32": np.uint32, "i64": np.uint64}[dtype]
+    assert np.array([got]).view(w)[0] == np.array([ref]).view(w)[0], f"{got} vs {ref}"
 
 
 def assert_select_matches(gpu_out: torch.Tensor, gpu_num: torch.Tensor, arr_cpu, flags_cpu, n: int):

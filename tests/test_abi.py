@@ -23,6 +23,8 @@ def lib():
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.mt_scan_rows.argtypes = [p, p, i64, i64, i32, i32, p]
     L.mt_exclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
+    L.mt_inclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
+    L.mt_reduce.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_select.argtypes = [p, p, p, p, p, p, p]
     L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
     L.mt_scan_scratch_slots.restype = i64
@@ -86,6 +88,17 @@ def test_exclusive_scan_host_checks(lib):
     assert lib.mt_exclusive_scan(A, B, S, N + 2, I32, 0, None) == ALIGN
 
 
+def test_inclusive_scan_and_reduce_host_checks(lib):
+    for fn in (lib.mt_inclusive_scan, lib.mt_reduce):
+        assert fn(A, B, S, N, BF16, 0, None) == DTYPE
+        assert fn(A, B, S, N, I32, 3, None) == ARG
+        assert fn(None, B, S, N, I32, 0, None) == ARG
+        assert fn(A, B, None, N, I32, 0, None) == ARG
+        assert fn(A, B, S, None, I32, 0, None) == ARG
+        assert fn(A + 4, B, S, N, I64, 0, None) == ALIGN
+        assert fn(A, B, S, N + 2, I32, 0, None) == ALIGN
+
+
 def test_select_host_checks(lib):
     assert lib.mt_select(None, A, B, N, S, N, None) == ARG
     assert lib.mt_select(A, B, A, N, S, N, None) == ALIAS
@@ -110,6 +123,9 @@ def test_scratch_slots(lib):
     # select: 8192 flags per tile
     assert f(1 << 28, I32, 2) == 4 + 16 * (1 << 15)
     assert f(1, I32, 2) == 4 + 16 * 1
+    # reduce: a header and one partial slot per CTA, whatever the capacity
+    assert f(1 << 28, I32, 3) == f(0, F32, 3) == f(5, I64, 3) == 4 + 4096
+    assert f(10, BF16, 3) == -1
 
 
 def test_strerror_and_counter(lib):
