@@ -11,11 +11,15 @@
 // grouping, so a float sum's rounding is the same on every call.
 //
 // min/max keep the earliest of equal elements ((b < a) ? b : a). For integers
-// equal values are identical, so any grouping gives that result; for f32 the
-// two zeros compare equal but differ in sign, so f32 min/max reduce 64-bit
-// keys (the value's order in the high half, the element index in the low
-// half, ties to the lower index) and the result is the element the winning
-// key names, read back with its sign.
+// equal values are identical, so any grouping gives that result. For f32 the
+// two zeros compare equal but differ in sign, so f32 min/max also remember
+// where their extreme came from: each thread folds its elements in index
+// order with a strict comparison (a later equal element never replaces an
+// earlier one) and keeps the index of the 16-byte chunk its extreme came
+// from; threads and CTAs then combine 64-bit keys (the value's order in the
+// high half, the chunk index in the low half, ties to the lower chunk), and
+// the last CTA re-reads the winning chunk and returns its earliest element
+// equal to the extreme, with that element's own bits.
 #include <type_traits>
 
 #include "mt_tile.cuh"
@@ -62,22 +66,32 @@ __device__ __forceinline__ uint32_t f32_order(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// f32 min: the smallest key wins: (order, index). f32 max: the largest key
-// wins: (order, ~index), so equal values still prefer the lower index.
+// f32 min/max: a float and the chunk it came from per thread; 64-bit keys
+// (order, chunk) between threads. min: the smallest key wins; max: the
+// largest key wins with ~chunk in the low half, so equal values still
+// prefer the lower chunk.
+constexpr uint32_t kNoChunk = 0xffffffffu;
+
+struct ChunkState {
+    float v;     // the thread's extreme so far
+    uint32_t c;  // the chunk it came from (kNoChunk: none yet)
+};
+
 template <bool kMax>
-struct KeyFold {
+struct ChunkFold {
     using T = uint64_t;
-    __device__ __forceinline__ static T ident() { return kMax ? 0ull : ~0ull; }
-    __device__ __forceinline__ static T make(float v, int64_t i) {
-        const uint32_t idx = (uint32_t)i;
-        return ((uint64_t)f32_order(v) << 32) | (kMax ? (uint64_t)(~idx) : (uint64_t)idx);
+    using State = ChunkState;
+    __device__ __forceinline__ static float ident_v() { return kMax ? -INFINITY : INFINITY; }
+    __device__ __forceinline__ static bool better(float x, float v) { return kMax ? (x > v) : (x < v); }
+    __device__ __forceinline__ static T ident() { return key(State{ident_v(), kNoChunk}); }
+    __device__ __forceinline__ static T key(const State &st) {
+        return ((uint64_t)f32_order(st.v) << 32) | (kMax ? (uint64_t)(~st.c) : (uint64_t)st.c);
     }
+    __device__ __forceinline__ static uint32_t chunk(T k) { return kMax ? ~(uint32_t)k : (uint32_t)k; }
+    __device__ __forceinline__ static uint32_t order(T k) { return (uint32_t)(k >> 32); }
     __device__ __forceinline__ static T apply(T a, T b) { return kMax ? (b > a ? b : a) : (b < a ? b : a); }
     __device__ __forceinline__ static uint64_t bits(T v) { return v; }
     __device__ __forceinline__ static T from(uint64_t b) { return b; }
-    __device__ __forceinline__ static uint32_t index(T k) {
-        return kMax ? ~(uint32_t)k : (uint32_t)k;
-    }
 };
 
 template <class S, class Op>
@@ -86,12 +100,14 @@ struct FoldOf {
 };
 template <>
 struct FoldOf<float, OpMin> {
-    using type = KeyFold<false>;
+    using type = ChunkFold<false>;
 };
 template <>
 struct FoldOf<float, OpMax> {
-    using type = KeyFold<true>;
+    using type = ChunkFold<true>;
 };
+template <class F>
+constexpr bool kChunkFold = std::is_same<F, ChunkFold<false>>::value || std::is_same<F, ChunkFold<true>>::value;
 
 template <class F>
 __device__ __forceinline__ typename F::T block_fold(typename F::T v, typename F::T *sm) {
@@ -111,7 +127,7 @@ __device__ __forceinline__ typename F::T block_fold(typename F::T v, typename F:
 }
 
 template <class S, class Op>
-__global__ void __launch_bounds__(kRedThreads) k_reduce(RedArgs a) {
+__global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(RedArgs a) {
     pdl_prologue();
     using C = Codec<S>;
     using Acc = typename C::Acc;
@@ -130,6 +146,9 @@ __global__ void __launch_bounds__(kRedThreads) k_reduce(RedArgs a) {
     const int64_t nchunks = n > 0 ? (hi + E - 1) / E : 0;  // no element: touch nothing
 
     T acc = F::ident();
+    [[maybe_unused]] ChunkState st{0.0f, kNoChunk};
+    if constexpr (kChunkFold<F>)
+        st.v = F::ident_v();
     for (int64_t t = blockIdx.x; t * kRedTileChunks < nchunks; t += gridDim.x) {
         const int64_t c0 = t * kRedTileChunks;
         const bool full = c0 * E >= lo && (c0 + kRedTileChunks) * E <= hi;
@@ -143,15 +162,31 @@ __global__ void __launch_bounds__(kRedThreads) k_reduce(RedArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < kRedItems; ++j) {
-            const int64_t v0 = (c0 + j * kRedThreads + threadIdx.x) * E;
+            const int64_t c = c0 + j * kRedThreads + threadIdx.x;
+            const int64_t v0 = c * E;
             Acc x[E];
             C::unpack(raw[j], x);
+            if constexpr (kChunkFold<F>) {
+                // the chunk's extreme, earliest first; then the thread's
+                float m = F::ident_v();
 #pragma unroll
-            for (int k = 0; k < E; ++k)
-                if (full || (v0 + k >= lo && v0 + k < hi))
-                    acc = F::apply(acc, F::make(x[k], v0 + k - head));
+                for (int k = 0; k < E; ++k)
+                    if ((full || (v0 + k >= lo && v0 + k < hi)) && F::better(x[k], m))
+                        m = x[k];
+                if (F::better(m, st.v)) {
+                    st.v = m;
+                    st.c = (uint32_t)c;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < E; ++k)
+                    if (full || (v0 + k >= lo && v0 + k < hi))
+                        acc = F::apply(acc, F::make(x[k], v0 + k - head));
+            }
         }
     }
+    if constexpr (kChunkFold<F>)
+        acc = F::key(st);
     const T part = block_fold<F>(acc, sm);
 
     // Partial to scratch; the last CTA to arrive folds all partials in order.
@@ -172,13 +207,28 @@ __global__ void __launch_bounds__(kRedThreads) k_reduce(RedArgs a) {
         r = F::apply(r, F::from(ld_relaxed_u64(a.scratch + kHeaderSlots + i)));
     r = block_fold<F>(r, sm);
     if (threadIdx.x == 0) {
-        if constexpr (std::is_same<F, Fold<S, Op>>::value) {
+        if constexpr (!kChunkFold<F>) {
             *static_cast<S *>(a.out) = (S)r;
         } else {
-            // the element the key names, with its own sign; no element: the identity
-            const float ident = Op::template identity<float>();
-            *static_cast<float *>(a.out) =
-                n > 0 ? reinterpret_cast<const float *>(a.in)[F::index(r)] : ident;
+            // the earliest element of the winning chunk equal to the extreme,
+            // with its own bits; no such chunk: the identity (or an infinity
+            // equal to it)
+            float res = F::ident_v();
+            const uint32_t c = F::chunk(r);
+            if (c != kNoChunk) {
+                Acc x[E];
+                C::unpack(ld_stream(vin + c), x);
+                bool found = false;
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const int64_t v = (int64_t)c * E + k;
+                    if (!found && v >= lo && v < hi && f32_order(x[k]) == F::order(r)) {
+                        res = x[k];
+                        found = true;
+                    }
+                }
+            }
+            *static_cast<float *>(a.out) = res;
         }
         a.scratch[0] = 0ull;  // the ticket counter, ready for the next call
     }
