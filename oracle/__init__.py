@@ -21,9 +21,9 @@ _SRC = os.path.join(_HERE, "mt_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 F32, BF16, F16, I32, I64 = 0, 1, 2, 3, 4
-ADD, MIN, MAX = 0, 1, 2
+ADD, MIN, MAX, MUL = 0, 1, 2, 3
 DTYPES = {"f32": F32, "bf16": BF16, "f16": F16, "i32": I32, "i64": I64}
-OPS = {"add": ADD, "min": MIN, "max": MAX}
+OPS = {"add": ADD, "min": MIN, "max": MAX, "mul": MUL}
 
 
 def build(force: bool = False) -> str:
@@ -50,6 +50,8 @@ def lib():
         L.oracle_scan_rows.restype = i32
         L.oracle_exclusive_scan.argtypes = [p, p, p, p, i64, i32, i32]
         L.oracle_exclusive_scan.restype = i32
+        L.oracle_scan_rows_op.argtypes = [p, p, p, i64, i64, i32, i32, i32]
+        L.oracle_scan_rows_op.restype = i32
         L.oracle_inclusive_scan.argtypes = [p, p, p, p, i64, i32, i32]
         L.oracle_inclusive_scan.restype = i32
         L.oracle_reduce.argtypes = [p, p, p, p, i64, i32, i32]
@@ -104,6 +106,24 @@ def scan_rows(x, dtype: str, inclusive: bool, want_f64: bool = False):
     if rc != 0:
         raise ValueError("oracle_scan_rows rejected its arguments")
     return (out, p64, m64) if want_f64 else out
+
+
+def scan_rows_op(x, dtype: str, op: str, inclusive: bool, want_f64: bool = False):
+    """Row-wise scan of a [rows, n] input with op in add / mul / min / max.
+
+    Returns the output in storage form (f32 array, or u16 bit patterns for
+    bf16/f16); with ``want_f64`` also the fp64 prefix.
+    """
+    d, o = DTYPES[dtype], OPS[op]
+    a = _np(x)
+    rows, n = a.shape
+    out = np.empty((rows, n), dtype=_STORE_NP[d])
+    p64 = np.empty((rows, n), dtype=np.float64) if want_f64 else None
+    rc = lib().oracle_scan_rows_op(_ptr(a), _ptr(out), _ptr(p64) if want_f64 else None, rows, n, d,
+                                   o, int(bool(inclusive)))
+    if rc != 0:
+        raise ValueError("oracle_scan_rows_op rejected its arguments")
+    return (out, p64) if want_f64 else out
 
 
 _SCAN_NP = {F32: np.float32, I32: np.int32, I64: np.int64}

@@ -23,6 +23,10 @@
  *              fraction bits, half is IEEE binary16 (5 / 10); narrowing
  *              rounds to nearest, ties to even, keeps signed zero and
  *              subnormals, overflows to infinity, quiets NaN.
+ *              "Multi-op scan variants (prod / max / min)" -- the same scan
+ *              with op x (identity 1.0), max (identity -inf) or min
+ *              (identity +inf); the exclusive variant stores the prefix
+ *              before the current element.
  *   [algos]    Quadrants "Algorithms" user guide:
  *              "Semantics > Common conventions > Identity value" -- add 0,
  *              min the largest value (+inf, INT_MAX), max the smallest
@@ -46,7 +50,7 @@
 #include <string.h>
 
 enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_I32 = 3, OR_I64 = 4 };
-enum { OR_ADD = 0, OR_MIN = 1, OR_MAX = 2 };
+enum { OR_ADD = 0, OR_MIN = 1, OR_MAX = 2, OR_MUL = 3 };
 
 /* ------------------------------------------------------------------------
  * Small-float codecs written from the format definitions ([tile],
@@ -231,6 +235,55 @@ int oracle_scan_rows(const void *inp, void *out, double *prefix64, double *abs64
             if (abs64)
                 abs64[k] = mag;
             lp = lp_next;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Row-wise scan with any of the page's four operations ([scan.rs] module
+ * doc and "Multi-op scan variants (prod / max / min)"; recurrence from
+ * [tile]): op = OR_ADD (seed 0), OR_MUL (seed 1.0), OR_MAX (seed -inf) or
+ * OR_MIN (seed +inf). Each row is scanned on its own, left to right, in
+ * fp64 on the decoded storage values; `out` receives RN_T of the fp64 prefix
+ * (min/max prefixes are input values, so they are stored exactly). min keeps
+ * the earlier value on ties ((x < lp) ? x : lp), max likewise. When
+ * `prefix64` is non-null it receives the fp64 prefix. Returns 0, or -1 on a
+ * bad argument.
+ * ---------------------------------------------------------------------- */
+int oracle_scan_rows_op(const void *inp, void *out, double *prefix64, int64_t rows, int64_t n,
+                        int dtype, int op, int inclusive)
+{
+    if (rows < 0 || n < 0 || (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_F16) ||
+        op < OR_ADD || op > OR_MUL)
+        return -1;
+    double seed = 0.0;
+    if (op == OR_MUL)
+        seed = 1.0;
+    else if (op == OR_MIN)
+        seed = INFINITY;
+    else if (op == OR_MAX)
+        seed = -INFINITY;
+    for (int64_t r = 0; r < rows; ++r) {
+        double lp = seed;
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t k = r * n + i;
+            const double x = load_float(inp, k, dtype);
+            double next;
+            if (op == OR_ADD)
+                next = lp + x;
+            else if (op == OR_MUL)
+                next = lp * x;
+            else if (op == OR_MIN)
+                next = (x < lp) ? x : lp;
+            else
+                next = (x > lp) ? x : lp;
+            const double y = inclusive ? next : lp;
+            if (out)
+                store_float(out, k, y, dtype);
+            if (prefix64)
+                prefix64[k] = y;
+            lp = next;
         }
     }
     return 0;

@@ -487,6 +487,91 @@ def pin_reduce_signed_zero_ties():
 
 
 # ---------------------------------------------------------------------------
+# Row scans with prod / max / min
+# ---------------------------------------------------------------------------
+
+def _num(tok):
+    return float(tok) if isinstance(tok, str) else float(tok)
+
+
+def pin_rows_op_golden():
+    g = load_all()["scanrs_multi_op"]
+    x = np.array([g["x"]], dtype=np.float32)
+    for op in ("prod", "max", "min"):
+        for kind in ("inclusive", "exclusive"):
+            want = [_num(t) for t in g[f"{op}_{kind}"]]
+            opn = "mul" if op == "prod" else op
+            for dt in ("f32", "bf16", "f16"):
+                xs = torch.from_numpy(x).to(torch.bfloat16 if dt == "bf16" else torch.float16) \
+                    if dt != "f32" else torch.from_numpy(x)
+                out = oracle.scan_rows_op(xs, dt, opn, kind == "inclusive")
+                if dt == "f32":
+                    got, exp = out[0].astype(np.float64), [float(np.float32(w)) for w in want]
+                else:  # the page's exact values rounded to the storage type by table search
+                    got = library_decode(out[0], dt)
+                    exp = [w if np.isinf(w) else float(library_decode(
+                        np.array([nearest_bits(w, dt)], dtype=np.uint16), dt)[0]) for w in want]
+                assert got.tolist() == exp, (op, kind, dt)
+
+
+def pin_rows_op_brute_force():
+    """Small-integer rows: every prefix product is an exact integer below
+    2^24, so the rounded prefix is exact in every storage type up to 2048
+    (bf16: 256) and is checked against exact integer arithmetic."""
+    rng = np.random.default_rng(41)
+    for dt, lim in (("f32", 1 << 24), ("f16", 2048), ("bf16", 256)):
+        for n in (1, 2, 7, 33):
+            x = rng.choice([-2.0, -1.0, 1.0, 2.0], size=(3, n)).astype(np.float32)
+            xs = torch.from_numpy(x) if dt == "f32" else torch.from_numpy(x).to(
+                torch.bfloat16 if dt == "bf16" else torch.float16)
+            for inclusive in (True, False):
+                for op in ("mul", "min", "max"):
+                    out = oracle.scan_rows_op(xs, dt, op, inclusive)
+                    got = out.astype(np.float64) if dt == "f32" else library_decode(out, dt)
+                    for r in range(3):
+                        acc = {"mul": 1, "min": float("inf"), "max": float("-inf")}[op]
+                        for i in range(n):
+                            v = int(x[r, i])
+                            nxt = acc * v if op == "mul" else (min(acc, v) if op == "min" else max(acc, v))
+                            want = nxt if inclusive else acc
+                            if op == "mul" and abs(want) > lim:
+                                acc = nxt
+                                continue
+                            assert got[r, i] == want, (dt, op, inclusive, r, i)
+                            acc = nxt
+
+
+def pin_rows_op_library():
+    rng = np.random.default_rng(43)
+    x = (rng.choice([-1.0, 1.0], size=(4, 3000)) *
+         np.exp(rng.uniform(-0.05, 0.05, size=(4, 3000)))).astype(np.float32)
+    x64 = x.astype(np.float64)
+    for inclusive in (True, False):
+        for op, acc, seed in (("mul", np.multiply.accumulate, 1.0),
+                              ("min", np.minimum.accumulate, np.inf),
+                              ("max", np.maximum.accumulate, -np.inf),
+                              ("add", np.add.accumulate, 0.0)):
+            out, p64 = oracle.scan_rows_op(x, "f32", op, inclusive, want_f64=True)
+            want = acc(x64, axis=1)
+            if not inclusive:
+                want = np.concatenate([np.full((4, 1), seed), want[:, :-1]], axis=1)
+            assert np.array_equal(p64, want), (op, inclusive)
+            assert np.array_equal(out, want.astype(np.float32)), (op, inclusive)
+
+
+def pin_rows_op_signed_zero_ties():
+    pz, nz = 0.0, -0.0
+    for first in (pz, nz):
+        second = nz if first == pz and not np.signbit(first) else pz
+        x = np.array([[1.0, first, second, 3.0]], dtype=np.float32)
+        out = oracle.scan_rows_op(x, "f32", "min", True)
+        assert out[0, 1] == 0 and np.signbit(out[0, 2]) == np.signbit(first)
+        y = np.array([[-1.0, first, second, -3.0]], dtype=np.float32)
+        out = oracle.scan_rows_op(y, "f32", "max", True)
+        assert out[0, 3] == 0 and np.signbit(out[0, 3]) == np.signbit(first)
+
+
+# ---------------------------------------------------------------------------
 # Select
 # ---------------------------------------------------------------------------
 

@@ -54,6 +54,11 @@ MUTANTS = {
         "                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] >= r) ? x[i] : r);"),
     "reduce_wrong_min_identity": ("            r = (op == OR_MIN) ? INT64_MAX : INT64_MIN;",
                                   "            r = (op == OR_MIN) ? INT64_MAX : 0;"),
+    "rows_prod_seed_zero": ("    if (op == OR_MUL)\n        seed = 1.0;", "    if (op == OR_MUL)\n        seed = 0.0;"),
+    "rows_op_min_keeps_later": ("                next = (x < lp) ? x : lp;", "                next = (x <= lp) ? x : lp;"),
+    "rows_op_incl_excl_swapped": ("            const double y = inclusive ? next : lp;",
+                                  "            const double y = inclusive ? lp : next;"),
+    "rows_prod_is_sum": ("                next = lp * x;", "                next = lp + x;"),
 }
 
 
