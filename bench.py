@@ -73,7 +73,7 @@ DOM_BYTES = call_bytes(*CALLS[0][1:4])
 
 KERNEL_SOURCES = ["prefix_scan_row_gb300/csrc/mt_internal.h", "prefix_scan_row_gb300/csrc/mt_tile.cuh",
                   "prefix_scan_row_gb300/csrc/mt_lookback.cuh", "prefix_scan_row_gb300/csrc/mt_tilescan.cuh",
-                  "prefix_scan_row_gb300/csrc/mt_rows.cu"]
+                  "prefix_scan_row_gb300/csrc/mt_rows.cuh", "prefix_scan_row_gb300/csrc/mt_rows.cu"]
 PROFILE = "profiles/rows_bf16_8192x8192_excl.md"
 
 
@@ -371,7 +371,7 @@ def run_ours(args, world, rank, local):
                         "copy, all on one stream, CUDA events around the steps")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
-                     "kernel": "k_scan_rows<__nv_bfloat16,4> on [8192,8192] exclusive",
+                     "kernel": "k_scan_rows<__nv_bfloat16,OpAdd,4> on [8192,8192] exclusive",
                      "bytes_per_launch": DOM_BYTES, "avg_launch_ms": round(dom_ms, 5),
                      "peak_of": peak_src},
         "clocks": sampler.summary(th0, th1),
@@ -482,6 +482,19 @@ def run_suite(args):
         for inc in incs:
             timeit(f"{name} {'incl' if inc else 'excl'}", lambda: mt.mt_scan_rows(x, o, inc),
                    call_bytes(r, n, d), r * n)
+        del x, o
+    # the product / max / min row scans on the same shapes
+    for name, (r, n, d), inc in [
+            ("rows_op {} f32 [1024,4096] incl", (1024, 4096, "f32"), True),
+            ("rows_op {} bf16 [8192,8192] excl", (8192, 8192, "bf16"), False),
+            ("rows_op {} bf16 [4096,4099] incl", (4096, 4099, "bf16"), True),
+            ("rows_op {} f32 [4,2^24] incl", (4, 1 << 24, "f32"), True)]:
+        if not any(wanted(name.format(op)) for op in ("mul", "max", "min")):
+            continue
+        x = (workloads.rows_f32(r, n) if d == "f32" else workloads.rows_half(r, n, d)).to(dev)
+        o = torch.empty_like(x)
+        for op in ("mul", "max", "min"):
+            timeit(name.format(op), lambda: mt.mt_scan_rows_op(x, o, op, inc), call_bytes(r, n, d), r * n)
         del x, o
     cap, n = workloads.SCAN1D_CAPACITY // args.scale, workloads.SCAN1D_LIVE // args.scale
     tag = "n=2^28-12345" if args.scale == 1 else f"n=(2^28-12345)/{args.scale}"

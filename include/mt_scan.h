@@ -37,7 +37,8 @@ typedef enum {
     MT_I64 = 4   /* int64, two's complement */
 } mt_dtype;
 
-typedef enum { MT_ADD = 0, MT_MIN = 1, MT_MAX = 2 } mt_op;
+/* MT_MUL (product) is a row-scan operation only (mt_scan_rows_op). */
+typedef enum { MT_ADD = 0, MT_MIN = 1, MT_MAX = 2, MT_MUL = 3 } mt_op;
 
 typedef enum {
     MT_SCRATCH_SCAN = 1,   /* for mt_exclusive_scan */
@@ -96,6 +97,28 @@ typedef enum {
  */
 int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
                  int inclusive, void *stream);
+
+/*
+ * mt_scan_rows_op -- mt_scan_rows with any of the four operations of the
+ * scan.rs page ([scan.rs] "Multi-op scan variants (prod / max / min)"):
+ *   op = MT_ADD: sum (identity 0)      -- exactly mt_scan_rows;
+ *   op = MT_MUL: product (identity 1.0);
+ *   op = MT_MAX: running max (identity -inf);
+ *   op = MT_MIN: running min (identity +inf).
+ * Inclusive out[r][i] = op(inp[r][0..i]); exclusive out[r][i] =
+ * op(inp[r][0..i-1]) with out[r][0] = the identity (stored as +-inf or 1 in
+ * the storage type). Values are widened to f32 and combined in f32; sums and
+ * products are rounded once to the storage type at the store and may be
+ * grouped differently from a left-to-right loop. min keeps the earlier
+ * element on ties ((b < a) ? b : a) and max likewise, so min/max results are
+ * input values, bit for bit (a zero result carries the sign of the earliest
+ * zero). Inputs are assumed NaN-free.
+ *
+ * Arguments, memory rules, workspace and errors are those of mt_scan_rows;
+ * an op outside the four is MT_ERR_ARG.
+ */
+int mt_scan_rows_op(const void *inp, void *out, int64_t rows, int64_t n, int dtype, int op,
+                    int inclusive, void *stream);
 
 /*
  * mt_exclusive_scan -- device-wide exclusive scan of a 1-D array

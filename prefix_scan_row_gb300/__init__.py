@@ -10,6 +10,8 @@ Names and arguments follow the C ABI:
 
 * ``mt_scan_rows(inp, out, inclusive)`` -- row-wise sum scan of a contiguous
   [rows, n] f32/bf16/f16 CUDA tensor.
+* ``mt_scan_rows_op(inp, out, op, inclusive)`` -- the same with op in
+  add / mul / max / min.
 * ``mt_exclusive_scan(arr, out, scratch, n_dev, op)`` -- device-wide exclusive
   add/min/max over i32/i64/f32 with the live count in a device int32.
 * ``mt_inclusive_scan(arr, out, scratch, n_dev, op)`` -- the inclusive form
@@ -29,7 +31,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmtscan.so")
 
 MT_F32, MT_BF16, MT_F16, MT_I32, MT_I64 = 0, 1, 2, 3, 4
-MT_ADD, MT_MIN, MT_MAX = 0, 1, 2
+MT_ADD, MT_MIN, MT_MAX, MT_MUL = 0, 1, 2, 3
 MT_SCRATCH_SCAN, MT_SCRATCH_SELECT, MT_SCRATCH_REDUCE = 1, 2, 3
 MT_OK = 0
 MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_LOOKBACK_TIMEOUT, MT_ERR_ALIGN = (
@@ -40,9 +42,9 @@ MT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_F16,
               torch.int32: MT_I32, torch.int64: MT_I64}
-OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX}
+OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX, "mul": MT_MUL}
 
-EXPORTS = ("mt_scan_rows", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",
+EXPORTS = ("mt_scan_rows", "mt_scan_rows_op", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",
            "mt_scan_scratch_slots",
            "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback",
            "mt_scan_rows_noalloc")
@@ -63,6 +65,8 @@ def _load():
     p, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
     L.mt_scan_rows.argtypes = [p, p, i64, i64, i32, i32, p]
     L.mt_scan_rows.restype = i32
+    L.mt_scan_rows_op.argtypes = [p, p, i64, i64, i32, i32, i32, p]
+    L.mt_scan_rows_op.restype = i32
     L.mt_exclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_exclusive_scan.restype = i32
     L.mt_inclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
@@ -123,6 +127,22 @@ def mt_scan_rows(inp: torch.Tensor, out: torch.Tensor, inclusive: bool, stream=N
     code = DTYPE_CODE.get(inp.dtype, -99)
     _check(lib.mt_scan_rows(_ptr(inp), _ptr(out), rows, n, code, int(bool(inclusive)),
                             _stream(stream)), "mt_scan_rows")
+
+
+def mt_scan_rows_op(inp: torch.Tensor, out: torch.Tensor, op: str, inclusive: bool,
+                    stream=None) -> None:
+    """Row-wise scan with op in 'add' | 'mul' | 'max' | 'min'."""
+    if inp.dim() == 1:
+        rows, n = 1, inp.shape[0]
+    else:
+        rows, n = inp.shape
+    if out.shape != inp.shape or out.dtype != inp.dtype:
+        raise ValueError("out must match inp in shape and dtype")
+    if not (inp.is_contiguous() and out.is_contiguous()):
+        raise ValueError("inp and out must be contiguous")
+    code = DTYPE_CODE.get(inp.dtype, -99)
+    _check(lib.mt_scan_rows_op(_ptr(inp), _ptr(out), rows, n, code, OP_CODE[op],
+                               int(bool(inclusive)), _stream(stream)), "mt_scan_rows_op")
 
 
 def mt_exclusive_scan(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor,

@@ -163,9 +163,10 @@ static bool all_device(std::initializer_list<const void *> ps, int dev) {
 
 using namespace mt;
 
-extern "C" int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
-                            int inclusive, void *stream) {
-    if (rows < 0 || n < 0)
+// mt_scan_rows and mt_scan_rows_op share their checks, workspace and kernels.
+static int rows_call(const void *inp, void *out, int64_t rows, int64_t n, int dtype, int op,
+                     int inclusive, void *stream) {
+    if (rows < 0 || n < 0 || op < MT_ADD || op > MT_MUL)
         return MT_ERR_ARG;
     if (dtype != MT_F32 && dtype != MT_BF16 && dtype != MT_F16)
         return MT_ERR_DTYPE;
@@ -205,10 +206,20 @@ extern "C" int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n,
             return MT_ERR_CUDA;
         }
     }
-    cudaError_t e = rows_launch(inp, out, rows, n, dtype, p, inclusive != 0, aligned_io, ws, L);
+    cudaError_t e = rows_launch(inp, out, rows, n, dtype, op, p, inclusive != 0, aligned_io, ws, L);
     if (ws != nullptr && cudaFreeAsync(ws, L.stream) != cudaSuccess)
         e = cudaErrorUnknown;
     return e == cudaSuccess ? MT_OK : MT_ERR_CUDA;
+}
+
+extern "C" int mt_scan_rows(const void *inp, void *out, int64_t rows, int64_t n, int dtype,
+                            int inclusive, void *stream) {
+    return rows_call(inp, out, rows, n, dtype, MT_ADD, inclusive, stream);
+}
+
+extern "C" int mt_scan_rows_op(const void *inp, void *out, int64_t rows, int64_t n, int dtype, int op,
+                               int inclusive, void *stream) {
+    return rows_call(inp, out, rows, n, dtype, op, inclusive, stream);
 }
 
 // The exclusive and inclusive 1-D scans share their checks and kernel.
@@ -326,7 +337,8 @@ extern "C" int mt_scan_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MT_ERR_CUDA;
     int worst = MT_OK;
-    cudaError_t (*takers[3])(int *) = {rows_take_error, scan1d_take_error, select_take_error};
+    cudaError_t (*takers[5])(int *) = {rows_take_error, rows_minmax_take_error, rows_mul_take_error,
+                                       scan1d_take_error, select_take_error};
     for (auto take : takers) {
         int code = 0;
         if (take(&code) != cudaSuccess)

@@ -63,10 +63,20 @@ struct RowPlan {
     int warps;               // single-tile rows: warps per CTA
 };
 RowPlan rows_plan(int dtype, int64_t n, bool heads_zero);
-cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int dtype,
+// op: 0 add, 1 min, 2 max, 3 mul (mt_op)
+cudaError_t rows_launch(const void *in, void *out, int64_t rows, int64_t n, int dtype, int op,
                         const RowPlan &p, bool inclusive, bool aligned_io, uint64_t *ws,
                         const Launch &L);
+#define MT_ROWS_LAUNCH_DECL(name)                                                                   \
+    cudaError_t name(const void *in, void *out, int64_t rows, int64_t n, int dtype, const RowPlan &p, \
+                     bool inclusive, bool aligned_io, uint64_t *ws, const Launch &L);
+MT_ROWS_LAUNCH_DECL(rows_launch_min)  // mt_rows_minmax.cu
+MT_ROWS_LAUNCH_DECL(rows_launch_max)  // mt_rows_minmax.cu
+MT_ROWS_LAUNCH_DECL(rows_launch_mul)  // mt_rows_mul.cu
+#undef MT_ROWS_LAUNCH_DECL
 cudaError_t rows_take_error(int *code);
+cudaError_t rows_minmax_take_error(int *code);
+cudaError_t rows_mul_take_error(int *code);
 int rows_rec_slots();  // 8-byte slots per look-back record of a long row
 
 // ---- device-wide exclusive scan (mt_scan1d.cu) ----------------------------

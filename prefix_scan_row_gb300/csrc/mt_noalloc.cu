@@ -111,6 +111,6 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
     } else {
         ws = nullptr;  // rows fit in one tile: no look-back, no workspace
     }
-    cudaError_t e = rows_launch(inp, out, rows, n, dtype, p, inclusive != 0, aligned_io, ws, L);
+    cudaError_t e = rows_launch(inp, out, rows, n, dtype, MT_ADD, p, inclusive != 0, aligned_io, ws, L);
     return e == cudaSuccess ? MT_OK : MT_ERR_CUDA;
 }

@@ -199,8 +199,9 @@ struct Staged {
     // the same result for adds of integers, for integer min/max, and for float
     // min/max unless the result is a zero (which of +0/-0 comes first then
     // matters): those take the quick unordered reduction, and a float min/max
-    // whose quick result is zero is redone in element order. Float adds take
-    // the quick one too (only rounding differs, within the stated tolerance).
+    // whose quick result is zero is redone in element order. Float adds and
+    // products take the quick one too (only rounding differs, within the
+    // stated tolerances).
     template <bool FULL>
     __device__ __forceinline__ static Acc reduce(Smem &sm, int llo, int lhi) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -227,7 +228,8 @@ struct Staged {
 #pragma unroll
         for (int w = 0; w < kNW; ++w)
             agg = Op::apply(agg, sm.red[0][w]);
-        constexpr bool kOrderFree = std::is_same<Op, OpAdd>::value || !std::is_same<Acc, float>::value;
+        constexpr bool kOrderFree = std::is_same<Op, OpAdd>::value || std::is_same<Op, OpMul>::value ||
+                                    !std::is_same<Acc, float>::value;
         if constexpr (!kOrderFree) {
             if (agg == Acc(0)) {  // block-uniform: every thread folded the same totals
                 __syncthreads();  // all reads of sm.red are done

@@ -82,6 +82,11 @@ struct OpMax {
     template <class T> __device__ __forceinline__ static T identity() { return Lim<T>::lo(); }
     template <class T> __device__ __forceinline__ static T apply(T a, T b) { return (b > a) ? b : a; }
 };
+// Product (the row scans' prod variant; f32 accumulation only).
+struct OpMul {
+    template <class T> __device__ __forceinline__ static T identity() { return T(1); }
+    __device__ __forceinline__ static float apply(float a, float b) { return a * b; }
+};
 
 // ---------------------------------------------------------------------------
 // Storage codecs: a 16-byte chunk <-> E accumulator values.

@@ -8,7 +8,12 @@ Tolerances (written here, used by every parity test):
     + 1e-6, with RN_T the oracle's round-to-nearest-even to the output type
     and ulp_T the spacing of T at that value (subnormal spacing near 0);
   * inputs whose every partial sum is exact in f32 (dyadic k/256 values):
-    bit-exact for all three storage types.
+    bit-exact for all three storage types;
+  * row products: every grouping of the k <= i+1 factors of out[i] has at
+    most k f32 roundings of relative size <= 2^-24 (no underflow on the
+    inputs used), so |gpu - p64| <= ((1 + 2^-24)^(i+1) - 1) |p64|, plus
+    ulp_T(RN_T(p64)) for bf16/f16 storage;
+  * row min/max: bit-exact (the results are input values).
 """
 from __future__ import annotations
 
@@ -70,6 +75,38 @@ def assert_scan_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dt
     w = {"i32": np.uint32, "f32": np.uint32, "i64": np.uint64}[dtype]
     bad = np.nonzero(got.view(w) != ref.view(w))[0]
     assert bad.size == 0, f"{bad.size} mismatches; first at {bad[0]}: {got[bad[0]]} vs {ref[bad[0]]}"
+
+
+def assert_rows_op_close(gpu_out: torch.Tensor, x_cpu: torch.Tensor, dtype: str, op: str,
+                         inclusive: bool):
+    """Row scan with op in add / mul / min / max against the oracle."""
+    if op == "add":
+        assert_rows_close(gpu_out, x_cpu, dtype, inclusive)
+        return
+    ref, p64 = oracle.scan_rows_op(x_cpu, dtype, op, inclusive, want_f64=True)
+    if op in ("min", "max"):
+        got = (gpu_out.detach().to("cpu").numpy().view(np.uint32) if dtype == "f32"
+               else bits16(gpu_out))
+        want = ref.view(np.uint32) if dtype == "f32" else ref
+        bad = np.nonzero(got != want)
+        assert bad[0].size == 0, _report(bad, got, want)
+        return
+    k = np.arange(1, p64.shape[1] + 1, dtype=np.float64)[None, :]
+    rel = np.expm1(k * np.log1p(2.0 ** -24))
+    bound = rel * np.abs(p64)
+    if dtype == "f32":
+        got = gpu_out.detach().to("cpu").numpy().astype(np.float64)
+        err = np.abs(got - p64)
+    else:
+        got = oracle.decode_half(bits16(gpu_out), dtype)
+        want = oracle.decode_half(ref, dtype)
+        err = np.abs(got - p64)
+        bound = bound + oracle.ulp_array(want, dtype)
+    bad = np.nonzero(~(err <= bound))
+    if bad[0].size:
+        i = tuple(b[0] for b in bad)
+        raise AssertionError(f"{bad[0].size} elements out of tolerance; first at {i}: "
+                             f"got {got[i]} p64 {p64[i]} err {err[i]} bound {bound[i]}")
 
 
 def assert_reduce_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dtype: str, op: str):

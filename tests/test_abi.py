@@ -22,6 +22,7 @@ def lib():
     L = ctypes.CDLL(path)
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.mt_scan_rows.argtypes = [p, p, i64, i64, i32, i32, p]
+    L.mt_scan_rows_op.argtypes = [p, p, i64, i64, i32, i32, i32, p]
     L.mt_exclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_inclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_reduce.argtypes = [p, p, p, p, i32, i32, p]
@@ -73,6 +74,18 @@ def test_rows_host_checks(lib):
     assert lib.mt_scan_rows(A + 2, B, 2, 2, F32, 1, None) == ALIGN
     assert lib.mt_scan_rows(A + 1, B, 2, 2, F16, 1, None) == ALIGN
     assert lib.mt_scan_rows(A, B, 1 << 40, 1 << 40, F32, 1, None) == ARG  # size overflow
+
+
+def test_rows_op_host_checks(lib):
+    f = lib.mt_scan_rows_op
+    assert f(A, B, 2, 8, F32, 4, 1, None) == ARG
+    assert f(A, B, 2, 8, F32, -1, 1, None) == ARG
+    assert f(A, B, -1, 8, F32, 3, 1, None) == ARG
+    assert f(A, B, 2, 8, I32, 3, 1, None) == DTYPE
+    assert f(A, B, 0, 8, F32, 3, 1, None) == 0  # empty
+    assert f(A + 2, B, 2, 8, F32, 3, 1, None) == ALIGN
+    # the 1-D calls take add / min / max only
+    assert lib.mt_exclusive_scan(A, B, S, N, F32, 3, None) == ARG
 
 
 def test_exclusive_scan_host_checks(lib):

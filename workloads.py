@@ -81,6 +81,18 @@ def bernoulli_u8(n: int, p: float, seed: int) -> torch.Tensor:
     return (u < p).to(torch.uint8)
 
 
+def near_one(shape, seed: int, dtype: str = "f32", spread: float = 0.05) -> torch.Tensor:
+    """Factors for product scans: a random sign times exp(u), u iid
+    uniform[-spread, spread), drawn in f32 and cast to storage. The log of a
+    prefix product is then a random walk with steps below `spread`, so
+    products over tens of thousands of elements stay far from overflow and
+    underflow in f32, bf16 and f16."""
+    g = generator(seed)
+    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int32).to(torch.float32).mul_(2.0).sub_(1.0)
+    u = torch.rand(shape, generator=g, dtype=torch.float32).mul_(2.0 * spread).sub_(spread)
+    return (sign * torch.exp(u)).to(_STORAGE[dtype])
+
+
 def dyadic(shape, seed: int, dtype: str = "f32") -> torch.Tensor:
     """Values k/256 with integer |k| <= 255: exact in f32, bf16 and f16."""
     k = torch.randint(-255, 256, shape, generator=generator(seed), dtype=torch.int32)
