@@ -20,9 +20,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mt_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-F32, BF16, F16, I32, I64 = 0, 1, 2, 3, 4
+F32, BF16, F16, I32, I64, U32, U64, F64 = 0, 1, 2, 3, 4, 5, 6, 7
 ADD, MIN, MAX, MUL = 0, 1, 2, 3
-DTYPES = {"f32": F32, "bf16": BF16, "f16": F16, "i32": I32, "i64": I64}
+DTYPES = {"f32": F32, "bf16": BF16, "f16": F16, "i32": I32, "i64": I64, "u32": U32, "u64": U64,
+          "f64": F64}
 OPS = {"add": ADD, "min": MIN, "max": MAX, "mul": MUL}
 
 
@@ -126,7 +127,8 @@ def scan_rows_op(x, dtype: str, op: str, inclusive: bool, want_f64: bool = False
     return (out, p64) if want_f64 else out
 
 
-_SCAN_NP = {F32: np.float32, I32: np.int32, I64: np.int64}
+_SCAN_NP = {F32: np.float32, I32: np.int32, I64: np.int64, U32: np.uint32, U64: np.uint64,
+            F64: np.float64}
 
 
 def exclusive_scan(arr, n: int, dtype: str, op: str, want_f64: bool = False):
@@ -136,7 +138,7 @@ def exclusive_scan(arr, n: int, dtype: str, op: str, want_f64: bool = False):
     a = _np(arr)[:n]
     a = np.ascontiguousarray(a)
     out = np.empty((n,), dtype=_SCAN_NP[d])
-    f64 = want_f64 and d == F32 and o == ADD
+    f64 = want_f64 and d in (F32, F64) and o == ADD
     p64 = np.empty((n,), dtype=np.float64) if f64 else None
     m64 = np.empty((n,), dtype=np.float64) if f64 else None
     rc = lib().oracle_exclusive_scan(_ptr(a), _ptr(out), _ptr(p64) if f64 else None,
@@ -152,7 +154,7 @@ def inclusive_scan(arr, n: int, dtype: str, op: str, want_f64: bool = False):
     d, o = DTYPES[dtype], OPS[op]
     a = np.ascontiguousarray(_np(arr)[:n])
     out = np.empty((n,), dtype=_SCAN_NP[d])
-    f64 = want_f64 and d == F32 and o == ADD
+    f64 = want_f64 and d in (F32, F64) and o == ADD
     p64 = np.empty((n,), dtype=np.float64) if f64 else None
     m64 = np.empty((n,), dtype=np.float64) if f64 else None
     rc = lib().oracle_inclusive_scan(_ptr(a), _ptr(out), _ptr(p64) if f64 else None,
@@ -175,7 +177,7 @@ def reduce(arr, n: int, dtype: str, op: str, want_f64: bool = False):
     rc = lib().oracle_reduce(_ptr(a), _ptr(out), _ptr(s64), _ptr(m64), n, d, o)
     if rc != 0:
         raise ValueError("oracle_reduce rejected its arguments")
-    f64 = want_f64 and d == F32 and o == ADD
+    f64 = want_f64 and d in (F32, F64) and o == ADD
     return (out[0], float(s64[0]), float(m64[0])) if f64 else out[0]
 
 

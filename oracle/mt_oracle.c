@@ -38,7 +38,10 @@
  *              of out is left untouched.
  *
  * Readings where the pages are silent:
- *   - integer add wraps modulo 2^width (two's complement);
+ *   - integer add wraps modulo 2^width (two's complement; unsigned types
+ *     likewise); min/max of u32/u64 compare as unsigned, with identities
+ *     UINT_MAX (min) and 0 (max);
+ *   - f64 add accumulates in long double (at least 64 significand bits);
  *   - min keeps the earlier value on ties: new = (x < acc) ? x : acc, max
  *     likewise with '>'; inputs are NaN-free;
  *   - float add accumulates in fp64 from the decoded storage values.
@@ -49,7 +52,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_I32 = 3, OR_I64 = 4 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_I32 = 3, OR_I64 = 4, OR_U32 = 5, OR_U64 = 6, OR_F64 = 7 };
 enum { OR_ADD = 0, OR_MIN = 1, OR_MAX = 2, OR_MUL = 3 };
 
 /* ------------------------------------------------------------------------
@@ -290,6 +293,92 @@ int oracle_scan_rows_op(const void *inp, void *out, double *prefix64, int64_t ro
 }
 
 /* ------------------------------------------------------------------------
+ * The 1-D scans for the unsigned and f64 dtypes of [algos] ("the new
+ * functional API covers {i32, u32, f32, i64, u64, f64}"): the recurrence
+ * lp[0] = identity, lp[i+1] = op(lp[i], x[i]); the exclusive form stores
+ * lp[i], the inclusive one lp[i+1]. For f64 add, `prefix64` / `abs64` (when
+ * non-null) receive the long double prefix rounded to double and the running
+ * sum of |x_j| for j <= i.
+ * ---------------------------------------------------------------------- */
+static void scan_u32(const uint32_t *x, uint32_t *y, int64_t n, int op, int inclusive)
+{
+    uint32_t lp = (op == OR_MIN) ? UINT32_MAX : 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t next;
+        if (op == OR_ADD)
+            next = lp + x[i]; /* wraps modulo 2^32 */
+        else if (op == OR_MIN)
+            next = (x[i] < lp) ? x[i] : lp;
+        else
+            next = (x[i] > lp) ? x[i] : lp;
+        y[i] = inclusive ? next : lp;
+        lp = next;
+    }
+}
+
+static void scan_u64(const uint64_t *x, uint64_t *y, int64_t n, int op, int inclusive)
+{
+    uint64_t lp = (op == OR_MIN) ? UINT64_MAX : 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        uint64_t next;
+        if (op == OR_ADD)
+            next = lp + x[i]; /* wraps modulo 2^64 */
+        else if (op == OR_MIN)
+            next = (x[i] < lp) ? x[i] : lp;
+        else
+            next = (x[i] > lp) ? x[i] : lp;
+        y[i] = inclusive ? next : lp;
+        lp = next;
+    }
+}
+
+static void scan_f64(const double *x, double *y, double *prefix64, double *abs64, int64_t n, int op,
+                     int inclusive)
+{
+    if (op == OR_ADD) {
+        long double lp = 0.0L, mag = 0.0L;
+        for (int64_t i = 0; i < n; ++i) {
+            const long double next = lp + (long double)x[i];
+            mag += fabsl((long double)x[i]);
+            const long double v = inclusive ? next : lp;
+            if (y)
+                y[i] = (double)v;
+            if (prefix64)
+                prefix64[i] = (double)v;
+            if (abs64)
+                abs64[i] = (double)mag;
+            lp = next;
+        }
+        return;
+    }
+    double lp = (op == OR_MIN) ? INFINITY : -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        double next;
+        if (op == OR_MIN)
+            next = (x[i] < lp) ? x[i] : lp;
+        else
+            next = (x[i] > lp) ? x[i] : lp;
+        y[i] = inclusive ? next : lp;
+        lp = next;
+    }
+}
+
+/* The same dtypes for the scans below; 1 when `dtype` is one of them. */
+static int scan_ext(const void *arr, void *out, double *prefix64, double *abs64, int64_t n, int dtype,
+                    int op, int inclusive)
+{
+    if (dtype == OR_U32)
+        scan_u32((const uint32_t *)arr, (uint32_t *)out, n, op, inclusive);
+    else if (dtype == OR_U64)
+        scan_u64((const uint64_t *)arr, (uint64_t *)out, n, op, inclusive);
+    else if (dtype == OR_F64)
+        scan_f64((const double *)arr, (double *)out, prefix64, abs64, n, op, inclusive);
+    else
+        return 0;
+    return 1;
+}
+
+/* ------------------------------------------------------------------------
  * Device-wide exclusive scan ([algos] exclusive_scan_{add,min,max}):
  * out[i] = op(arr[0:i]), out[0] = identity of (op, dtype). Only out[0:n] is
  * written. For f32 add, `out` gets the fp64 prefix rounded to f32 and, when
@@ -301,6 +390,8 @@ int oracle_exclusive_scan(const void *arr, void *out, double *prefix64, double *
 {
     if (n < 0 || op < OR_ADD || op > OR_MAX)
         return -1;
+    if (scan_ext(arr, out, prefix64, abs64, n, dtype, op, 0))
+        return 0;
     if (dtype == OR_I32) {
         const int32_t *x = (const int32_t *)arr;
         int32_t *y = (int32_t *)out;
@@ -391,6 +482,8 @@ int oracle_inclusive_scan(const void *arr, void *out, double *prefix64, double *
 {
     if (n < 0 || op < OR_ADD || op > OR_MAX)
         return -1;
+    if (scan_ext(arr, out, prefix64, abs64, n, dtype, op, 1))
+        return 0;
     if (dtype == OR_I32) {
         const int32_t *x = (const int32_t *)arr;
         int32_t *y = (int32_t *)out;
@@ -479,6 +572,44 @@ int oracle_reduce(const void *arr, void *out, double *sum64, double *abs64, int6
 {
     if (n < 0 || op < OR_ADD || op > OR_MAX)
         return -1;
+    if (dtype == OR_U32) {
+        const uint32_t *x = (const uint32_t *)arr;
+        uint32_t r = (op == OR_MIN) ? UINT32_MAX : 0u;
+        for (int64_t i = 0; i < n; ++i)
+            r = (op == OR_ADD) ? r + x[i] : (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);
+        memcpy(out, &r, 4);
+        return 0;
+    }
+    if (dtype == OR_U64) {
+        const uint64_t *x = (const uint64_t *)arr;
+        uint64_t r = (op == OR_MIN) ? UINT64_MAX : 0u;
+        for (int64_t i = 0; i < n; ++i)
+            r = (op == OR_ADD) ? r + x[i] : (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);
+        memcpy(out, &r, 8);
+        return 0;
+    }
+    if (dtype == OR_F64) {
+        const double *x = (const double *)arr;
+        double r;
+        if (op == OR_ADD) {
+            long double acc = 0.0L, mag = 0.0L;
+            for (int64_t i = 0; i < n; ++i) {
+                acc += (long double)x[i];
+                mag += fabsl((long double)x[i]);
+            }
+            r = (double)acc;
+            if (sum64)
+                *sum64 = (double)acc;
+            if (abs64)
+                *abs64 = (double)mag;
+        } else {
+            r = (op == OR_MIN) ? INFINITY : -INFINITY;
+            for (int64_t i = 0; i < n; ++i)
+                r = (op == OR_MIN) ? ((x[i] < r) ? x[i] : r) : ((x[i] > r) ? x[i] : r);
+        }
+        memcpy(out, &r, 8);
+        return 0;
+    }
     if (dtype == OR_I32) {
         const int32_t *x = (const int32_t *)arr;
         int32_t r;

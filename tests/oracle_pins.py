@@ -487,6 +487,102 @@ def pin_reduce_signed_zero_ties():
 
 
 # ---------------------------------------------------------------------------
+# The unsigned and f64 dtypes of the 1-D calls
+# ---------------------------------------------------------------------------
+U32_MAX, U64_MAX = 2**32 - 1, 2**64 - 1
+_NPX = {"u32": np.uint32, "u64": np.uint64, "f64": np.float64}
+_IDX = {("u32", "add"): 0, ("u32", "min"): U32_MAX, ("u32", "max"): 0,
+        ("u64", "add"): 0, ("u64", "min"): U64_MAX, ("u64", "max"): 0,
+        ("f64", "add"): 0.0, ("f64", "min"): np.inf, ("f64", "max"): -np.inf}
+
+
+def pin_ext_golden():
+    g = load_all()
+    ex = g["algos_exclusive_scan_add_i32"]
+    inc = g["algos_inclusive_scan_add_i32"]
+    mm = g["algos_exclusive_scan_minmax_i32"]
+    red = g["algos_reduce_i32"]
+    for dt in ("u32", "u64", "f64"):
+        arr = np.array(ex["arr"], dtype=_NPX[dt])
+        assert oracle.exclusive_scan(arr, len(arr), dt, "add").tolist() == ex["exclusive"], dt
+        assert oracle.inclusive_scan(arr, len(arr), dt, "add").tolist() == inc["inclusive"], dt
+        for op in ("min", "max"):
+            got = oracle.exclusive_scan(np.array(mm["arr"], dtype=_NPX[dt]), len(mm["arr"]), dt, op)
+            want = [(_IDX[(dt, op)] if i == 0 else v) for i, v in enumerate(mm[op])]
+            assert got.tolist() == want, (dt, op)
+        for op in ("add", "min", "max"):
+            assert oracle.reduce(arr, len(arr), dt, op) == red[op], (dt, op)
+            assert oracle.reduce(arr, 0, dt, op) == _IDX[(dt, op)], (dt, op)
+
+
+def pin_ext_unsigned_order_and_wrap():
+    a = np.array([1, 2**31 + 5, 3, U32_MAX], dtype=np.uint32)
+    assert oracle.inclusive_scan(a, 4, "u32", "max").tolist() == [1, 2**31 + 5, 2**31 + 5, U32_MAX]
+    assert oracle.inclusive_scan(a, 4, "u32", "min").tolist() == [1, 1, 1, 1]
+    assert oracle.exclusive_scan(a, 4, "u32", "add").tolist() == [0, 1, 2**31 + 6, 2**31 + 9]
+    assert oracle.reduce(a, 4, "u32", "add") == (1 + 2**31 + 5 + 3 + U32_MAX) % 2**32
+    b = np.array([2**63 + 7, 1, U64_MAX], dtype=np.uint64)
+    assert oracle.inclusive_scan(b, 3, "u64", "max").tolist() == [2**63 + 7, 2**63 + 7, U64_MAX]
+    assert oracle.inclusive_scan(b, 3, "u64", "min").tolist() == [2**63 + 7, 1, 1]
+    assert oracle.inclusive_scan(b, 3, "u64", "add").tolist() == [2**63 + 7, 2**63 + 8, 2**63 + 7]
+    assert oracle.reduce(b, 3, "u64", "min") == 1
+
+
+def pin_ext_library():
+    rng = np.random.default_rng(47)
+    n = 20000
+    for dt in ("u32", "u64", "f64"):
+        if dt == "u32":
+            x = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
+        elif dt == "u64":
+            x = rng.integers(0, 2**63, n, dtype=np.uint64) * np.uint64(2) + np.uint64(1)
+        else:
+            x = rng.uniform(-1, 1, n)
+        assert np.array_equal(oracle.inclusive_scan(x, n, dt, "min"), np.minimum.accumulate(x))
+        assert np.array_equal(oracle.inclusive_scan(x, n, dt, "max"), np.maximum.accumulate(x))
+        assert oracle.reduce(x, n, dt, "min") == x.min() and oracle.reduce(x, n, dt, "max") == x.max()
+        if dt != "f64":
+            with np.errstate(over="ignore"):
+                want = np.cumsum(x, dtype=x.dtype)  # numpy wraps unsigned sums
+            assert np.array_equal(oracle.inclusive_scan(x, n, dt, "add"), want)
+            assert oracle.reduce(x, n, dt, "add") == want[-1]
+
+
+def pin_ext_f64_signed_zero_ties():
+    for first in (0.0, -0.0):
+        second = -0.0 if not np.signbit(first) else 0.0
+        x = np.array([1.0, first, 2.0, second])
+        r = oracle.reduce(x, 4, "f64", "min")
+        assert r == 0 and np.signbit(r) == np.signbit(first)
+        y = np.array([-1.0, first, -2.0, second])
+        r = oracle.reduce(y, 4, "f64", "max")
+        assert r == 0 and np.signbit(r) == np.signbit(first)
+        inc = oracle.inclusive_scan(y, 4, "f64", "max")
+        assert np.signbit(inc[3]) == np.signbit(first)
+
+
+def pin_ext_f64_sums():
+    """Dyadic f64 inputs: every prefix is exact, so the oracle's prefix is
+    the exact one; random inputs: each prefix within one ulp of the
+    correctly rounded prefix (math.fsum)."""
+    import math
+    rng = np.random.default_rng(53)
+    x = rng.integers(-2**20, 2**20, 5000) / 1024.0
+    out, p, mag = oracle.inclusive_scan(x, 5000, "f64", "add", want_f64=True)
+    assert np.array_equal(p, np.cumsum(x)) and np.array_equal(out, p)
+    assert np.array_equal(mag, np.cumsum(np.abs(x)))
+    ex = oracle.exclusive_scan(x, 5000, "f64", "add")
+    assert ex[0] == 0.0 and np.array_equal(ex[1:], p[:-1])
+    y = rng.uniform(-1, 1, 2000) * 10.0 ** rng.integers(-8, 9, 2000)
+    got = oracle.inclusive_scan(y, 2000, "f64", "add")
+    for i in range(0, 2000, 97):
+        want = math.fsum(y[: i + 1])
+        assert abs(got[i] - want) <= np.spacing(abs(want)) + 1e-300, i
+    r, s64, m64 = oracle.reduce(y, 2000, "f64", "add", want_f64=True)
+    assert abs(r - math.fsum(y)) <= np.spacing(abs(math.fsum(y)))
+
+
+# ---------------------------------------------------------------------------
 # Row scans with prod / max / min
 # ---------------------------------------------------------------------------
 

@@ -59,6 +59,11 @@ MUTANTS = {
     "rows_op_incl_excl_swapped": ("            const double y = inclusive ? next : lp;",
                                   "            const double y = inclusive ? lp : next;"),
     "rows_prod_is_sum": ("                next = lp * x;", "                next = lp + x;"),
+    "u32_signed_compare": ("            next = (x[i] < lp) ? x[i] : lp;\n        else\n            next = (x[i] > lp) ? x[i] : lp;\n        y[i] = inclusive ? next : lp;\n        lp = next;\n    }\n}\n\nstatic void scan_u64",
+                           "            next = ((int32_t)x[i] < (int32_t)lp) ? x[i] : lp;\n        else\n            next = ((int32_t)x[i] > (int32_t)lp) ? x[i] : lp;\n        y[i] = inclusive ? next : lp;\n        lp = next;\n    }\n}\n\nstatic void scan_u64"),
+    "u64_wrong_min_identity": ("    uint64_t lp = (op == OR_MIN) ? UINT64_MAX : 0u;", "    uint64_t lp = (op == OR_MIN) ? INT64_MAX : 0u;"),
+    "f64_add_wrong_sign": ("            const long double next = lp + (long double)x[i];",
+                           "            const long double next = lp - (long double)x[i];"),
 }
 
 
