@@ -499,12 +499,13 @@ def run_suite(args):
     cap, n = workloads.SCAN1D_CAPACITY // args.scale, workloads.SCAN1D_LIVE // args.scale
     tag = "n=2^28-12345" if args.scale == 1 else f"n=(2^28-12345)/{args.scale}"
     n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
-    for d, tdt, s in (("i32", torch.int32, 4), ("f32", torch.float32, 4), ("i64", torch.int64, 8)):
+    for d, tdt, s in (("i32", torch.int32, 4), ("f32", torch.float32, 4), ("i64", torch.int64, 8),
+                      ("u32", torch.uint32, 4), ("u64", torch.uint64, 8), ("f64", torch.float64, 8)):
         if not any(wanted(f"{k} {d} {op} {tag}") for op in ("add", "min", "max")
                    for k in ("exclusive_scan", "inclusive_scan", "reduce")):
             continue
-        a = workloads.scan1d(d, capacity=cap).to(dev)
-        o = torch.empty_like(a)
+        a = workloads.scan1d(d, capacity=cap).to(dev).view(tdt)  # unsigned: a view of the signed twin
+        o = torch.empty(a.shape, dtype=torch.int64 if s == 8 else torch.int32, device=dev).view(tdt)
         scr = mt.alloc_scratch(cap, tdt, mt.MT_SCRATCH_SCAN, device=dev)
         for op in ("add", "min", "max"):
             timeit(f"exclusive_scan {d} {op} {tag}",
@@ -513,7 +514,7 @@ def run_suite(args):
             timeit(f"inclusive_scan {d} {op} {tag}",
                    lambda: mt.mt_inclusive_scan(a, o, scr, n_dev, op), 2 * s * n, n)
         rscr = mt.alloc_scratch(cap, tdt, mt.MT_SCRATCH_REDUCE, device=dev)
-        r1 = torch.empty(1, dtype=tdt, device=dev)
+        r1 = torch.empty(1, dtype=torch.int64 if s == 8 else torch.int32, device=dev).view(tdt)
         for op in ("add", "min", "max"):
             timeit(f"reduce {d} {op} {tag}",
                    lambda: mt.mt_reduce(a, r1, rscr, n_dev, op), s * n, n)

@@ -34,7 +34,10 @@ typedef enum {
     MT_BF16 = 1, /* bfloat16: 8 exponent / 7 fraction bits */
     MT_F16 = 2,  /* IEEE binary16 */
     MT_I32 = 3,  /* int32, two's complement */
-    MT_I64 = 4   /* int64, two's complement */
+    MT_I64 = 4,  /* int64, two's complement */
+    MT_U32 = 5,  /* uint32 (1-D scans and reduce) */
+    MT_U64 = 6,  /* uint64 (1-D scans and reduce) */
+    MT_F64 = 7   /* float64 (1-D scans and reduce) */
 } mt_dtype;
 
 /* MT_MUL (product) is a row-scan operation only (mt_scan_rows_op). */
@@ -131,9 +134,14 @@ int mt_scan_rows_op(const void *inp, void *out, int64_t rows, int64_t n, int dty
  * grouping; f32 add is summed in f32 and may be grouped differently from a
  * left-to-right loop. Inputs are assumed NaN-free (NaN order is unspecified).
  *
- * arr, out : device arrays of `dtype` (MT_I32, MT_I64 or MT_F32), aligned to
- *            the element size. out must not be arr ([algos]: "No in-place
- *            scan") -> MT_ERR_ALIAS; other overlaps are undefined.
+ * arr, out : device arrays of `dtype`, aligned to the element size: MT_I32,
+ *            MT_I64 or MT_F32, and the rest of [algos]'s list ("the new
+ *            functional API covers {i32, u32, f32, i64, u64, f64}"): MT_U32
+ *            and MT_U64 (add wraps; min/max compare as unsigned, identities
+ *            UINT_MAX and 0) and MT_F64 (as f32: identities +-inf, earliest
+ *            element on ties, sums grouped differently from a left-to-right
+ *            loop). out must not be arr ([algos]: "No in-place scan") ->
+ *            MT_ERR_ALIAS; other overlaps are undefined.
  * scratch  : device memory of at least
  *            mt_scan_scratch_slots(capacity, dtype, MT_SCRATCH_SCAN) 8-byte
  *            slots, 16-byte aligned. It needs no initialisation ([algos]
@@ -173,8 +181,8 @@ int mt_inclusive_scan(const void *arr, void *out, void *scratch, const int32_t *
  * result carries the sign of the first zero). f32 add is summed in f32 in a
  * fixed grouping (the same bits on every call on the same GPU).
  *
- * arr      : device array of `dtype` (MT_I32, MT_I64 or MT_F32), aligned to
- *            the element size.
+ * arr      : device array of `dtype` (any dtype of mt_exclusive_scan), aligned
+ *            to the element size.
  * out      : device pointer to one element of `dtype`.
  * scratch  : device memory of mt_scan_scratch_slots(capacity, dtype,
  *            MT_SCRATCH_REDUCE) 8-byte slots (a fixed size: the header and one

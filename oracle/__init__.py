@@ -77,6 +77,10 @@ def _np(x) -> np.ndarray:
             x = x.detach().cpu().contiguous()
             if x.dtype in (torch.bfloat16, torch.float16):
                 x = x.view(torch.int16)
+            elif x.dtype == torch.uint32:  # numpy reads the signed bits back as unsigned
+                return np.ascontiguousarray(x.view(torch.int32).numpy()).view(np.uint32)
+            elif x.dtype == torch.uint64:
+                return np.ascontiguousarray(x.view(torch.int64).numpy()).view(np.uint64)
             return np.ascontiguousarray(x.numpy())
     except ImportError:  # pragma: no cover
         pass

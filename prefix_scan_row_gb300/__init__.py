@@ -30,7 +30,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmtscan.so")
 
-MT_F32, MT_BF16, MT_F16, MT_I32, MT_I64 = 0, 1, 2, 3, 4
+MT_F32, MT_BF16, MT_F16, MT_I32, MT_I64, MT_U32, MT_U64, MT_F64 = 0, 1, 2, 3, 4, 5, 6, 7
 MT_ADD, MT_MIN, MT_MAX, MT_MUL = 0, 1, 2, 3
 MT_SCRATCH_SCAN, MT_SCRATCH_SELECT, MT_SCRATCH_REDUCE = 1, 2, 3
 MT_OK = 0
@@ -41,7 +41,8 @@ MT_ERR_MEMORY = -8
 MT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_F16,
-              torch.int32: MT_I32, torch.int64: MT_I64}
+              torch.int32: MT_I32, torch.int64: MT_I64, torch.uint32: MT_U32, torch.uint64: MT_U64,
+              torch.float64: MT_F64}
 OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX, "mul": MT_MUL}
 
 EXPORTS = ("mt_scan_rows", "mt_scan_rows_op", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",

@@ -103,11 +103,17 @@ static bool make_launch(void *stream, Launch *L, int *dev) {
     return L->sm_count > 0;
 }
 
+// The dtypes of the 1-D scans and the reduce.
+static bool is_1d_dtype(int dtype) {
+    return dtype == MT_F32 || dtype == MT_I32 || dtype == MT_I64 || dtype == MT_U32 || dtype == MT_U64 ||
+           dtype == MT_F64;
+}
+
 static int elem_size(int dtype) {
     switch (dtype) {
-    case MT_F32: case MT_I32: return 4;
+    case MT_F32: case MT_I32: case MT_U32: return 4;
     case MT_BF16: case MT_F16: return 2;
-    case MT_I64: return 8;
+    case MT_I64: case MT_U64: case MT_F64: return 8;
     default: return 0;
     }
 }
@@ -225,7 +231,7 @@ extern "C" int mt_scan_rows_op(const void *inp, void *out, int64_t rows, int64_t
 // The exclusive and inclusive 1-D scans share their checks and kernel.
 static int scan1d_call(const void *arr, void *out, void *scratch, const int32_t *n_dev, int dtype,
                        int op, bool inclusive, void *stream) {
-    if (dtype != MT_F32 && dtype != MT_I32 && dtype != MT_I64)
+    if (!is_1d_dtype(dtype))
         return MT_ERR_DTYPE;
     if (op < MT_ADD || op > MT_MAX)
         return MT_ERR_ARG;
@@ -265,7 +271,7 @@ extern "C" int mt_inclusive_scan(const void *arr, void *out, void *scratch, cons
 
 extern "C" int mt_reduce(const void *arr, void *out, void *scratch, const int32_t *n_dev, int dtype,
                          int op, void *stream) {
-    if (dtype != MT_F32 && dtype != MT_I32 && dtype != MT_I64)
+    if (!is_1d_dtype(dtype))
         return MT_ERR_DTYPE;
     if (op < MT_ADD || op > MT_MAX)
         return MT_ERR_ARG;
@@ -337,8 +343,8 @@ extern "C" int mt_scan_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MT_ERR_CUDA;
     int worst = MT_OK;
-    cudaError_t (*takers[5])(int *) = {rows_take_error, rows_minmax_take_error, rows_mul_take_error,
-                                       scan1d_take_error, select_take_error};
+    cudaError_t (*takers[6])(int *) = {rows_take_error, rows_minmax_take_error, rows_mul_take_error,
+                                       scan1d_take_error, scan1d_ext_take_error, select_take_error};
     for (auto take : takers) {
         int code = 0;
         if (take(&code) != cudaSuccess)

@@ -85,6 +85,9 @@ int scan1d_rec_slots(int dtype);
 cudaError_t scan1d_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
                           int dtype, int op, bool inclusive, bool aligned_io, const Launch &L);
 cudaError_t scan1d_take_error(int *code);
+struct SegArgs;
+cudaError_t scan1d_launch_ext(const SegArgs &a, int dtype, int op, const Launch &L);  // mt_scan1d_ext.cu
+cudaError_t scan1d_ext_take_error(int *code);
 
 // ---- device-wide reduction (mt_reduce.cu) ---------------------------------
 int64_t reduce_scratch_slots();  // fixed: header + one partial per CTA

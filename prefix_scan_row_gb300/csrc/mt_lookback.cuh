@@ -58,7 +58,7 @@ template <class Acc> struct Status<Acc, true> {
 template <class Acc> struct Status<Acc, false> {
     static constexpr int kSlots = MT_REC_SLOTS;
     __device__ __forceinline__ static void publish(uint64_t *rec, uint32_t flag, Acc v) {
-        const uint64_t u = (uint64_t)v;
+        const uint64_t u = bits64<Acc>(v);
         const uint64_t f = (uint64_t)flag << 32;
         st_relaxed_u64(rec, f | (u & 0xffffffffull));
         st_relaxed_u64(rec + 1, f | (u >> 32));
@@ -68,7 +68,7 @@ template <class Acc> struct Status<Acc, false> {
         const uint64_t w1 = ld_relaxed_u64(rec + 1);
         const uint32_t f0 = (uint32_t)(w0 >> 32), f1 = (uint32_t)(w1 >> 32);
         flag = (f0 == f1) ? f0 : kEmpty;
-        v = (Acc)((w1 << 32) | (w0 & 0xffffffffull));
+        v = from64<Acc>((w1 << 32) | (w0 & 0xffffffffull));
     }
 };
 

@@ -1,5 +1,6 @@
 // mt_reduce.cu -- device-wide reduction out[0] = op(arr[0:n]) (add / min /
-// max over i32, i64 and f32) with the live count read on the device.
+// max over i32, i64, u32, u64, f32 and f64) with the live count read on the
+// device.
 //
 // Semantics follow the Quadrants "Algorithms" user guide, section
 // "qd.algorithms.reduce_{add,min,max}": the result goes to out[0], and an
@@ -11,15 +12,15 @@
 // grouping, so a float sum's rounding is the same on every call.
 //
 // min/max keep the earliest of equal elements ((b < a) ? b : a). For integers
-// equal values are identical, so any grouping gives that result. For f32 the
-// two zeros compare equal but differ in sign, so f32 min/max also remember
-// where their extreme came from: each thread folds its elements in index
-// order with a strict comparison (a later equal element never replaces an
-// earlier one) and keeps the index of the 16-byte chunk its extreme came
-// from; threads and CTAs then combine 64-bit keys (the value's order in the
-// high half, the chunk index in the low half, ties to the lower chunk), and
-// the last CTA re-reads the winning chunk and returns its earliest element
-// equal to the extreme, with that element's own bits.
+// equal values are identical, so any grouping gives that result. For floats
+// the two zeros compare equal but differ in sign, so f32/f64 min/max also
+// remember where their extreme came from: each thread folds its elements in
+// index order with a strict comparison (a later equal element never replaces
+// an earlier one) and keeps the index of the 16-byte chunk its extreme came
+// from; threads and CTAs then combine (order, chunk) pairs -- the value's
+// order-preserving image, ties to the lower chunk -- and the last CTA
+// re-reads the winning chunk and returns its earliest element equal to the
+// extreme, with that element's own bits.
 #include <type_traits>
 
 #include "mt_tile.cuh"
@@ -29,92 +30,107 @@ namespace mt {
 constexpr int kRedThreads = 256;
 constexpr int kRedItems = 8;  // 16-byte chunks per thread per tile: 128 bytes in flight
 constexpr int kRedTileChunks = kRedThreads * kRedItems;
-constexpr int kRedMaxCtas = 4096;  // partial slots in the scratch
+constexpr int kRedMaxCtas = 4096;   // partials in the scratch
+constexpr int kRedPartialSlots = 2;  // 8-byte slots per partial (a pair needs two)
 
 struct RedArgs {
     const char *in;
     void *out;
-    uint64_t *scratch;  // [0] ticket counter (zero at launch), then kRedMaxCtas partial slots
+    uint64_t *scratch;  // [0] ticket counter (zero at launch), then kRedMaxCtas partials
     const int32_t *n_dev;
 };
 
-// ---- what is folded: the value itself, or an f32 (value, index) key --------
+// ---- what is folded -----------------------------------------------------------
+// The value itself (integers; float sums).
 template <class S, class Op>
 struct Fold {
     using Acc = typename Codec<S>::Acc;
     using T = Acc;
     __device__ __forceinline__ static T ident() { return Op::template identity<Acc>(); }
-    __device__ __forceinline__ static T make(Acc v, int64_t) { return v; }
     __device__ __forceinline__ static T apply(T a, T b) { return Op::apply(a, b); }
-    __device__ __forceinline__ static uint64_t bits(T v) {
+    __device__ __forceinline__ static T shfl_down(T v, int d) { return __shfl_down_sync(kFull, v, d); }
+    __device__ __forceinline__ static void store(uint64_t *p, T v) {
         if constexpr (sizeof(T) == 8)
-            return (uint64_t)v;
+            st_relaxed_u64(p, bits64<T>(v));
         else
-            return (uint64_t)bits32<T>(v);
+            st_relaxed_u64(p, (uint64_t)bits32<T>(v));
     }
-    __device__ __forceinline__ static T from(uint64_t b) {
+    __device__ __forceinline__ static T load(const uint64_t *p) {
         if constexpr (sizeof(T) == 8)
-            return (T)b;
+            return from64<T>(ld_relaxed_u64(p));
         else
-            return from32<T>((uint32_t)b);
+            return from32<T>((uint32_t)ld_relaxed_u64(p));
     }
 };
 
-// Order-preserving 32-bit image of an f32 in which -0 and +0 coincide.
-__device__ __forceinline__ uint32_t f32_order(float v) {
-    uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+// Order-preserving unsigned images of f32 / f64 in which -0 and +0 coincide.
+__device__ __forceinline__ uint64_t float_order(float v) {
+    const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ uint64_t float_order(double v) {
+    const uint64_t u = (uint64_t)__double_as_longlong(v == 0.0 ? 0.0 : v);
+    return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
 
-// f32 min/max: a float and the chunk it came from per thread; 64-bit keys
-// (order, chunk) between threads. min: the smallest key wins; max: the
-// largest key wins with ~chunk in the low half, so equal values still
-// prefer the lower chunk.
 constexpr uint32_t kNoChunk = 0xffffffffu;
 
+// A float's extreme and the chunk it came from (kNoChunk: none yet).
+template <class V>
 struct ChunkState {
-    float v;     // the thread's extreme so far
-    uint32_t c;  // the chunk it came from (kNoChunk: none yet)
+    V v;
+    uint32_t c;
 };
 
-template <bool kMax>
+// f32/f64 min/max: threads fold ChunkState; between threads and CTAs an
+// (order, chunk) pair, the better order winning and equal orders going to
+// the lower chunk.
+template <class V, bool kMax>
 struct ChunkFold {
-    using T = uint64_t;
-    using State = ChunkState;
-    __device__ __forceinline__ static float ident_v() { return kMax ? -INFINITY : INFINITY; }
-    __device__ __forceinline__ static bool better(float x, float v) { return kMax ? (x > v) : (x < v); }
-    __device__ __forceinline__ static T ident() { return key(State{ident_v(), kNoChunk}); }
-    __device__ __forceinline__ static T key(const State &st) {
-        return ((uint64_t)f32_order(st.v) << 32) | (kMax ? (uint64_t)(~st.c) : (uint64_t)st.c);
+    struct T {
+        uint64_t o;  // float_order of the extreme
+        uint32_t c;  // its chunk
+    };
+    __device__ __forceinline__ static V ident_v() { return kMax ? Lim<V>::lo() : Lim<V>::hi(); }
+    __device__ __forceinline__ static bool better(V x, V v) { return kMax ? (x > v) : (x < v); }
+    __device__ __forceinline__ static T pair(const ChunkState<V> &st) { return T{float_order(st.v), st.c}; }
+    __device__ __forceinline__ static T ident() { return T{float_order(ident_v()), kNoChunk}; }
+    __device__ __forceinline__ static T apply(T a, T b) {
+        const bool take_b = (kMax ? (b.o > a.o) : (b.o < a.o)) || (b.o == a.o && b.c < a.c);
+        return take_b ? b : a;
     }
-    __device__ __forceinline__ static uint32_t chunk(T k) { return kMax ? ~(uint32_t)k : (uint32_t)k; }
-    __device__ __forceinline__ static uint32_t order(T k) { return (uint32_t)(k >> 32); }
-    __device__ __forceinline__ static T apply(T a, T b) { return kMax ? (b > a ? b : a) : (b < a ? b : a); }
-    __device__ __forceinline__ static uint64_t bits(T v) { return v; }
-    __device__ __forceinline__ static T from(uint64_t b) { return b; }
+    __device__ __forceinline__ static T shfl_down(T v, int d) {
+        return T{__shfl_down_sync(kFull, v.o, d), __shfl_down_sync(kFull, v.c, d)};
+    }
+    __device__ __forceinline__ static void store(uint64_t *p, T v) {
+        st_relaxed_u64(p, v.o);
+        st_relaxed_u64(p + 1, (uint64_t)v.c);
+    }
+    __device__ __forceinline__ static T load(const uint64_t *p) {
+        return T{ld_relaxed_u64(p), (uint32_t)ld_relaxed_u64(p + 1)};
+    }
 };
 
 template <class S, class Op>
 struct FoldOf {
     using type = Fold<S, Op>;
 };
-template <>
-struct FoldOf<float, OpMin> {
-    using type = ChunkFold<false>;
-};
-template <>
-struct FoldOf<float, OpMax> {
-    using type = ChunkFold<true>;
-};
+template <> struct FoldOf<float, OpMin> { using type = ChunkFold<float, false>; };
+template <> struct FoldOf<float, OpMax> { using type = ChunkFold<float, true>; };
+template <> struct FoldOf<double, OpMin> { using type = ChunkFold<double, false>; };
+template <> struct FoldOf<double, OpMax> { using type = ChunkFold<double, true>; };
+
 template <class F>
-constexpr bool kChunkFold = std::is_same<F, ChunkFold<false>>::value || std::is_same<F, ChunkFold<true>>::value;
+struct IsChunkFold : std::false_type {};
+template <class V, bool kMax>
+struct IsChunkFold<ChunkFold<V, kMax>> : std::true_type {};
 
 template <class F>
 __device__ __forceinline__ typename F::T block_fold(typename F::T v, typename F::T *sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
-        v = F::apply(v, __shfl_down_sync(kFull, v, d));  // lane order kept: lower lanes left
+        v = F::apply(v, F::shfl_down(v, d));  // lower lanes stay the left operand
     if (lane == 0)
         sm[warp] = v;
     __syncthreads();
@@ -133,6 +149,7 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
     using Acc = typename C::Acc;
     using F = typename FoldOf<S, Op>::type;
     using T = typename F::T;
+    constexpr bool kChunk = IsChunkFold<F>::value;
     constexpr int E = C::E;
     constexpr int64_t s = sizeof(S);
     __shared__ T sm[kRedThreads / 32];
@@ -146,8 +163,8 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
     const int64_t nchunks = n > 0 ? (hi + E - 1) / E : 0;  // no element: touch nothing
 
     T acc = F::ident();
-    [[maybe_unused]] ChunkState st{0.0f, kNoChunk};
-    if constexpr (kChunkFold<F>)
+    [[maybe_unused]] ChunkState<Acc> st{Acc(0), kNoChunk};
+    if constexpr (kChunk)
         st.v = F::ident_v();
     for (int64_t t = blockIdx.x; t * kRedTileChunks < nchunks; t += gridDim.x) {
         const int64_t c0 = t * kRedTileChunks;
@@ -166,9 +183,9 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
             const int64_t v0 = c * E;
             Acc x[E];
             C::unpack(raw[j], x);
-            if constexpr (kChunkFold<F>) {
+            if constexpr (kChunk) {
                 // the chunk's extreme, earliest first; then the thread's
-                float m = F::ident_v();
+                Acc m = F::ident_v();
 #pragma unroll
                 for (int k = 0; k < E; ++k)
                     if ((full || (v0 + k >= lo && v0 + k < hi)) && F::better(x[k], m))
@@ -181,17 +198,17 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
 #pragma unroll
                 for (int k = 0; k < E; ++k)
                     if (full || (v0 + k >= lo && v0 + k < hi))
-                        acc = F::apply(acc, F::make(x[k], v0 + k - head));
+                        acc = F::apply(acc, x[k]);
             }
         }
     }
-    if constexpr (kChunkFold<F>)
-        acc = F::key(st);
+    if constexpr (kChunk)
+        acc = F::pair(st);
     const T part = block_fold<F>(acc, sm);
 
-    // Partial to scratch; the last CTA to arrive folds all partials in order.
+    // Partial to scratch; the last CTA to arrive folds all partials.
     if (threadIdx.x == 0) {
-        st_relaxed_u64(a.scratch + kHeaderSlots + blockIdx.x, F::bits(part));
+        F::store(a.scratch + kHeaderSlots + kRedPartialSlots * blockIdx.x, part);
         __threadfence();
         const unsigned long long ticket = atomicAdd(reinterpret_cast<unsigned long long *>(a.scratch), 1ull);
         last = ticket == gridDim.x - 1;
@@ -204,31 +221,30 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
     // thread i folds partials i, i + 256, ...; the block fold then combines the
     // threads in a fixed tree: the same grouping on every call.
     for (int i = threadIdx.x; i < (int)gridDim.x; i += kRedThreads)
-        r = F::apply(r, F::from(ld_relaxed_u64(a.scratch + kHeaderSlots + i)));
+        r = F::apply(r, F::load(a.scratch + kHeaderSlots + kRedPartialSlots * i));
     r = block_fold<F>(r, sm);
     if (threadIdx.x == 0) {
-        if constexpr (!kChunkFold<F>) {
+        if constexpr (!kChunk) {
             *static_cast<S *>(a.out) = (S)r;
         } else {
             // the earliest element of the winning chunk equal to the extreme,
             // with its own bits; no such chunk: the identity (or an infinity
             // equal to it)
-            float res = F::ident_v();
-            const uint32_t c = F::chunk(r);
-            if (c != kNoChunk) {
+            Acc res = F::ident_v();
+            if (r.c != kNoChunk) {
                 Acc x[E];
-                C::unpack(ld_stream(vin + c), x);
+                C::unpack(ld_stream(vin + r.c), x);
                 bool found = false;
 #pragma unroll
                 for (int k = 0; k < E; ++k) {
-                    const int64_t v = (int64_t)c * E + k;
-                    if (!found && v >= lo && v < hi && f32_order(x[k]) == F::order(r)) {
+                    const int64_t v = (int64_t)r.c * E + k;
+                    if (!found && v >= lo && v < hi && float_order(x[k]) == r.o) {
                         res = x[k];
                         found = true;
                     }
                 }
             }
-            *static_cast<float *>(a.out) = res;
+            *static_cast<S *>(a.out) = res;
         }
         a.scratch[0] = 0ull;  // the ticket counter, ready for the next call
     }
@@ -258,7 +274,7 @@ static cudaError_t launch_reduce(const RedArgs &a, const Launch &L) {
     return e;
 }
 
-int64_t reduce_scratch_slots() { return kHeaderSlots + kRedMaxCtas; }
+int64_t reduce_scratch_slots() { return kHeaderSlots + (int64_t)kRedPartialSlots * kRedMaxCtas; }
 
 template <class S>
 static cudaError_t reduce_op(int op, const RedArgs &a, const Launch &L) {
@@ -281,6 +297,9 @@ cudaError_t reduce_launch(const void *arr, void *out, uint64_t *scratch, const i
     case 0: return reduce_op<float>(op, a, L);
     case 3: return reduce_op<int32_t>(op, a, L);
     case 4: return reduce_op<int64_t>(op, a, L);
+    case 5: return reduce_op<uint32_t>(op, a, L);
+    case 6: return reduce_op<uint64_t>(op, a, L);
+    case 7: return reduce_op<double>(op, a, L);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -229,7 +229,7 @@ struct Staged {
         for (int w = 0; w < kNW; ++w)
             agg = Op::apply(agg, sm.red[0][w]);
         constexpr bool kOrderFree = std::is_same<Op, OpAdd>::value || std::is_same<Op, OpMul>::value ||
-                                    !std::is_same<Acc, float>::value;
+                                    !std::is_floating_point<Acc>::value;
         if constexpr (!kOrderFree) {
             if (agg == Acc(0)) {  // block-uniform: every thread folded the same totals
                 __syncthreads();  // all reads of sm.red are done

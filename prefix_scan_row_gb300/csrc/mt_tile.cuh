@@ -50,6 +50,18 @@ template <> struct Lim<float> {
     __device__ __forceinline__ static float hi() { return __int_as_float(0x7f800000); }   // +inf
     __device__ __forceinline__ static float lo() { return __int_as_float((int)0xff800000u); }  // -inf
 };
+template <> struct Lim<double> {
+    __device__ __forceinline__ static double hi() { return __longlong_as_double(0x7ff0000000000000ll); }  // +inf
+    __device__ __forceinline__ static double lo() { return __longlong_as_double((long long)0xfff0000000000000ull); }
+};
+template <> struct Lim<uint32_t> {
+    __device__ __forceinline__ static uint32_t hi() { return 0xffffffffu; }
+    __device__ __forceinline__ static uint32_t lo() { return 0u; }
+};
+template <> struct Lim<uint64_t> {
+    __device__ __forceinline__ static uint64_t hi() { return 0xffffffffffffffffull; }
+    __device__ __forceinline__ static uint64_t lo() { return 0ull; }
+};
 template <> struct Lim<int32_t> {
     __device__ __forceinline__ static int32_t hi() { return 0x7fffffff; }
     __device__ __forceinline__ static int32_t lo() { return (int32_t)0x80000000u; }
@@ -70,6 +82,8 @@ struct OpAdd {
     __device__ __forceinline__ static int64_t apply(int64_t a, int64_t b) {
         return (int64_t)((uint64_t)a + (uint64_t)b);
     }
+    __device__ __forceinline__ static uint64_t apply(uint64_t a, uint64_t b) { return a + b; }
+    __device__ __forceinline__ static double apply(double a, double b) { return a + b; }
 };
 
 // min/max keep the earlier operand on ties, so any grouping gives the same
@@ -183,6 +197,46 @@ template <> struct Codec<int64_t> {
     __device__ __forceinline__ static void store1(int64_t *p, Acc v) { *p = v; }
 };
 
+template <> struct Codec<uint32_t> {
+    using Acc = uint32_t;
+    static constexpr int E = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) { return make_uint4(x[0], x[1], x[2], x[3]); }
+    __device__ __forceinline__ static Acc load1(const uint32_t *p) { return *p; }
+    __device__ __forceinline__ static void store1(uint32_t *p, Acc v) { *p = v; }
+};
+
+template <> struct Codec<uint64_t> {
+    using Acc = uint64_t;
+    static constexpr int E = 2;
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        x[0] = ((uint64_t)v.y << 32) | v.x;
+        x[1] = ((uint64_t)v.w << 32) | v.z;
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4((uint32_t)x[0], (uint32_t)(x[0] >> 32), (uint32_t)x[1], (uint32_t)(x[1] >> 32));
+    }
+    __device__ __forceinline__ static Acc load1(const uint64_t *p) { return *p; }
+    __device__ __forceinline__ static void store1(uint64_t *p, Acc v) { *p = v; }
+};
+
+template <> struct Codec<double> {
+    using Acc = double;
+    static constexpr int E = 2;
+    __device__ __forceinline__ static void unpack(const uint4 &v, Acc (&x)[E]) {
+        x[0] = __hiloint2double((int)v.y, (int)v.x);
+        x[1] = __hiloint2double((int)v.w, (int)v.z);
+    }
+    __device__ __forceinline__ static uint4 pack(const Acc (&x)[E]) {
+        return make_uint4((uint32_t)__double2loint(x[0]), (uint32_t)__double2hiint(x[0]),
+                          (uint32_t)__double2loint(x[1]), (uint32_t)__double2hiint(x[1]));
+    }
+    __device__ __forceinline__ static Acc load1(const double *p) { return *p; }
+    __device__ __forceinline__ static void store1(double *p, Acc v) { *p = v; }
+};
+
 // ---------------------------------------------------------------------------
 // Memory primitives (inline PTX).
 // ---------------------------------------------------------------------------
@@ -273,5 +327,14 @@ template <class T> __device__ __forceinline__ T from32(uint32_t b);
 template <> __device__ __forceinline__ float from32<float>(uint32_t b) { return __uint_as_float(b); }
 template <> __device__ __forceinline__ int32_t from32<int32_t>(uint32_t b) { return (int32_t)b; }
 template <> __device__ __forceinline__ uint32_t from32<uint32_t>(uint32_t b) { return b; }
+// 8-byte values as raw bits (status records, partials).
+template <class T> __device__ __forceinline__ uint64_t bits64(T v);
+template <> __device__ __forceinline__ uint64_t bits64<int64_t>(int64_t v) { return (uint64_t)v; }
+template <> __device__ __forceinline__ uint64_t bits64<uint64_t>(uint64_t v) { return v; }
+template <> __device__ __forceinline__ uint64_t bits64<double>(double v) { return (uint64_t)__double_as_longlong(v); }
+template <class T> __device__ __forceinline__ T from64(uint64_t b);
+template <> __device__ __forceinline__ int64_t from64<int64_t>(uint64_t b) { return (int64_t)b; }
+template <> __device__ __forceinline__ uint64_t from64<uint64_t>(uint64_t b) { return b; }
+template <> __device__ __forceinline__ double from64<double>(uint64_t b) { return __longlong_as_double((long long)b); }
 
 }  // namespace mt

@@ -13,7 +13,9 @@ Tolerances (written here, used by every parity test):
     most k f32 roundings of relative size <= 2^-24 (no underflow on the
     inputs used), so |gpu - p64| <= ((1 + 2^-24)^(i+1) - 1) |p64|, plus
     ulp_T(RN_T(p64)) for bf16/f16 storage;
-  * row min/max: bit-exact (the results are input values).
+  * row min/max: bit-exact (the results are input values);
+  * f64 add (1-D): |gpu - p| <= 1e-12 * sum_{j<=i} |x_j| + 1e-15, p the oracle's
+    long-double prefix; u32/u64 and f64 min/max: bit-exact.
 """
 from __future__ import annotations
 
@@ -23,6 +25,22 @@ import torch
 import oracle
 
 REL, ABS = 1e-5, 1e-6
+REL64, ABS64 = 1e-12, 1e-15  # f64 add: the f32 rule with f64's spacing
+
+
+_BITS = {"i32": np.uint32, "f32": np.uint32, "u32": np.uint32, "i64": np.uint64, "u64": np.uint64,
+         "f64": np.uint64}
+
+
+def _np_cpu(t: torch.Tensor) -> np.ndarray:
+    """A device tensor as a numpy array (unsigned 32/64-bit tensors through
+    their signed bit patterns, which numpy then reads as unsigned)."""
+    t = t.detach()
+    if t.dtype == torch.uint32:
+        return t.view(torch.int32).to("cpu").contiguous().numpy().view(np.uint32)
+    if t.dtype == torch.uint64:
+        return t.view(torch.int64).to("cpu").contiguous().numpy().view(np.uint64)
+    return t.to("cpu").contiguous().numpy()
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
@@ -63,16 +81,16 @@ def assert_scan_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dt
     """1-D exclusive (or inclusive) scan of arr[0:n]: bit-exact except f32 add
     (tolerance)."""
     scan = oracle.inclusive_scan if inclusive else oracle.exclusive_scan
-    got = gpu_out[:n].detach().to("cpu").numpy()
-    if dtype == "f32" and op == "add":
+    got = _np_cpu(gpu_out[:n])
+    if dtype in ("f32", "f64") and op == "add":
         _, p64, mag = scan(arr_cpu, n, dtype, op, want_f64=True)
         err = np.abs(got.astype(np.float64) - p64)
-        bound = REL * mag + ABS
+        bound = (REL * mag + ABS) if dtype == "f32" else (REL64 * mag + ABS64)
         bad = np.nonzero(~(err <= bound))[0]
         assert bad.size == 0, f"{bad.size} out of tolerance; first {bad[0]}: {got[bad[0]]} vs {p64[bad[0]]}"
         return
     ref = scan(arr_cpu, n, dtype, op)
-    w = {"i32": np.uint32, "f32": np.uint32, "i64": np.uint64}[dtype]
+    w = _BITS[dtype]
     bad = np.nonzero(got.view(w) != ref.view(w))[0]
     assert bad.size == 0, f"{bad.size} mismatches; first at {bad[0]}: {got[bad[0]]} vs {ref[bad[0]]}"
 
@@ -112,13 +130,14 @@ def assert_rows_op_close(gpu_out: torch.Tensor, x_cpu: torch.Tensor, dtype: str,
 def assert_reduce_matches(gpu_out: torch.Tensor, arr_cpu: torch.Tensor, n: int, dtype: str, op: str):
     """out[0] of a reduction: bit-exact except f32 add, which must lie within
     REL * sum|x| + ABS of the fp64 sum."""
-    got = gpu_out[:1].detach().to("cpu").numpy()[0]
-    if dtype == "f32" and op == "add":
+    got = _np_cpu(gpu_out[:1])[0]
+    if dtype in ("f32", "f64") and op == "add":
         _, s64, m64 = oracle.reduce(arr_cpu, n, dtype, op, want_f64=True)
-        assert abs(float(got) - s64) <= REL * m64 + ABS, f"{got} vs {s64} (sum|x| {m64})"
+        rel, ab = (REL, ABS) if dtype == "f32" else (REL64, ABS64)
+        assert abs(float(got) - s64) <= rel * m64 + ab, f"{got} vs {s64} (sum|x| {m64})"
         return
     ref = oracle.reduce(arr_cpu, n, dtype, op)
-    w = {"i32": np.uint32, "f32": np.uint32, "i64": np.uint64}[dtype]
+    w = _BITS[dtype]
     assert np.array([got]).view(w)[0] == np.array([ref]).view(w)[0], f"{got} vs {ref}"
 
 

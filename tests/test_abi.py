@@ -133,11 +133,13 @@ def test_scratch_slots(lib):
     # 6144 elements per super-tile for i64
     assert f(6144, I64, 1) == 4 + 16 * 2
     assert f(6143, I64, 1) == 4 + 16 * 1
+    # u32 as i32; u64 and f64 as i64
+    assert f(12288, 5, 1) == 4 + 16 * 2 and f(6144, 6, 1) == f(6144, 7, 1) == 4 + 16 * 2
     # select: 8192 flags per tile
     assert f(1 << 28, I32, 2) == 4 + 16 * (1 << 15)
     assert f(1, I32, 2) == 4 + 16 * 1
     # reduce: a header and one partial slot per CTA, whatever the capacity
-    assert f(1 << 28, I32, 3) == f(0, F32, 3) == f(5, I64, 3) == 4 + 4096
+    assert f(1 << 28, I32, 3) == f(0, F32, 3) == f(5, I64, 3) == f(7, 7, 3) == 4 + 2 * 4096
     assert f(10, BF16, 3) == -1
 
 

@@ -63,6 +63,23 @@ def uniform(shape, seed: int, lo: float, hi: float, dtype: str = "f32") -> torch
     return x.to(_STORAGE[dtype])
 
 
+def bits_uniform(shape, seed: int, dtype: str) -> torch.Tensor:
+    """u32 / u64 values with every bit pattern equally likely (u64: the low
+    63 bits uniform, the top bit set half the time)."""
+    g = generator(seed)
+    if dtype == "u32":
+        return torch.randint(-(2**31), 2**31, shape, generator=g, dtype=torch.int32).view(torch.uint32)
+    lo = torch.randint(-(2**62), 2**62, shape, generator=g, dtype=torch.int64)
+    top = torch.randint(0, 2, shape, generator=g, dtype=torch.int64)
+    return (lo ^ (top << 63)).view(torch.uint64)
+
+
+def uniform64(shape, seed: int, lo: float, hi: float) -> torch.Tensor:
+    """iid uniform[lo, hi) drawn directly in f64."""
+    u = torch.rand(shape, generator=generator(seed), dtype=torch.float64)
+    return u.mul_(hi - lo).add_(lo)
+
+
 def normal(shape, seed: int, dtype: str = "f32") -> torch.Tensor:
     """iid N(0, 1) drawn in f32, then cast (round to nearest even) to storage."""
     x = torch.randn(shape, generator=generator(seed), dtype=torch.float32)
@@ -122,6 +139,14 @@ def scan1d(dtype: str, capacity: int = SCAN1D_CAPACITY, seed: int = SEED_SCAN1D)
         return randint((capacity,), seed, 0, 1 << 20, "i64")
     if dtype == "f32":
         return uniform((capacity,), seed, -1.0, 1.0, "f32")
+    # the other dtypes of the 1-D calls, drawn the same way (unsigned values
+    # returned as their signed twins: the caller views them as unsigned)
+    if dtype == "u32":
+        return randint((capacity,), seed, 0, 16, "i32")
+    if dtype == "u64":
+        return randint((capacity,), seed, 0, 1 << 20, "i64")
+    if dtype == "f64":
+        return uniform64((capacity,), seed, -1.0, 1.0)
     raise ValueError(dtype)
 
 
