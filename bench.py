@@ -533,6 +533,18 @@ def run_suite(args):
         timeit(f"select f32 n={ns} p={p}", lambda: mt.mt_select(v, f, o, num, scr, nd),
                5 * ns + 4 * k, ns)
         del v, f, o, scr
+    for p in (0.5, 0.01):  # 8-byte elements: the same flags, f64 values
+        if not wanted(f"select_wide f64 n={ns} p={p}"):
+            continue
+        v, f = workloads.select_inputs(ns, p)
+        k = int(f.sum())
+        v, f = v.to(dev).to(torch.float64), f.to(dev)
+        o = torch.empty_like(v)
+        num = torch.zeros(1, dtype=torch.int32, device=dev)
+        scr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_SELECT, device=dev)
+        timeit(f"select_wide f64 n={ns} p={p}", lambda: mt.mt_select_wide(v, f, o, num, scr, nd),
+               9 * ns + 8 * k, ns)
+        del v, f, o, scr
     if args.suite_out:
         with open(args.suite_out, "w") as fh:
             json.dump({"peak_gbs": peak, "peak_source": src, "rows": rows_out}, fh, indent=1)

@@ -217,6 +217,19 @@ int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out
               void *scratch, const int32_t *n_dev, void *stream);
 
 /*
+ * mt_select_wide -- mt_select for elements of 4 or 8 bytes (elem_bytes),
+ * copied bit for bit: [algos] "qd.algorithms.select" takes no dtype ("the
+ * scatter is dtype-agnostic") and its API covers 32- and 64-bit scalars.
+ * Arguments, scratch (MT_SCRATCH_SELECT), results and errors are those of
+ * mt_select, with arr and out aligned to elem_bytes. 8-byte elements are
+ * bulk-copied, so arr and flags must then be 16-byte aligned
+ * (MT_ERR_ALIGN otherwise; allocations from cudaMalloc or torch are). An
+ * elem_bytes other than 4 or 8 is MT_ERR_ARG.
+ */
+int mt_select_wide(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
+                   void *scratch, const int32_t *n_dev, int elem_bytes, void *stream);
+
+/*
  * mt_scan_scratch_slots -- number of 8-byte scratch slots that
  * mt_exclusive_scan / mt_inclusive_scan (kind MT_SCRATCH_SCAN, with their
  * dtype), mt_select (kind MT_SCRATCH_SELECT, dtype ignored) or mt_reduce

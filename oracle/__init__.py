@@ -59,6 +59,8 @@ def lib():
         L.oracle_reduce.restype = i32
         L.oracle_select.argtypes = [p, p, p, i64]
         L.oracle_select.restype = i64
+        L.oracle_select_wide.argtypes = [p, p, p, i64, i32]
+        L.oracle_select_wide.restype = i64
         L.oracle_decode_half.argtypes = [p, p, i64, i32]
         L.oracle_decode_half.restype = None
         L.oracle_encode_half.argtypes = [p, p, i64, i32]
@@ -192,6 +194,19 @@ def select(arr, flags, n: int):
     f = np.ascontiguousarray(_np(flags)[:n]).view(np.uint8)
     out = np.empty((max(n, 1),), dtype=np.uint32)
     k = lib().oracle_select(_ptr(a), _ptr(f), _ptr(out), n)
+    return out[:k].copy(), int(k)
+
+
+def select_wide(arr, flags, n: int, elem_bytes: int):
+    """Stream compaction of 4- or 8-byte elements; returns (out[0:num_out] as
+    u32/u64 bit patterns, num_out)."""
+    w = np.uint32 if elem_bytes == 4 else np.uint64
+    a = np.ascontiguousarray(_np(arr)[:n]).view(w)
+    f = np.ascontiguousarray(_np(flags)[:n]).view(np.uint8)
+    out = np.empty((max(n, 1),), dtype=w)
+    k = lib().oracle_select_wide(_ptr(a), _ptr(f), _ptr(out), n, elem_bytes)
+    if k < 0:
+        raise ValueError("oracle_select_wide rejected its arguments")
     return out[:k].copy(), int(k)
 
 

@@ -684,3 +684,22 @@ int64_t oracle_select(const uint32_t *arr, const uint8_t *flags, uint32_t *out, 
     }
     return j;
 }
+
+/* ------------------------------------------------------------------------
+ * The same compaction for elements of `elem_bytes` bytes (4 or 8), copied
+ * byte for byte ([algos] select: no dtype, the scatter is dtype-agnostic).
+ * Returns the count, or -1 for another element size.
+ * ---------------------------------------------------------------------- */
+int64_t oracle_select_wide(const void *arr, const uint8_t *flags, void *out, int64_t n, int elem_bytes)
+{
+    if (elem_bytes != 4 && elem_bytes != 8)
+        return -1;
+    int64_t j = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (flags[i] == 1) {
+            memcpy((char *)out + j * elem_bytes, (const char *)arr + i * elem_bytes, (size_t)elem_bytes);
+            ++j;
+        }
+    }
+    return j;
+}

@@ -46,7 +46,7 @@ DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_
 OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX, "mul": MT_MUL}
 
 EXPORTS = ("mt_scan_rows", "mt_scan_rows_op", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",
-           "mt_scan_scratch_slots",
+           "mt_select_wide", "mt_scan_scratch_slots",
            "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback",
            "mt_scan_rows_noalloc")
 
@@ -75,6 +75,8 @@ def _load():
     L.mt_reduce.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_reduce.restype = i32
     L.mt_select.argtypes = [p, p, p, p, p, p, p]
+    L.mt_select_wide.argtypes = [p, p, p, p, p, p, i32, p]
+    L.mt_select_wide.restype = i32
     L.mt_select.restype = i32
     L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
     L.mt_scan_scratch_slots.restype = i64
@@ -191,6 +193,18 @@ def mt_select(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out
         raise ValueError("flags must be uint8, num_out and n_dev int32")
     _check(lib.mt_select(_ptr(arr), _ptr(flags), _ptr(out), _ptr(num_out), _ptr(scratch),
                          _ptr(n_dev), _stream(stream)), "mt_select")
+
+
+def mt_select_wide(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out: torch.Tensor,
+                   scratch: torch.Tensor, n_dev: torch.Tensor, stream=None) -> None:
+    """Stream compaction of 4- or 8-byte elements (the element size of arr)."""
+    eb = arr.element_size()
+    if out.element_size() != eb or eb not in (4, 8):
+        raise ValueError("select copies 4- or 8-byte elements; out must match arr")
+    if flags.dtype != torch.uint8 or num_out.dtype != torch.int32 or n_dev.dtype != torch.int32:
+        raise ValueError("flags must be uint8, num_out and n_dev int32")
+    _check(lib.mt_select_wide(_ptr(arr), _ptr(flags), _ptr(out), _ptr(num_out), _ptr(scratch),
+                              _ptr(n_dev), eb, _stream(stream)), "mt_select_wide")
 
 
 def mt_scan_scratch_slots(capacity: int, dtype, kind: int) -> int:

@@ -293,16 +293,20 @@ extern "C" int mt_reduce(const void *arr, void *out, void *scratch, const int32_
     return reduce_launch(arr, out, sw, n_dev, dtype, op, L) == cudaSuccess ? MT_OK : MT_ERR_CUDA;
 }
 
-extern "C" int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
-                         void *scratch, const int32_t *n_dev, void *stream) {
+// mt_select and mt_select_wide share their checks and kernels.
+static int select_call(const void *arr, const uint8_t *flags, void *out, int32_t *num_out, void *scratch,
+                       const int32_t *n_dev, int elem_bytes, void *stream) {
     if (arr == nullptr || flags == nullptr || out == nullptr || num_out == nullptr ||
-        scratch == nullptr || n_dev == nullptr)
+        scratch == nullptr || n_dev == nullptr || (elem_bytes != 4 && elem_bytes != 8))
         return MT_ERR_ARG;
     if (arr == out)
         return MT_ERR_ALIAS;
-    if (((uintptr_t)arr % 4) != 0 || ((uintptr_t)out % 4) != 0 || ((uintptr_t)num_out % 4) != 0 ||
-        ((uintptr_t)scratch % 16) != 0 || ((uintptr_t)n_dev % 4) != 0)
+    if (((uintptr_t)arr % elem_bytes) != 0 || ((uintptr_t)out % elem_bytes) != 0 ||
+        ((uintptr_t)num_out % 4) != 0 || ((uintptr_t)scratch % 16) != 0 || ((uintptr_t)n_dev % 4) != 0)
         return MT_ERR_ALIGN;
+    const bool aligned = ((uintptr_t)arr % 16 == 0) && ((uintptr_t)flags % 16 == 0);
+    if (elem_bytes == 8 && !aligned)
+        return MT_ERR_ALIGN;  // 8-byte elements are bulk-copied: arr and flags 16-byte aligned
     Launch L;
     int dev = 0;
     if (!make_launch(stream, &L, &dev))
@@ -313,10 +317,19 @@ extern "C" int mt_select(const void *arr, const uint8_t *flags, void *out, int32
     if (launch_reset(sw, 0, n_dev, select_tile_elems(), 1, 0, select_rec_slots(), num_out, L) !=
         cudaSuccess)
         return MT_ERR_CUDA;
-    const bool aligned = ((uintptr_t)arr % 16 == 0) && ((uintptr_t)flags % 16 == 0);
-    return select_launch(arr, flags, out, num_out, sw, n_dev, aligned, L) == cudaSuccess
+    return select_launch(arr, flags, out, num_out, sw, n_dev, elem_bytes, aligned, L) == cudaSuccess
                ? MT_OK
                : MT_ERR_CUDA;
+}
+
+extern "C" int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
+                         void *scratch, const int32_t *n_dev, void *stream) {
+    return select_call(arr, flags, out, num_out, scratch, n_dev, 4, stream);
+}
+
+extern "C" int mt_select_wide(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
+                              void *scratch, const int32_t *n_dev, int elem_bytes, void *stream) {
+    return select_call(arr, flags, out, num_out, scratch, n_dev, elem_bytes, stream);
 }
 
 extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) {

@@ -38,9 +38,9 @@ struct SelSmem {
 };
 
 struct SelArgs {
-    const uint32_t *arr;
+    const void *arr;  // 4-byte (k_select, k_select_staged<uint32_t>) or 8-byte elements
     const uint8_t *flags;
-    uint32_t *out;
+    void *out;
     int32_t *num_out;
     const int32_t *n_dev;
     unsigned long long *counter;
@@ -63,6 +63,7 @@ __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
 __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
     pdl_prologue();
     __shared__ SelSmem sm;
+    const uint32_t *arr = static_cast<const uint32_t *>(a.arr);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
@@ -111,13 +112,13 @@ __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
                 v[j][w] = make_uint4(0u, 0u, 0u, 0u);
                 if (fw != 0u) {
                     if (a.aligned) {
-                        v[j][w] = ld_stream(reinterpret_cast<const uint4 *>(a.arr) + (e0 + 4 * w) / 4);
+                        v[j][w] = ld_stream(reinterpret_cast<const uint4 *>(arr) + (e0 + 4 * w) / 4);
                     } else {
                         uint32_t t[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                         for (int b = 0; b < 4; ++b)
                             if ((fw >> (8 * b)) & 0xffu)
-                                t[b] = a.arr[e0 + 4 * w + b];
+                                t[b] = arr[e0 + 4 * w + b];
                         v[j][w] = make_uint4(t[0], t[1], t[2], t[3]);
                     }
                 }
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
         }
         __syncthreads();
         // One contiguous run per tile: coalesced 4-byte stores.
-        uint32_t *dst = a.out + G;
+        uint32_t *dst = static_cast<uint32_t *>(a.out) + G;
         for (uint32_t i = threadIdx.x; i < agg; i += kThreads)
             dst[i] = sm.vals[i];
         if (g == ntiles - 1 && threadIdx.x == 0)
@@ -188,9 +189,11 @@ __global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
 }
 
 // ---- staged variant (16-byte aligned flags and values) ----------------------
+// VT: the element type, copied bit for bit (4 or 8 bytes).
+template <class VT>
 struct SelStagedSmem {
     uint4 flags[kSelChunks];  // 16 flags per chunk
-    uint32_t vals[kSelTE];    // the tile's values; each warp packs its selected ones in place
+    VT vals[kSelTE];          // the tile's values; each warp packs its selected ones in place
     uint64_t bar_f;           // the flags' copy
     uint64_t bar_v;           // the values' copy
     int64_t tile;
@@ -206,9 +209,9 @@ struct SelStagedSmem {
 // only published their counts.)
 // Returns false when the values' copy did not complete in time (the caller
 // records the error and drains it).
-template <bool FULL>
-__device__ __forceinline__ bool select_tile(SelStagedSmem &sm, const SelArgs &a, int64_t g, int64_t ntiles,
-                                            int elems, uint32_t phase) {
+template <bool FULL, class VT>
+__device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs &a, int64_t g,
+                                            int64_t ntiles, int elems, uint32_t phase) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // Count: popcounts of this thread's 16-flag chunks (flags past n are 0).
     uint32_t mine = 0u;
@@ -264,7 +267,7 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem &sm, const SelArgs &a,
         const int e = wstart + step * 32 + lane;
         const bool sel = (FULL || e < elems) && fb[e] != 0;
         const unsigned bal = __ballot_sync(kFull, sel);
-        const uint32_t val = sm.vals[e];
+        const VT val = sm.vals[e];
         if (sel)
             sm.vals[wstart + cnt + __popc(bal & lt)] = val;
         cnt += __popc(bal);
@@ -272,7 +275,7 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem &sm, const SelArgs &a,
     __syncwarp();
     // The tile's output offset (the look-back ends with a block barrier).
     const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
-    uint32_t *dst = a.out + G + wpre;
+    VT *dst = static_cast<VT *>(a.out) + G + wpre;
     for (uint32_t i = lane; i < cnt; i += 32)
         dst[i] = sm.vals[wstart + i];
     if (g == ntiles - 1 && threadIdx.x == 0)
@@ -280,10 +283,11 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem &sm, const SelArgs &a,
     return true;
 }
 
+template <class VT>
 __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
     pdl_prologue();
     extern __shared__ __align__(128) unsigned char dsm[];
-    SelStagedSmem &sm = *reinterpret_cast<SelStagedSmem *>(dsm);
+    SelStagedSmem<VT> &sm = *reinterpret_cast<SelStagedSmem<VT> *>(dsm);
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
     const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
@@ -305,11 +309,11 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
             const uint32_t fb = (uint32_t)((elems + 15) / 16 * 16);
-            const uint32_t vb = (uint32_t)(((int64_t)elems * 4 + 15) / 16 * 16);
+            const uint32_t vb = (uint32_t)(((int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
             mbar_arrive_expect_tx(&sm.bar_f, fb);
             bulk_g2s(&sm.flags[0], a.flags + t0, fb, &sm.bar_f);
             mbar_arrive_expect_tx(&sm.bar_v, vb);
-            bulk_g2s(&sm.vals[0], a.arr + t0, vb, &sm.bar_v);
+            bulk_g2s(&sm.vals[0], static_cast<const VT *>(a.arr) + t0, vb, &sm.bar_v);
         }
         // Warp 0 waits for the flags; the block barrier passes the
         // completion (and the copied bytes) on to the other warps. The
@@ -320,8 +324,8 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
         if (__syncthreads_or(!ok))
             ok = false;  // every thread: the flags did not arrive
         else
-            ok = (elems == kSelTE) ? select_tile<true>(sm, a, g, ntiles, elems, phase)
-                                   : select_tile<false>(sm, a, g, ntiles, elems, phase);
+            ok = (elems == kSelTE) ? select_tile<true, VT>(sm, a, g, ntiles, elems, phase)
+                                   : select_tile<false, VT>(sm, a, g, ntiles, elems, phase);
         if (!ok) {  // block-uniform
             if (threadIdx.x == 0) {
                 atomicCAS(&g_mt_err, 0, kErrTimeout);
@@ -339,6 +343,7 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
 int64_t select_tile_elems() { return kSelTE; }
 int select_rec_slots() { return Status<uint32_t>::kSlots; }
 
+template <class VT>
 static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
     static int per_sm[128] = {0};
     int dev = 0;
@@ -347,34 +352,35 @@ static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
         return e;
     if (dev < 0 || dev >= 128)
         return cudaErrorInvalidDevice;
-    const int bytes = (int)sizeof(SelStagedSmem);
+    const int bytes = (int)sizeof(SelStagedSmem<VT>);
     if (per_sm[dev] == 0) {
-        e = cudaFuncSetAttribute(k_select_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = cudaFuncSetAttribute(k_select_staged<VT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
-        e = cudaFuncSetAttribute(k_select_staged, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(k_select_staged<VT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_staged, kThreads, bytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_staged<VT>, kThreads, bytes);
         if (e != cudaSuccess)
             return e;
         per_sm[dev] = b > 0 ? b : 1;
     }
-    e = launch_pdl(k_select_staged, (unsigned)(L.sm_count * per_sm[dev]), kThreads, bytes, L.stream, a);
+    e = launch_pdl(k_select_staged<VT>, (unsigned)(L.sm_count * per_sm[dev]), kThreads, bytes, L.stream, a);
     note_launch();
     return e;
 }
 
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
-                          uint64_t *scratch, const int32_t *n_dev, bool aligned, const Launch &L) {
+                          uint64_t *scratch, const int32_t *n_dev, int elem_bytes, bool aligned,
+                          const Launch &L) {
     static int per_sm = 0;
-    if (aligned) {
+    if (aligned || elem_bytes == 8) {  // 8-byte elements: the caller checked the alignment
         SelArgs a;
-        a.arr = static_cast<const uint32_t *>(arr);
+        a.arr = arr;
         a.flags = flags;
-        a.out = static_cast<uint32_t *>(out);
+        a.out = out;
         a.num_out = num_out;
         a.n_dev = n_dev;
         a.counter = reinterpret_cast<unsigned long long *>(scratch);
@@ -382,7 +388,7 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
         a.lb.recs = scratch + kHeaderSlots;
         a.lb.skip_tile = L.skip_tile;
         a.lb.spin_limit = L.spin_limit;
-        return launch_staged_select(a, L);
+        return elem_bytes == 8 ? launch_staged_select<uint64_t>(a, L) : launch_staged_select<uint32_t>(a, L);
     }
     if (per_sm == 0) {
         int b = 0;
@@ -392,9 +398,9 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
         per_sm = b > 0 ? b : 1;
     }
     SelArgs a;
-    a.arr = static_cast<const uint32_t *>(arr);
+    a.arr = arr;
     a.flags = flags;
-    a.out = static_cast<uint32_t *>(out);
+    a.out = out;
     a.num_out = num_out;
     a.n_dev = n_dev;
     a.counter = reinterpret_cast<unsigned long long *>(scratch);

@@ -692,4 +692,20 @@ def pin_select_brute_force():
             assert out.tolist() == want
 
 
+def pin_select_wide():
+    g = load_all()["algos_select_i32"]
+    for eb, dt in ((4, np.int32), (8, np.int64)):
+        arr = np.array(g["arr"], dtype=dt)
+        flags = np.array(g["flags"], dtype=np.uint8)
+        out, k = oracle.select_wide(arr, flags, len(arr), eb)
+        assert k == g["num_out"] and out.view(dt).tolist() == g["out"], eb
+    rng = np.random.default_rng(59)
+    for n in (0, 1, 300, 5000):
+        bits = rng.integers(0, 2**63, n, dtype=np.uint64) * np.uint64(2) + rng.integers(0, 2, n, dtype=np.uint64)
+        flags = (rng.random(n) < 0.3).astype(np.uint8)
+        out, k = oracle.select_wide(bits, flags, n, 8)
+        want = [int(b) for b, f in zip(bits, flags) if f == 1]
+        assert k == len(want) and out.tolist() == want
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -27,6 +27,7 @@ def lib():
     L.mt_inclusive_scan.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_reduce.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_select.argtypes = [p, p, p, p, p, p, p]
+    L.mt_select_wide.argtypes = [p, p, p, p, p, p, i32, p]
     L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
     L.mt_scan_scratch_slots.restype = i64
     L.mt_scan_strerror.argtypes = [i32]
@@ -117,6 +118,16 @@ def test_select_host_checks(lib):
     assert lib.mt_select(A, B, A, N, S, N, None) == ALIAS
     assert lib.mt_select(A + 2, B, S, N, S, N, None) == ALIGN
     assert lib.mt_select(A, B, S, N + 1, S, N, None) == ALIGN
+
+
+def test_select_wide_host_checks(lib):
+    f = lib.mt_select_wide
+    assert f(A, B, S, N, S, N, 3, None) == ARG
+    assert f(A, B, S, N, S, N, 16, None) == ARG
+    assert f(A, B, A, N, S, N, 8, None) == ALIAS
+    assert f(A + 4, B, S, N, S, N, 8, None) == ALIGN
+    assert f(A + 8, B, S, N, S, N, 8, None) == ALIGN  # 8-byte elements need 16-byte arr
+    assert f(A, B + 1, S, N, S, N, 8, None) == ALIGN  # ... and 16-byte flags
 
 
 def test_scratch_slots(lib):

@@ -1,0 +1,104 @@
+"""Parity of mt_select_wide (8-byte elements; CUDA, through the C ABI) with
+the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from golden_io import load_all
+
+pytestmark = pytest.mark.gpu
+
+SENT = -0x0BADBAD0BADBAD0  # sentinel 64-bit pattern
+
+
+@pytest.fixture(scope="module")
+def mt():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import prefix_scan_row_gb300 as m
+    return m
+
+
+def run_select64(mt, vals_cpu, flags_cpu, n, out_off=0):
+    cap = vals_cpu.numel()
+    arr = vals_cpu.cuda()
+    flags = flags_cpu.cuda()
+    obuf = torch.full((cap + out_off + 16,), SENT, dtype=torch.int64, device="cuda")
+    out = obuf[out_off:out_off + cap].view(vals_cpu.dtype)
+    num_out = torch.full((1,), -9, dtype=torch.int32, device="cuda")
+    scratch = mt.alloc_scratch(max(cap, 1), torch.int32, mt.MT_SCRATCH_SELECT)
+    scratch.fill_(-1)
+    n_dev = torch.tensor([n], dtype=torch.int32, device="cuda")
+    mt.mt_select_wide(arr, flags, out, num_out, scratch, n_dev)
+    torch.cuda.synchronize()
+    assert mt.mt_scan_status() == 0
+    k = int(num_out.item())
+    assert torch.all(obuf[out_off + k:] == SENT).item(), "tail of out was touched"
+    if out_off:
+        assert torch.all(obuf[:out_off] == SENT).item()
+    return out, k
+
+
+def check(out, k, vals_cpu, flags_cpu, n):
+    ref, kr = oracle.select_wide(vals_cpu, flags_cpu, n, 8)
+    assert k == kr, f"num_out {k} != {kr}"
+    got = out[:k].detach().cpu().contiguous().view(torch.int64).numpy().view(np.uint64)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches; first at {bad[0]}"
+
+
+def test_select_wide_golden(mt):
+    g = load_all()["algos_select_i32"]
+    vals = torch.tensor(g["arr"], dtype=torch.int64)
+    flags = torch.tensor(g["flags"], dtype=torch.uint8)
+    out, k = run_select64(mt, vals, flags, len(g["arr"]))
+    assert k == g["num_out"] and out[:k].cpu().tolist() == g["out"]
+
+
+@pytest.mark.parametrize("p", [0.0, 0.01, 0.5, 1.0])
+@pytest.mark.parametrize("n", [0, 1, 17, 8191, 8192, 8193, 100003, (1 << 20) + 3])
+def test_select_wide_sizes(mt, p, n):
+    cap = n + 29
+    vals = workloads.randint((cap,), n + 5, -(2**62), 2**62, "i64")
+    flags = workloads.bernoulli_u8(cap, p, n + 6)
+    out, k = run_select64(mt, vals, flags, n)
+    check(out, k, vals, flags, n)
+
+
+def test_select_wide_f64_bits_and_out_offset(mt):
+    """f64 elements move as bits (NaN payloads and -0 included); out may be
+    8-byte aligned only."""
+    n = 300001
+    bits = workloads.randint((n,), 61, -(2**62), 2**62, "i64")
+    bits[::7] = 0x7FF8DEADBEEF0001  # NaN payloads
+    bits[::11] = -(2**63)           # -0.0
+    vals = bits.view(torch.float64)
+    flags = workloads.bernoulli_u8(n, 0.4, 62)
+    out, k = run_select64(mt, vals, flags, n, out_off=1)
+    check(out, k, vals, flags, n)
+
+
+def test_select_wide_full_size(mt):
+    """2^26 8-byte elements at p = 0.5."""
+    n = 1 << 26
+    vals = workloads.randint((n,), 63, -(2**62), 2**62, "i64")
+    flags = workloads.bernoulli_u8(n, 0.5, 64)
+    out, k = run_select64(mt, vals, flags, n)
+    check(out, k, vals, flags, n)
+
+
+def test_select_wide_alignment_rules(mt):
+    n = 1000
+    base = torch.zeros(n + 4, dtype=torch.int64, device="cuda")
+    fl = torch.ones(n + 16, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(n, dtype=torch.int64, device="cuda")
+    num = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scr = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
+    nd = torch.tensor([n], dtype=torch.int32, device="cuda")
+    for arr, flags in ((base[1:n + 1], fl[:n]), (base[:n], fl[3:n + 3])):  # 8-aligned arr / odd flags
+        with pytest.raises(mt.ScanError) as ei:
+            mt.mt_select_wide(arr, flags, out, num, scr, nd)
+        assert ei.value.code == mt.MT_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert mt.mt_scan_status() == 0

@@ -62,6 +62,8 @@ MUTANTS = {
     "u32_signed_compare": ("            next = (x[i] < lp) ? x[i] : lp;\n        else\n            next = (x[i] > lp) ? x[i] : lp;\n        y[i] = inclusive ? next : lp;\n        lp = next;\n    }\n}\n\nstatic void scan_u64",
                            "            next = ((int32_t)x[i] < (int32_t)lp) ? x[i] : lp;\n        else\n            next = ((int32_t)x[i] > (int32_t)lp) ? x[i] : lp;\n        y[i] = inclusive ? next : lp;\n        lp = next;\n    }\n}\n\nstatic void scan_u64"),
     "u64_wrong_min_identity": ("    uint64_t lp = (op == OR_MIN) ? UINT64_MAX : 0u;", "    uint64_t lp = (op == OR_MIN) ? INT64_MAX : 0u;"),
+    "select_wide_half_copy": ("memcpy((char *)out + j * elem_bytes, (const char *)arr + i * elem_bytes, (size_t)elem_bytes);",
+                              "memcpy((char *)out + j * elem_bytes, (const char *)arr + i * elem_bytes, 4);"),
     "f64_add_wrong_sign": ("            const long double next = lp + (long double)x[i];",
                            "            const long double next = lp - (long double)x[i];"),
 }
