@@ -61,6 +61,8 @@ def lib():
         L.oracle_select.restype = i64
         L.oracle_select_wide.argtypes = [p, p, p, i64, i32]
         L.oracle_select_wide.restype = i64
+        L.oracle_reduce_by_key_add.argtypes = [p, p, p, p, p, p, i64, i32, i32]
+        L.oracle_reduce_by_key_add.restype = i64
         L.oracle_decode_half.argtypes = [p, p, i64, i32]
         L.oracle_decode_half.restype = None
         L.oracle_encode_half.argtypes = [p, p, i64, i32]
@@ -236,3 +238,26 @@ def ulp_array(v: np.ndarray, dtype: str) -> np.ndarray:
     _, e2 = np.frexp(a)
     E = np.where(a == 0.0, emin, np.maximum(e2 - 1, emin))
     return np.ldexp(1.0, (E - frac_bits).astype(np.int32))
+
+
+_RBK_NP = {I32: np.int32, U32: np.uint32, F32: np.float32}
+
+
+def reduce_by_key_add(keys, vals, n: int, key_dtype: str, val_dtype: str, want_f64: bool = False):
+    """Runs of consecutive equal keys -> (keys_out[0:r], values_out[0:r], r);
+    with ``want_f64`` for f32 values also each run's fp64 sum and sum of |v|."""
+    kd, vd = DTYPES[key_dtype], DTYPES[val_dtype]
+    k = np.ascontiguousarray(_np(keys)[:n])
+    v = np.ascontiguousarray(_np(vals)[:n])
+    ko = np.empty((max(n, 1),), dtype=_RBK_NP[kd])
+    vo = np.empty((max(n, 1),), dtype=_RBK_NP[vd])
+    s64 = np.empty((max(n, 1),), dtype=np.float64)
+    m64 = np.empty((max(n, 1),), dtype=np.float64)
+    r = lib().oracle_reduce_by_key_add(_ptr(k), _ptr(v), _ptr(ko), _ptr(vo), _ptr(s64), _ptr(m64), n,
+                                       kd, vd)
+    if r < 0:
+        raise ValueError("oracle_reduce_by_key_add rejected its arguments")
+    if want_f64:
+        return ko[:r].copy(), vo[:r].copy(), int(r), s64[:r].copy(), m64[:r].copy()
+    return ko[:r].copy(), vo[:r].copy(), int(r)
+

@@ -703,3 +703,69 @@ int64_t oracle_select_wide(const void *arr, const uint8_t *flags, void *out, int
     }
     return j;
 }
+
+/* ------------------------------------------------------------------------
+ * Reduce by key ([algos] qd.algorithms.reduce_by_key_add): every run of
+ * consecutive equal keys becomes one output entry (key, sum of the run's
+ * values), in input order; keys equal but separated by other keys form
+ * separate runs. Keys and values are i32, u32 or f32 (key_dtype, val_dtype:
+ * OR_I32, OR_U32 or OR_F32). Keys compare with == on their type: f32 NaN
+ * differs from everything (each NaN is a run of its own) and -0 equals +0.
+ * keys_out[r] is the key of the run's first element. Integer sums wrap
+ * modulo 2^32; f32 sums accumulate in fp64 and are rounded once; when
+ * non-null, sum64 / abs64 receive each run's fp64 sum and sum of |v|.
+ * Only the first num_runs entries of the outputs are written. Returns the
+ * number of runs, or -1 on a bad argument.
+ * ---------------------------------------------------------------------- */
+static int key_equal(const void *keys, int64_t i, int64_t j, int key_dtype)
+{
+    if (key_dtype == OR_F32) {
+        float a, b;
+        memcpy(&a, (const char *)keys + 4 * i, 4);
+        memcpy(&b, (const char *)keys + 4 * j, 4);
+        return a == b;
+    }
+    uint32_t a, b;
+    memcpy(&a, (const char *)keys + 4 * i, 4);
+    memcpy(&b, (const char *)keys + 4 * j, 4);
+    return a == b;
+}
+
+int64_t oracle_reduce_by_key_add(const void *keys, const void *vals, void *keys_out, void *vals_out,
+                                 double *sum64, double *abs64, int64_t n, int key_dtype, int val_dtype)
+{
+    if (n < 0 || (key_dtype != OR_I32 && key_dtype != OR_U32 && key_dtype != OR_F32) ||
+        (val_dtype != OR_I32 && val_dtype != OR_U32 && val_dtype != OR_F32))
+        return -1;
+    int64_t r = -1;            /* index of the current run */
+    uint32_t isum = 0;         /* integer sum of the current run (wraps) */
+    double fsum = 0.0, fabs_sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int head = (i == 0) || !key_equal(keys, i, i - 1, key_dtype);
+        if (head) {
+            ++r;
+            memcpy((char *)keys_out + 4 * r, (const char *)keys + 4 * i, 4);
+            isum = 0;
+            fsum = 0.0;
+            fabs_sum = 0.0;
+        }
+        if (val_dtype == OR_F32) {
+            float v;
+            memcpy(&v, (const char *)vals + 4 * i, 4);
+            fsum += (double)v;
+            fabs_sum += fabs((double)v);
+            const float f = (float)fsum;
+            memcpy((char *)vals_out + 4 * r, &f, 4);
+            if (sum64)
+                sum64[r] = fsum;
+            if (abs64)
+                abs64[r] = fabs_sum;
+        } else {
+            uint32_t v;
+            memcpy(&v, (const char *)vals + 4 * i, 4);
+            isum += v;
+            memcpy((char *)vals_out + 4 * r, &isum, 4);
+        }
+    }
+    return r + 1;
+}

@@ -708,4 +708,59 @@ def pin_select_wide():
         assert k == len(want) and out.tolist() == want
 
 
+# ---------------------------------------------------------------------------
+# Reduce by key
+# ---------------------------------------------------------------------------
+
+def pin_reduce_by_key_golden():
+    g = load_all()["algos_reduce_by_key_add_i32"]
+    for kd, vd in (("i32", "i32"), ("u32", "u32"), ("f32", "f32"), ("i32", "f32")):
+        keys = np.array(g["keys"], dtype={"i32": np.int32, "u32": np.uint32, "f32": np.float32}[kd])
+        vals = np.array(g["values"], dtype={"i32": np.int32, "u32": np.uint32, "f32": np.float32}[vd])
+        ko, vo, r = oracle.reduce_by_key_add(keys, vals, len(keys), kd, vd)
+        assert r == g["num_runs"] and ko.tolist() == g["keys_out"] and vo.tolist() == g["values_out"]
+
+
+def pin_reduce_by_key_brute_force():
+    """Runs found by an independent scan with itertools.groupby-style logic."""
+    rng = np.random.default_rng(67)
+    for n in (0, 1, 2, 9, 300, 5000):
+        keys = rng.integers(0, 4, n).astype(np.int32)  # small alphabet: long and short runs
+        vals = rng.integers(-1000, 1000, n).astype(np.int32)
+        ko, vo, r = oracle.reduce_by_key_add(keys, vals, n, "i32", "i32")
+        want_k, want_v = [], []
+        for i in range(n):
+            if i == 0 or keys[i] != keys[i - 1]:
+                want_k.append(int(keys[i]))
+                want_v.append(0)
+            want_v[-1] += int(vals[i])
+        assert r == len(want_k) and ko.tolist() == want_k and vo.tolist() == want_v, n
+        fv = (rng.integers(-4096, 4096, n) / 256.0).astype(np.float32)  # exact partial sums
+        ko, vo, r, s64, m64 = oracle.reduce_by_key_add(keys, fv, n, "i32", "f32", want_f64=True)
+        j = -1
+        sums, mags = [], []
+        for i in range(n):
+            if i == 0 or keys[i] != keys[i - 1]:
+                sums.append(Fraction(0))
+                mags.append(Fraction(0))
+            sums[-1] += Fraction(float(fv[i]))
+            mags[-1] += abs(Fraction(float(fv[i])))
+        assert [Fraction(float(x)) for x in vo] == sums and [Fraction(x) for x in s64] == sums
+        assert [Fraction(x) for x in m64] == mags
+
+
+def pin_reduce_by_key_float_keys_and_wrap():
+    nan = np.float32("nan")
+    keys = np.array([1.0, nan, nan, 0.0, -0.0, 2.0, 2.0, 1.0], dtype=np.float32)
+    vals = np.arange(1, 9, dtype=np.int32)
+    ko, vo, r = oracle.reduce_by_key_add(keys, vals, 8, "f32", "i32")
+    assert r == 6  # 1 | nan | nan | (0, -0) | (2, 2) | 1
+    assert vo.tolist() == [1, 2, 3, 4 + 5, 6 + 7, 8]
+    assert np.isnan(ko[1]) and np.isnan(ko[2]) and ko[3] == 0 and not np.signbit(ko[3])
+    u = np.array([7, 7, 7], dtype=np.uint32)
+    w = np.array([2**32 - 1, 2, 2**31], dtype=np.uint32)
+    _, vo, r = oracle.reduce_by_key_add(u, w, 3, "u32", "u32")
+    assert r == 1 and int(vo[0]) == (2**32 - 1 + 2 + 2**31) % 2**32
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

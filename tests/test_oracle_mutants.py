@@ -64,6 +64,10 @@ MUTANTS = {
     "u64_wrong_min_identity": ("    uint64_t lp = (op == OR_MIN) ? UINT64_MAX : 0u;", "    uint64_t lp = (op == OR_MIN) ? INT64_MAX : 0u;"),
     "select_wide_half_copy": ("memcpy((char *)out + j * elem_bytes, (const char *)arr + i * elem_bytes, (size_t)elem_bytes);",
                               "memcpy((char *)out + j * elem_bytes, (const char *)arr + i * elem_bytes, 4);"),
+    "rbk_key_compare_bits": ("        return a == b;\n    }\n    uint32_t a, b;", "        return memcmp(&a, &b, 4) == 0;\n    }\n    uint32_t a, b;"),
+    "rbk_sum_not_reset": ("            isum = 0;\n            fsum = 0.0;", "            fsum = 0.0;"),
+    "rbk_reset_every_element": ("        if (head) {\n            ++r;\n            memcpy((char *)keys_out + 4 * r, (const char *)keys + 4 * i, 4);",
+                           "        if (head)\n            ++r;\n        {\n            memcpy((char *)keys_out + 4 * r, (const char *)keys + 4 * i, 4);"),
     "f64_add_wrong_sign": ("            const long double next = lp + (long double)x[i];",
                            "            const long double next = lp - (long double)x[i];"),
 }
