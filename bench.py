@@ -545,6 +545,21 @@ def run_suite(args):
         timeit(f"select_wide f64 n={ns} p={p}", lambda: mt.mt_select_wide(v, f, o, num, scr, nd),
                9 * ns + 8 * k, ns)
         del v, f, o, scr
+    # reduce by key: i32 keys in runs of mean length 8, f32 values
+    nr = workloads.SELECT_N // args.scale
+    if wanted(f"reduce_by_key i32/f32 n={nr} mean_run=8"):
+        kk, vv = workloads.runs(nr, 8.0, workloads.SEED_SELECT + 7, "i32", "f32")
+        kk, vv = kk.to(dev), vv.to(dev)
+        ko, vo = torch.empty_like(kk), torch.empty_like(vv)
+        num = torch.zeros(1, dtype=torch.int32, device=dev)
+        scr = mt.alloc_scratch(nr, torch.int32, mt.MT_SCRATCH_REDUCE_BY_KEY, device=dev)
+        nrd = torch.tensor([nr], dtype=torch.int32, device=dev)
+        mt.mt_reduce_by_key_add(kk, vv, ko, vo, num, scr, nrd)
+        torch.cuda.synchronize()
+        runs_n = int(num.item())
+        timeit(f"reduce_by_key i32/f32 n={nr} mean_run=8",
+               lambda: mt.mt_reduce_by_key_add(kk, vv, ko, vo, num, scr, nrd), 8 * nr + 8 * runs_n, nr)
+        del kk, vv, ko, vo, scr
     if args.suite_out:
         with open(args.suite_out, "w") as fh:
             json.dump({"peak_gbs": peak, "peak_source": src, "rows": rows_out}, fh, indent=1)

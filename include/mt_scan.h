@@ -46,7 +46,8 @@ typedef enum { MT_ADD = 0, MT_MIN = 1, MT_MAX = 2, MT_MUL = 3 } mt_op;
 typedef enum {
     MT_SCRATCH_SCAN = 1,   /* for mt_exclusive_scan */
     MT_SCRATCH_SELECT = 2, /* for mt_select */
-    MT_SCRATCH_REDUCE = 3  /* for mt_reduce */
+    MT_SCRATCH_REDUCE = 3, /* for mt_reduce */
+    MT_SCRATCH_REDUCE_BY_KEY = 4 /* for mt_reduce_by_key_add */
 } mt_scratch_kind;
 
 typedef enum {
@@ -228,6 +229,35 @@ int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out
  */
 int mt_select_wide(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                    void *scratch, const int32_t *n_dev, int elem_bytes, void *stream);
+
+/*
+ * mt_reduce_by_key_add -- run-length sums ([algos]
+ * "qd.algorithms.reduce_by_key_add"): every run of consecutive equal keys in
+ * keys_in[0:n] becomes one entry, in input order: keys_out[r] = the run's key
+ * (that of its first element), values_out[r] = the sum of its values, and
+ * *num_runs = the number of runs. Keys equal but separated by other keys form
+ * separate runs.
+ *
+ * keys_in, values_in : device arrays of n elements; key_dtype and
+ *            value_dtype are MT_I32, MT_U32 or MT_F32. Float keys compare
+ *            with == (each NaN is a run of its own; -0 equals +0). Integer
+ *            sums wrap modulo 2^32; f32 sums are added in f32 in a fixed
+ *            order (not a left-to-right loop, so not bitwise that loop's).
+ *            Both 4-byte aligned and at the same address modulo 16 (they
+ *            are read as aligned 16-byte chunks together).
+ * keys_out, values_out : device arrays with room for n entries; only the
+ *            first *num_runs are written (the page's zero-initialisation of
+ *            all of values_out is not done: the tail is untouched).
+ * num_runs : device pointer to one int32 (0 for n <= 0).
+ * scratch  : mt_scan_scratch_slots(capacity, 0, MT_SCRATCH_REDUCE_BY_KEY)
+ *            8-byte slots, 16-byte aligned; no initialisation needed.
+ * n_dev    : device pointer to the int32 live count.
+ * Errors: MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS (an output is an input),
+ * MT_ERR_ALIGN, MT_ERR_MEMORY, MT_ERR_CUDA.
+ */
+int mt_reduce_by_key_add(const void *keys_in, const void *values_in, void *keys_out, void *values_out,
+                         int32_t *num_runs, void *scratch, const int32_t *n_dev, int key_dtype,
+                         int value_dtype, void *stream);
 
 /*
  * mt_scan_scratch_slots -- number of 8-byte scratch slots that

@@ -17,7 +17,10 @@ Names and arguments follow the C ABI:
 * ``mt_inclusive_scan(arr, out, scratch, n_dev, op)`` -- the inclusive form
   (in place allowed).
 * ``mt_reduce(arr, out, scratch, n_dev, op)`` -- out[0] = op(arr[0:n]).
-* ``mt_select(arr, flags, out, num_out, scratch, n_dev)`` -- stream compaction.
+* ``mt_select(arr, flags, out, num_out, scratch, n_dev)`` -- stream compaction
+  (``mt_select_wide`` for 8-byte elements).
+* ``mt_reduce_by_key_add(keys_in, values_in, keys_out, values_out, num_runs,
+  scratch, n_dev)`` -- run-length sums of consecutive equal keys.
 * ``mt_scan_scratch_slots(capacity, dtype, kind)`` -- scratch sizing.
 """
 from __future__ import annotations
@@ -32,7 +35,7 @@ LIB_PATH = os.path.join(_HERE, "libmtscan.so")
 
 MT_F32, MT_BF16, MT_F16, MT_I32, MT_I64, MT_U32, MT_U64, MT_F64 = 0, 1, 2, 3, 4, 5, 6, 7
 MT_ADD, MT_MIN, MT_MAX, MT_MUL = 0, 1, 2, 3
-MT_SCRATCH_SCAN, MT_SCRATCH_SELECT, MT_SCRATCH_REDUCE = 1, 2, 3
+MT_SCRATCH_SCAN, MT_SCRATCH_SELECT, MT_SCRATCH_REDUCE, MT_SCRATCH_REDUCE_BY_KEY = 1, 2, 3, 4
 MT_OK = 0
 MT_ERR_ARG, MT_ERR_DTYPE, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_LOOKBACK_TIMEOUT, MT_ERR_ALIGN = (
     -1, -2, -3, -4, -5, -6)
@@ -46,7 +49,7 @@ DTYPE_CODE = {torch.float32: MT_F32, torch.bfloat16: MT_BF16, torch.float16: MT_
 OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX, "mul": MT_MUL}
 
 EXPORTS = ("mt_scan_rows", "mt_scan_rows_op", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",
-           "mt_select_wide", "mt_scan_scratch_slots",
+           "mt_select_wide", "mt_reduce_by_key_add", "mt_scan_scratch_slots",
            "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback",
            "mt_scan_rows_noalloc")
 
@@ -77,6 +80,8 @@ def _load():
     L.mt_select.argtypes = [p, p, p, p, p, p, p]
     L.mt_select_wide.argtypes = [p, p, p, p, p, p, i32, p]
     L.mt_select_wide.restype = i32
+    L.mt_reduce_by_key_add.argtypes = [p, p, p, p, p, p, p, i32, i32, p]
+    L.mt_reduce_by_key_add.restype = i32
     L.mt_select.restype = i32
     L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
     L.mt_scan_scratch_slots.restype = i64
@@ -205,6 +210,20 @@ def mt_select_wide(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, nu
         raise ValueError("flags must be uint8, num_out and n_dev int32")
     _check(lib.mt_select_wide(_ptr(arr), _ptr(flags), _ptr(out), _ptr(num_out), _ptr(scratch),
                               _ptr(n_dev), eb, _stream(stream)), "mt_select_wide")
+
+
+def mt_reduce_by_key_add(keys_in: torch.Tensor, values_in: torch.Tensor, keys_out: torch.Tensor,
+                         values_out: torch.Tensor, num_runs: torch.Tensor, scratch: torch.Tensor,
+                         n_dev: torch.Tensor, stream=None) -> None:
+    """Runs of consecutive equal keys -> (key, sum of values); i32/u32/f32."""
+    if keys_out.dtype != keys_in.dtype or values_out.dtype != values_in.dtype:
+        raise ValueError("outputs must have their inputs' dtypes")
+    if num_runs.dtype != torch.int32 or n_dev.dtype != torch.int32:
+        raise ValueError("num_runs and n_dev must be int32")
+    _check(lib.mt_reduce_by_key_add(_ptr(keys_in), _ptr(values_in), _ptr(keys_out), _ptr(values_out),
+                                    _ptr(num_runs), _ptr(scratch), _ptr(n_dev),
+                                    DTYPE_CODE.get(keys_in.dtype, -99), DTYPE_CODE.get(values_in.dtype, -99),
+                                    _stream(stream)), "mt_reduce_by_key_add")
 
 
 def mt_scan_scratch_slots(capacity: int, dtype, kind: int) -> int:

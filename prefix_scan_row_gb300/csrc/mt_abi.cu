@@ -332,6 +332,37 @@ extern "C" int mt_select_wide(const void *arr, const uint8_t *flags, void *out, 
     return select_call(arr, flags, out, num_out, scratch, n_dev, elem_bytes, stream);
 }
 
+extern "C" int mt_reduce_by_key_add(const void *keys_in, const void *values_in, void *keys_out,
+                                    void *values_out, int32_t *num_runs, void *scratch,
+                                    const int32_t *n_dev, int key_dtype, int value_dtype, void *stream) {
+    const auto ok_dtype = [](int d) { return d == MT_I32 || d == MT_U32 || d == MT_F32; };
+    if (!ok_dtype(key_dtype) || !ok_dtype(value_dtype))
+        return MT_ERR_DTYPE;
+    if (keys_in == nullptr || values_in == nullptr || keys_out == nullptr || values_out == nullptr ||
+        num_runs == nullptr || scratch == nullptr || n_dev == nullptr)
+        return MT_ERR_ARG;
+    if (keys_out == keys_in || keys_out == values_in || values_out == keys_in || values_out == values_in)
+        return MT_ERR_ALIAS;
+    const uintptr_t k = (uintptr_t)keys_in, v = (uintptr_t)values_in;
+    if (k % 4 || v % 4 || (uintptr_t)keys_out % 4 || (uintptr_t)values_out % 4 || (uintptr_t)num_runs % 4 ||
+        (uintptr_t)scratch % 16 || (uintptr_t)n_dev % 4 || (k % 16) != (v % 16))
+        return MT_ERR_ALIGN;  // keys and values are read as aligned 16-byte chunks of the same phase
+    Launch L;
+    int dev = 0;
+    if (!make_launch(stream, &L, &dev))
+        return MT_ERR_CUDA;
+    if (!all_device({keys_in, values_in, keys_out, values_out, num_runs, scratch, n_dev}, dev))
+        return MT_ERR_MEMORY;
+    uint64_t *sw = static_cast<uint64_t *>(scratch);
+    if (launch_reset(sw, 0, n_dev, rbk_tile_elems(), 4, (int)(k & 15u), rbk_rec_slots(), num_runs, L) !=
+        cudaSuccess)
+        return MT_ERR_CUDA;
+    return rbk_launch(keys_in, values_in, keys_out, values_out, num_runs, sw, n_dev, key_dtype == MT_F32,
+                      value_dtype == MT_F32, L) == cudaSuccess
+               ? MT_OK
+               : MT_ERR_CUDA;
+}
+
 extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) {
     if (capacity < 0)
         return -1;
@@ -347,6 +378,11 @@ extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) 
         const int64_t te = select_tile_elems();
         return kHeaderSlots + (capacity + te - 1) / te * select_rec_slots();
     }
+    if (kind == MT_SCRATCH_REDUCE_BY_KEY) {
+        const int64_t te = rbk_tile_elems();
+        const int64_t ntiles = capacity > 0 ? (capacity + 3 + te - 1) / te : 0;  // up to 3 elements of head
+        return kHeaderSlots + ntiles * rbk_rec_slots();
+    }
     if (kind == MT_SCRATCH_REDUCE)
         return elem_size(dtype) > 0 && dtype != MT_BF16 && dtype != MT_F16 ? reduce_scratch_slots() : -1;
     return -1;
@@ -356,8 +392,9 @@ extern "C" int mt_scan_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MT_ERR_CUDA;
     int worst = MT_OK;
-    cudaError_t (*takers[6])(int *) = {rows_take_error, rows_minmax_take_error, rows_mul_take_error,
-                                       scan1d_take_error, scan1d_ext_take_error, select_take_error};
+    cudaError_t (*takers[7])(int *) = {rows_take_error,   rows_minmax_take_error, rows_mul_take_error,
+                                       scan1d_take_error, scan1d_ext_take_error,  select_take_error,
+                                       rbk_take_error};
     for (auto take : takers) {
         int code = 0;
         if (take(&code) != cudaSuccess)

@@ -94,6 +94,14 @@ int64_t reduce_scratch_slots();  // fixed: header + one partial per CTA
 cudaError_t reduce_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
                           int dtype, int op, const Launch &L);
 
+// ---- reduce by key (mt_rbk.cu) ---------------------------------------------
+int64_t rbk_tile_elems();
+int rbk_rec_slots();
+cudaError_t rbk_launch(const void *keys, const void *vals, void *keys_out, void *vals_out, int32_t *num_runs,
+                       uint64_t *scratch, const int32_t *n_dev, bool key_float, bool val_float,
+                       const Launch &L);
+cudaError_t rbk_take_error(int *code);
+
 // ---- select (mt_select.cu) ------------------------------------------------
 int64_t select_tile_elems();
 int select_rec_slots();

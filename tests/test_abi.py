@@ -28,6 +28,7 @@ def lib():
     L.mt_reduce.argtypes = [p, p, p, p, i32, i32, p]
     L.mt_select.argtypes = [p, p, p, p, p, p, p]
     L.mt_select_wide.argtypes = [p, p, p, p, p, p, i32, p]
+    L.mt_reduce_by_key_add.argtypes = [p, p, p, p, p, p, p, i32, i32, p]
     L.mt_scan_scratch_slots.argtypes = [i64, i32, i32]
     L.mt_scan_scratch_slots.restype = i64
     L.mt_scan_strerror.argtypes = [i32]
@@ -130,6 +131,18 @@ def test_select_wide_host_checks(lib):
     assert f(A, B + 1, S, N, S, N, 8, None) == ALIGN  # ... and 16-byte flags
 
 
+def test_reduce_by_key_host_checks(lib):
+    f = lib.mt_reduce_by_key_add
+    C, D = 0x50000, 0x60000
+    assert f(A, B, C, D, N, S, N, I64, I32, None) == DTYPE
+    assert f(A, B, C, D, N, S, N, I32, BF16, None) == DTYPE
+    assert f(None, B, C, D, N, S, N, I32, I32, None) == ARG
+    assert f(A, B, A, D, N, S, N, I32, I32, None) == ALIAS
+    assert f(A, B, C, B, N, S, N, I32, I32, None) == ALIAS
+    assert f(A + 4, B, C, D, N, S, N, I32, I32, None) == ALIGN  # keys and values out of phase
+    assert f(A + 2, B + 2, C, D, N, S, N, I32, I32, None) == ALIGN
+
+
 def test_scratch_slots(lib):
     f = lib.mt_scan_scratch_slots
     assert f(0, I32, 1) == 4
@@ -152,6 +165,8 @@ def test_scratch_slots(lib):
     # reduce: a header and one partial slot per CTA, whatever the capacity
     assert f(1 << 28, I32, 3) == f(0, F32, 3) == f(5, I64, 3) == f(7, 7, 3) == 4 + 2 * 4096
     assert f(10, BF16, 3) == -1
+    # reduce by key: 4096 elements per tile (plus up to 3 of head phase)
+    assert f(4093, 0, 4) == 4 + 16 and f(4094, 0, 4) == 4 + 32 and f(0, 0, 4) == 4
 
 
 def test_strerror_and_counter(lib):

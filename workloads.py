@@ -150,6 +150,31 @@ def scan1d(dtype: str, capacity: int = SCAN1D_CAPACITY, seed: int = SEED_SCAN1D)
     raise ValueError(dtype)
 
 
+def runs(n: int, mean_run: float, seed: int, key_dtype: str = "i32", val_dtype: str = "f32"):
+    """(keys [n], values [n]) for reduce-by-key: run lengths geometric with
+    the given mean, each run's key drawn from a small alphabet (so equal keys
+    also recur in separate runs), values uniform[-1, 1) (f32) or integers in
+    [-1000, 1000) (i32 / u32)."""
+    g = generator(seed)
+    starts = torch.rand((n,), generator=g) < (1.0 / mean_run)
+    if n:
+        starts[0] = True
+    run_id = torch.cumsum(starts.to(torch.int64), 0) - 1
+    alphabet = torch.randint(0, 64, (int(run_id[-1].item()) + 1 if n else 1,), generator=g,
+                             dtype=torch.int64)
+    k = alphabet[run_id] if n else torch.zeros((0,), dtype=torch.int64)
+    keys = k.to(torch.float32) if key_dtype == "f32" else k.to(torch.int32)
+    if key_dtype == "u32":
+        keys = keys.view(torch.uint32)
+    if val_dtype == "f32":
+        vals = torch.rand((n,), generator=g, dtype=torch.float32).mul_(2.0).sub_(1.0)
+    else:
+        vals = torch.randint(-1000, 1000, (n,), generator=g, dtype=torch.int32)
+        if val_dtype == "u32":
+            vals = vals.view(torch.uint32)
+    return keys, vals
+
+
 def select_inputs(n: int = SELECT_N, p: float = 0.5, seed: int = SEED_SELECT):
     """(values f32 [n], flags u8 [n]); the flags use seed + 1 so p does not
     change the values."""
