@@ -14,18 +14,24 @@
 // run -- and the tile scans pairs with the segmented operator
 //   (c1, s1) + (c2, s2) = (c1 + c2, c2 != 0 ? s2 : s1 + s2),
 // whose inclusive prefix at an element is (runs started so far, sum of the
-// open run). Tiles are chained by the decoupled look-back on that pair
-// (packed in 64 bits), so every run's sum is complete at its last element:
-// heads write keys_out[c - 1], run ends write values_out[c - 1]. No atomics
-// on the outputs, and sums are added in a fixed order.
+// open run). Super-tiles of 8192 keys and values arrive in shared memory by
+// bulk copies; a first pass finds the super-tile's own pair (its head count,
+// its last head, the sum of the values from there on) and publishes it at
+// once; warp 0 then looks back for the pairs of all earlier super-tiles
+// (packed in 64 bits), and the scan writes final results: heads
+// keys_out[c - 1], run ends values_out[c - 1]. No atomics on the outputs,
+// and sums are added in a fixed order.
+#include <type_traits>
+
 #include "mt_lookback.cuh"
 
 namespace mt {
 
 constexpr int kRbkThreads = 256;
-constexpr int kRbkItems = 4;                                       // 16-byte chunks per thread
-constexpr int kRbkChunks = kRbkThreads * kRbkItems;                // per tile
-constexpr int64_t kRbkTE = (int64_t)kRbkChunks * 4;                // elements per tile (4096)
+constexpr int kRbkItems = 2;                                      // 16-byte chunks per thread per sub-tile
+constexpr int kRbkSub = 4;                                        // sub-tiles per super-tile
+constexpr int kRbkChunks = kRbkSub * kRbkThreads * kRbkItems;     // chunks per super-tile
+constexpr int64_t kRbkTE = (int64_t)kRbkChunks * 4;               // elements per super-tile (8192)
 
 struct RbkArgs {
     const char *keys;   // keys and values share their 16-byte phase
@@ -57,6 +63,38 @@ struct SegOp {
     }
 };
 
+// The same pair unpacked, for the scan inside a tile: c counts heads, s is
+// an f32 (VF) or a wrapping u32 sum.
+template <bool VF>
+struct Seg {
+    using V = typename std::conditional<VF, float, uint32_t>::type;
+    uint32_t c;
+    V s;
+    __device__ __forceinline__ static Seg ident() { return Seg{0u, V(0)}; }
+    __device__ __forceinline__ static Seg apply(const Seg &a, const Seg &b) {
+        return Seg{a.c + b.c, b.c != 0u ? b.s : a.s + b.s};
+    }
+    __device__ __forceinline__ static V val(uint32_t bits) {
+        if constexpr (VF)
+            return __uint_as_float(bits);
+        else
+            return bits;
+    }
+    __device__ __forceinline__ static uint32_t bits(V v) {
+        if constexpr (VF)
+            return __float_as_uint(v);
+        else
+            return v;
+    }
+    __device__ __forceinline__ static Seg unpack(uint64_t p) { return Seg{(uint32_t)(p >> 32), val((uint32_t)p)}; }
+    __device__ __forceinline__ Seg shfl_up(int d) const {
+        return Seg{__shfl_up_sync(kFull, c, d), __shfl_up_sync(kFull, s, d)};
+    }
+    __device__ __forceinline__ Seg shfl(int l) const {
+        return Seg{__shfl_sync(kFull, c, l), __shfl_sync(kFull, s, l)};
+    }
+};
+
 template <bool KF>
 __device__ __forceinline__ bool keys_differ(uint32_t a, uint32_t b) {
     if (KF)
@@ -68,15 +106,33 @@ __device__ __forceinline__ uint32_t word(const uint4 &v, int k) {
     return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
+// Shared state of one CTA: the super-tile's keys and values (bulk-copied),
+// the keys just before and after it, and the block's scratch.
+struct RbkSmem {
+    uint4 keys[kRbkChunks];
+    uint4 vals[kRbkChunks];
+    uint64_t bar;
+    unsigned long long tile;
+    uint32_t kprev, knext;     // the neighbours' keys (when they exist)
+    uint8_t heads[kRbkChunks]; // 4 head bits per chunk (bit k: element 4c + k starts a run)
+    uint32_t red_c[kRbkThreads / 32];
+    int32_t red_l[kRbkThreads / 32];
+    uint32_t red_s[kRbkThreads / 32];
+    uint32_t warp_c[2][kRbkThreads / 32];  // warp totals of a sub-tile scan
+    uint32_t warp_s[2][kRbkThreads / 32];
+    uint64_t prefix;
+};
+
 template <bool KF, bool VF>
 __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
     pdl_prologue();
     using Op = SegOp<VF>;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kNW = kRbkThreads / 32;
-    __shared__ uint64_t warp_tot[2][kNW];
-    __shared__ uint64_t prefix[2];
-    __shared__ unsigned long long tile_id;
+    constexpr int kSubChunks = kRbkThreads * kRbkItems;  // chunks per sub-tile
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    RbkSmem &sm = *reinterpret_cast<RbkSmem *>(dsm);
+    const uint32_t *skey = reinterpret_cast<const uint32_t *>(sm.keys);
 
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
@@ -87,121 +143,219 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
     const int64_t lo = head, hi = head + n;
     const int64_t ntiles = n > 0 ? (hi + kRbkTE - 1) / kRbkTE : 0;
 
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    uint32_t phase = 0;
     for (int64_t it = 0;; ++it) {
         if (threadIdx.x == 0)
-            tile_id = atomicAdd(a.counter, 1ull);
-        __syncthreads();  // tile id visible; every thread is done with the last tile's shared state
-        const int64_t g = (int64_t)tile_id;
+            sm.tile = atomicAdd(a.counter, 1ull);
+        __syncthreads();  // tile id visible; every thread is done with the last super-tile
+        const int64_t g = (int64_t)sm.tile;
         if (g >= ntiles)
             break;
-        const int buf = (int)(it & 1);
         const int64_t t0 = g * kRbkTE;
-
-        // Loads: keys and values of this thread's chunks, and for each chunk
-        // the key before it and the key after it (neighbours' chunks: L1/L2).
-        uint4 kr[kRbkItems], vr[kRbkItems];
-        uint32_t kprev[kRbkItems], knext[kRbkItems];
-#pragma unroll
-        for (int j = 0; j < kRbkItems; ++j) {
-            const int c = warp * 32 * kRbkItems + j * 32 + lane;
-            const int64_t v0 = t0 + (int64_t)c * 4;
-            kr[j] = vr[j] = make_uint4(0u, 0u, 0u, 0u);
-            kprev[j] = knext[j] = 0u;
-            if (v0 < hi && v0 + 4 > lo) {
-                kr[j] = ld_stream(vk + v0 / 4);
-                vr[j] = ld_stream(vv + v0 / 4);
-            }
-            if (v0 - 1 >= lo && v0 - 1 < hi)
-                kprev[j] = __ldg(ek + v0 - 1);
-            if (v0 + 4 >= lo && v0 + 4 < hi)
-                knext[j] = __ldg(ek + v0 + 4);
+        // in-tile valid range [llo, lhi) of virtual elements
+        const int llo = lo > t0 ? (int)(lo - t0) : 0;
+        const int lhi = hi - t0 < kRbkTE ? (int)(hi - t0) : (int)kRbkTE;
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();  // the last iteration's shared accesses come first
+            const int64_t c0 = t0 / 4;
+            int64_t cend = (hi + 3) / 4;
+            if (cend > c0 + kRbkChunks)
+                cend = c0 + kRbkChunks;
+            const uint32_t bytes = (uint32_t)((cend - c0) * 16);
+            mbar_arrive_expect_tx(&sm.bar, 2 * bytes);
+            bulk_g2s(&sm.keys[0], vk + c0, bytes, &sm.bar);
+            bulk_g2s(&sm.vals[0], vv + c0, bytes, &sm.bar);
+            sm.kprev = (t0 + llo - 1 >= lo) ? __ldg(ek + t0 + llo - 1) : 0u;
+            sm.knext = (t0 + lhi < hi) ? __ldg(ek + t0 + lhi) : 0u;
         }
+        bool ok = true;
+        if (threadIdx.x < 32)
+            ok = mbar_wait(&sm.bar, phase, kCopyWaitLimit);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) {
+                atomicCAS(&g_mt_err, 0, kErrTimeout);
+                mbar_wait(&sm.bar, phase, kCopyWaitLimit);  // drain the copies before leaving
+            }
+            return;
+        }
+        phase ^= 1u;
+        const uint32_t kprev = sm.kprev, knext = sm.knext;
 
-        // Per element: the pair (head, value); serial inclusive scan per chunk.
-        uint64_t x[kRbkItems][4];
-        bool endf[kRbkItems][4], headf[kRbkItems][4];
-#pragma unroll
-        for (int j = 0; j < kRbkItems; ++j) {
-            const int c = warp * 32 * kRbkItems + j * 32 + lane;
-            const int64_t v0 = t0 + (int64_t)c * 4;
+        // Pass 0: the super-tile's pair (heads, sum of the run open at its
+        // end), published before the scan. Head bits, their count and the
+        // last head first (one 16-byte read of keys per chunk) ...
+        uint32_t cnt = 0u;
+        int last = -1;
+        for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
+            const uint4 kk = lds128(&sm.keys[c]);
+            uint32_t before = (4 * c - 1 >= llo) ? skey[4 * c - 1] : kprev;
+            uint32_t m = 0u;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int64_t v = v0 + k;
-                const bool valid = v >= lo && v < hi;
-                const uint32_t key = word(kr[j], k);
-                const uint32_t before = k == 0 ? kprev[j] : word(kr[j], k - 1);
-                const uint32_t after = k == 3 ? knext[j] : word(kr[j], k + 1);
-                const bool h = valid && (v == lo || keys_differ<KF>(key, before));
-                headf[j][k] = h;
-                endf[j][k] = valid && (v == hi - 1 || keys_differ<KF>(after, key));
-                // invalid elements are the identity (0, 0)
-                x[j][k] = valid ? (((uint64_t)(h ? 1u : 0u) << 32) | word(vr[j], k)) : 0ull;
+                const int i = 4 * c + k;
+                const uint32_t key = word(kk, k);
+                const bool h = i >= llo && i < lhi && (t0 + i == lo || keys_differ<KF>(key, before));
+                m |= (h ? 1u : 0u) << k;
+                before = key;
             }
-#pragma unroll
-            for (int k = 1; k < 4; ++k)
-                x[j][k] = Op::apply(x[j][k - 1], x[j][k]);
-        }
-
-        // Warp scans of the chunk totals (one per j), then the run over j.
-        uint64_t inc[kRbkItems];
-#pragma unroll
-        for (int j = 0; j < kRbkItems; ++j)
-            inc[j] = x[j][3];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-#pragma unroll
-            for (int j = 0; j < kRbkItems; ++j) {
-                const uint64_t y = __shfl_up_sync(kFull, inc[j], d);
-                if (lane >= d)
-                    inc[j] = Op::apply(y, inc[j]);
+            sm.heads[c] = (uint8_t)m;
+            if (m) {
+                cnt += __popc(m);
+                last = 4 * c + 31 - __clz(m);
             }
         }
-        uint64_t pre[kRbkItems];
-        uint64_t run = 0ull;
 #pragma unroll
-        for (int j = 0; j < kRbkItems; ++j) {
-            uint64_t e = __shfl_up_sync(kFull, inc[j], 1);
-            if (lane == 0)
-                e = 0ull;
-            pre[j] = Op::apply(run, e);
-            run = Op::apply(run, __shfl_sync(kFull, inc[j], 31));
+        for (int d = 16; d > 0; d >>= 1) {
+            cnt += __shfl_xor_sync(kFull, cnt, d);
+            last = max(last, __shfl_xor_sync(kFull, last, d));
         }
-        if (lane == 0)
-            warp_tot[buf][warp] = run;
-        __syncthreads();
-        uint64_t wpre = 0ull, agg = 0ull;
+        if (lane == 0) {
+            sm.red_c[warp] = cnt;
+            sm.red_l[warp] = last;
+        }
+        __syncthreads();  // also: every head mask is written
+        uint32_t tc = 0u;
+        int tl = -1;
 #pragma unroll
         for (int w = 0; w < kNW; ++w) {
-            const uint64_t t = warp_tot[buf][w];
-            if (w < warp)
-                wpre = Op::apply(wpre, t);
-            agg = Op::apply(agg, t);
+            tc += sm.red_c[w];
+            tl = max(tl, sm.red_l[w]);
         }
-
-        // The tile's prefix: (runs started before it, sum of the run open at
-        // its start); the first tile's is the identity.
-        const uint64_t tp = tile_prefix<uint64_t, Op>(a.lb, g, 0, agg, &prefix[buf]);
-        const uint64_t base0 = Op::apply(tp, wpre);
-
-        // Heads write their key, run ends the run's sum, at run index c - 1.
-#pragma unroll
-        for (int j = 0; j < kRbkItems; ++j) {
-            const uint64_t base = Op::apply(base0, pre[j]);
-            const int c = warp * 32 * kRbkItems + j * 32 + lane;
-            const int64_t v0 = t0 + (int64_t)c * 4;
+        // ... then the values from the last head (or the tile start) on.
+        const int from = tl >= 0 ? tl : llo;
+        uint32_t ssum = 0u;  // bits of the partial sum
+        for (int c = from / 4 + threadIdx.x; c < (lhi + 3) / 4; c += kRbkThreads) {
+            const uint4 vv4 = lds128(&sm.vals[c]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint64_t p = Op::apply(base, x[j][k]);
-                const uint32_t r = (uint32_t)(p >> 32) - 1u;
-                if (headf[j][k])
-                    a.keys_out[r] = word(kr[j], k);
-                if (endf[j][k]) {
-                    a.vals_out[r] = (uint32_t)p;
-                    if (v0 + k == hi - 1)
-                        *a.num_runs = (int32_t)(r + 1u);
+                const int i = 4 * c + k;
+                if (i >= from && i < lhi) {
+                    const uint32_t v = word(vv4, k);
+                    ssum = VF ? __float_as_uint(__uint_as_float(ssum) + __uint_as_float(v)) : ssum + v;
                 }
             }
         }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const uint32_t o = __shfl_xor_sync(kFull, ssum, d);
+            ssum = VF ? __float_as_uint(__uint_as_float(ssum) + __uint_as_float(o)) : ssum + o;
+        }
+        if (lane == 0)
+            sm.red_s[warp] = ssum;
+        __syncthreads();
+        uint32_t ts = 0u;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w)
+            ts = VF ? __float_as_uint(__uint_as_float(ts) + __uint_as_float(sm.red_s[w])) : ts + sm.red_s[w];
+        const uint64_t agg = ((uint64_t)tc << 32) | ts;
+        publish_aggregate<uint64_t, Op>(a.lb, g, 0, agg);
+
+        // Does the super-tile's last element end its run?
+        const bool last_ends = lhi > llo && (t0 + lhi == hi || keys_differ<KF>(knext, skey[lhi - 1]));
+
+        // The prefix of the super-tile, looked back for before the scan: the
+        // scan below then writes final results.
+        using P = Seg<VF>;
+        P carry = P::unpack(lookback_prefix<uint64_t, Op>(a.lb, g, 0, agg, &sm.prefix));
+
+        // Pass 1: sub-tiles in order, chunk j*32 + lane of each warp's run.
+#pragma unroll 1
+        for (int sub = 0; sub < kRbkSub; ++sub) {
+            P x[kRbkItems][4];
+            uint32_t hm[kRbkItems], em[kRbkItems];  // head and run-end bits per chunk
+#pragma unroll
+            for (int j = 0; j < kRbkItems; ++j) {
+                const int c = sub * kSubChunks + warp * 32 * kRbkItems + j * 32 + lane;
+                const uint4 vv4 = lds128(&sm.vals[c]);
+                const uint32_t m = sm.heads[c];
+                const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : 0u;
+                // element i ends a run when i + 1 starts one, or it is the last
+                uint32_t e = (m >> 1) | ((mn & 1u) << 3);
+                const int li = lhi - 1 - 4 * c;  // the last valid element, if in this chunk
+                if (li >= 0 && li < 4)
+                    e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
+                else if (li < 0)
+                    e = 0u;
+                uint32_t vm = 0u;  // valid elements of the chunk
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = 4 * c + k;
+                    const bool valid = i >= llo && i < lhi;
+                    vm |= (valid ? 1u : 0u) << k;
+                    x[j][k] = P{(m >> k) & 1u, valid ? P::val(word(vv4, k)) : typename P::V(0)};
+                }
+                hm[j] = m;       // heads are valid elements by construction
+                em[j] = e & vm;  // no end for an element outside the array
+#pragma unroll
+                for (int k = 1; k < 4; ++k)
+                    x[j][k] = P::apply(x[j][k - 1], x[j][k]);
+            }
+            P inc[kRbkItems];
+#pragma unroll
+            for (int j = 0; j < kRbkItems; ++j)
+                inc[j] = x[j][3];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+                for (int j = 0; j < kRbkItems; ++j) {
+                    const P y = inc[j].shfl_up(d);
+                    if (lane >= d)
+                        inc[j] = P::apply(y, inc[j]);
+                }
+            }
+            P pre[kRbkItems];
+            P run = P::ident();
+#pragma unroll
+            for (int j = 0; j < kRbkItems; ++j) {
+                P e = inc[j].shfl_up(1);
+                if (lane == 0)
+                    e = P::ident();
+                pre[j] = P::apply(run, e);
+                run = P::apply(run, inc[j].shfl(31));
+            }
+            if (lane == 0) {
+                sm.warp_c[sub & 1][warp] = run.c;
+                sm.warp_s[sub & 1][warp] = P::bits(run.s);
+            }
+            __syncthreads();
+            P wpre = P::ident(), tot = P::ident();
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+                const P t{sm.warp_c[sub & 1][w], P::val(sm.warp_s[sub & 1][w])};
+                if (w < warp)
+                    wpre = P::apply(wpre, t);
+                tot = P::apply(tot, t);
+            }
+            const P base0 = P::apply(carry, wpre);
+            // heads write their key, run ends the run's sum, at run index c - 1
+#pragma unroll
+            for (int j = 0; j < kRbkItems; ++j) {
+                if ((hm[j] | em[j]) == 0u)
+                    continue;
+                const P base = P::apply(base0, pre[j]);
+                const int c = sub * kSubChunks + warp * 32 * kRbkItems + j * 32 + lane;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (((hm[j] | em[j]) >> k) & 1u) {
+                        const P p = P::apply(base, x[j][k]);
+                        const uint32_t r = p.c - 1u;
+                        if ((hm[j] >> k) & 1u)
+                            a.keys_out[r] = skey[4 * c + k];
+                        if ((em[j] >> k) & 1u) {
+                            a.vals_out[r] = P::bits(p.s);
+                            if (t0 + 4 * c + k == hi - 1)
+                                *a.num_runs = (int32_t)(r + 1u);
+                        }
+                    }
+                }
+            }
+            carry = P::apply(carry, tot);
+        }
+        fence_proxy_async_smem();  // this thread's shared accesses precede the next bulk copies
     }
 }
 
@@ -214,14 +368,23 @@ static cudaError_t launch_rbk(const RbkArgs &a, const Launch &L) {
         return e;
     if (dev < 0 || dev >= 128)
         return cudaErrorInvalidDevice;
+    const int bytes = (int)sizeof(RbkSmem);
     if (per_sm[dev] == 0) {
+        e = cudaFuncSetAttribute(k_reduce_by_key<KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaFuncSetAttribute(k_reduce_by_key<KF, VF>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
         int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_reduce_by_key<KF, VF>, kRbkThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_reduce_by_key<KF, VF>, kRbkThreads, bytes);
         if (e != cudaSuccess)
             return e;
         per_sm[dev] = b > 0 ? b : 1;
     }
-    e = launch_pdl(k_reduce_by_key<KF, VF>, (unsigned)(L.sm_count * per_sm[dev]), kRbkThreads, 0, L.stream, a);
+    e = launch_pdl(k_reduce_by_key<KF, VF>, (unsigned)(L.sm_count * per_sm[dev]), kRbkThreads, bytes,
+                   L.stream, a);
     note_launch();
     return e;
 }
