@@ -15,12 +15,13 @@
 //   (c1, s1) + (c2, s2) = (c1 + c2, c2 != 0 ? s2 : s1 + s2),
 // whose inclusive prefix at an element is (runs started so far, sum of the
 // open run). Super-tiles of 8192 keys and values arrive in shared memory by
-// bulk copies; a first pass finds the super-tile's own pair (its head count,
-// its last head, the sum of the values from there on) and publishes it at
-// once; warp 0 then looks back for the pairs of all earlier super-tiles
-// (packed in 64 bits), and the scan writes final results: heads
-// keys_out[c - 1], run ends values_out[c - 1]. No atomics on the outputs,
-// and sums are added in a fixed order.
+// bulk copies. Each thread folds segments of 16 consecutive elements serially
+// (head bits kept as a mask), so only one pair per thread and segment enters
+// the warp and block scans; the super-tile's own pair is published as soon as
+// that scan is done; warp 0 then looks back for the pairs of all earlier
+// super-tiles (packed in 64 bits), and a second pass over each segment writes
+// the results: heads keys_out[c - 1], run ends values_out[c - 1]. No atomics
+// on the outputs, and sums are added in a fixed order.
 #include <type_traits>
 
 #include "mt_lookback.cuh"
@@ -28,10 +29,11 @@
 namespace mt {
 
 constexpr int kRbkThreads = 256;
-constexpr int kRbkItems = 2;                                      // 16-byte chunks per thread per sub-tile
-constexpr int kRbkSub = 4;                                        // sub-tiles per super-tile
-constexpr int kRbkChunks = kRbkSub * kRbkThreads * kRbkItems;     // chunks per super-tile
-constexpr int64_t kRbkTE = (int64_t)kRbkChunks * 4;               // elements per super-tile (8192)
+constexpr int kRbkSeg = 16;                                       // consecutive elements per thread segment
+constexpr int kRbkSub = 8192 / (256 * kRbkSeg);                   // segments per thread per super-tile
+constexpr int kRbkSubElems = kRbkThreads * kRbkSeg;               // elements per sub-tile (4096)
+constexpr int64_t kRbkTE = (int64_t)kRbkSub * kRbkSubElems;       // elements per super-tile (8192)
+constexpr int kRbkChunks = (int)(kRbkTE / 4);                     // 16-byte chunks per super-tile
 
 struct RbkArgs {
     const char *keys;   // keys and values share their 16-byte phase
@@ -114,12 +116,9 @@ struct RbkSmem {
     uint64_t bar;
     unsigned long long tile;
     uint32_t kprev, knext;     // the neighbours' keys (when they exist)
-    uint8_t heads[kRbkChunks]; // 4 head bits per chunk (bit k: element 4c + k starts a run)
-    uint32_t red_c[kRbkThreads / 32];
-    int32_t red_l[kRbkThreads / 32];
-    uint32_t red_s[kRbkThreads / 32];
-    uint32_t warp_c[2][kRbkThreads / 32];  // warp totals of a sub-tile scan
-    uint32_t warp_s[2][kRbkThreads / 32];
+    uint32_t heads[kRbkSub][kRbkThreads];   // head bits of each segment (bit k: its element k)
+    uint32_t warp_c[kRbkSub][kRbkThreads / 32];  // warp totals of the segment scan
+    uint32_t warp_s[kRbkSub][kRbkThreads / 32];
     uint64_t prefix;
 };
 
@@ -128,7 +127,6 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
     pdl_prologue();
     using Op = SegOp<VF>;
     constexpr int kNW = kRbkThreads / 32;
-    constexpr int kSubChunks = kRbkThreads * kRbkItems;  // chunks per sub-tile
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(128) unsigned char dsm[];
     RbkSmem &sm = *reinterpret_cast<RbkSmem *>(dsm);
@@ -184,176 +182,127 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
         }
         phase ^= 1u;
         const uint32_t kprev = sm.kprev, knext = sm.knext;
+        using P = Seg<VF>;
+        using V = typename P::V;
 
-        // Pass 0: the super-tile's pair (heads, sum of the run open at its
-        // end), published before the scan. Head bits, their count and the
-        // last head first (one 16-byte read of keys per chunk) ...
-        uint32_t cnt = 0u;
-        int last = -1;
-        for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
-            const uint4 kk = lds128(&sm.keys[c]);
-            uint32_t before = (4 * c - 1 >= llo) ? skey[4 * c - 1] : kprev;
+        // Pass A: each thread folds its segment of 16 consecutive elements of
+        // each sub-tile in order: head bits, and the segment's pair (heads,
+        // sum of the values after its last head -- all of them if none).
+        P seg[kRbkSub];
+#pragma unroll
+        for (int sub = 0; sub < kRbkSub; ++sub) {
+            const int i0 = sub * kRbkSubElems + kRbkSeg * threadIdx.x;
+            uint32_t prev = (i0 - 1 >= llo) ? skey[i0 - 1] : kprev;
             uint32_t m = 0u;
+            P acc = P::ident();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * c + k;
-                const uint32_t key = word(kk, k);
-                const bool h = i >= llo && i < lhi && (t0 + i == lo || keys_differ<KF>(key, before));
-                m |= (h ? 1u : 0u) << k;
-                before = key;
-            }
-            sm.heads[c] = (uint8_t)m;
-            if (m) {
-                cnt += __popc(m);
-                last = 4 * c + 31 - __clz(m);
-            }
-        }
+            for (int q = 0; q < kRbkSeg / 4; ++q) {
+                const uint4 kk = lds128(&sm.keys[i0 / 4 + q]);
+                const uint4 vv4 = lds128(&sm.vals[i0 / 4 + q]);
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            cnt += __shfl_xor_sync(kFull, cnt, d);
-            last = max(last, __shfl_xor_sync(kFull, last, d));
-        }
-        if (lane == 0) {
-            sm.red_c[warp] = cnt;
-            sm.red_l[warp] = last;
-        }
-        __syncthreads();  // also: every head mask is written
-        uint32_t tc = 0u;
-        int tl = -1;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) {
-            tc += sm.red_c[w];
-            tl = max(tl, sm.red_l[w]);
-        }
-        // ... then the values from the last head (or the tile start) on.
-        const int from = tl >= 0 ? tl : llo;
-        uint32_t ssum = 0u;  // bits of the partial sum
-        for (int c = from / 4 + threadIdx.x; c < (lhi + 3) / 4; c += kRbkThreads) {
-            const uint4 vv4 = lds128(&sm.vals[c]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * c + k;
-                if (i >= from && i < lhi) {
-                    const uint32_t v = word(vv4, k);
-                    ssum = VF ? __float_as_uint(__uint_as_float(ssum) + __uint_as_float(v)) : ssum + v;
+                for (int k = 0; k < 4; ++k) {
+                    const int i = i0 + 4 * q + k;
+                    const uint32_t key = word(kk, k);
+                    if (i >= llo && i < lhi) {
+                        const bool h = t0 + i == lo || keys_differ<KF>(key, prev);
+                        m |= (h ? 1u : 0u) << (4 * q + k);
+                        acc = P::apply(acc, P{h ? 1u : 0u, P::val(word(vv4, k))});
+                    }
+                    prev = key;
                 }
             }
+            sm.heads[sub][threadIdx.x] = m;
+            seg[sub] = acc;
         }
+
+        // The segments' exclusive prefixes in order (sub-tile, then thread):
+        // warp scans, warp totals through shared memory.
+        P excl[kRbkSub];
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const uint32_t o = __shfl_xor_sync(kFull, ssum, d);
-            ssum = VF ? __float_as_uint(__uint_as_float(ssum) + __uint_as_float(o)) : ssum + o;
+        for (int sub = 0; sub < kRbkSub; ++sub) {
+            P inc = seg[sub];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const P y = inc.shfl_up(d);
+                if (lane >= d)
+                    inc = P::apply(y, inc);
+            }
+            P e = inc.shfl_up(1);
+            if (lane == 0)
+                e = P::ident();
+            excl[sub] = e;
+            if (lane == 31) {
+                sm.warp_c[sub][warp] = inc.c;
+                sm.warp_s[sub][warp] = P::bits(inc.s);
+            }
         }
-        if (lane == 0)
-            sm.red_s[warp] = ssum;
-        __syncthreads();
-        uint32_t ts = 0u;
+        __syncthreads();  // warp totals and head bits are written
+        P agg = P::ident();
 #pragma unroll
-        for (int w = 0; w < kNW; ++w)
-            ts = VF ? __float_as_uint(__uint_as_float(ts) + __uint_as_float(sm.red_s[w])) : ts + sm.red_s[w];
-        const uint64_t agg = ((uint64_t)tc << 32) | ts;
-        publish_aggregate<uint64_t, Op>(a.lb, g, 0, agg);
+        for (int sub = 0; sub < kRbkSub; ++sub) {
+            P before = agg;  // everything before this sub-tile's warp `warp`
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+                const P t{sm.warp_c[sub][w], P::val(sm.warp_s[sub][w])};
+                if (w < warp)
+                    before = P::apply(before, t);
+                agg = P::apply(agg, t);
+            }
+            excl[sub] = P::apply(before, excl[sub]);
+        }
+        const uint64_t aggp = ((uint64_t)agg.c << 32) | P::bits(agg.s);
+        publish_aggregate<uint64_t, Op>(a.lb, g, 0, aggp);
 
         // Does the super-tile's last element end its run?
         const bool last_ends = lhi > llo && (t0 + lhi == hi || keys_differ<KF>(knext, skey[lhi - 1]));
 
-        // The prefix of the super-tile, looked back for before the scan: the
-        // scan below then writes final results.
-        using P = Seg<VF>;
-        P carry = P::unpack(lookback_prefix<uint64_t, Op>(a.lb, g, 0, agg, &sm.prefix));
+        // The prefix of the super-tile, looked back for before the outputs.
+        const P tp = P::unpack(lookback_prefix<uint64_t, Op>(a.lb, g, 0, aggp, &sm.prefix));
 
-        // Pass 1: sub-tiles in order, chunk j*32 + lane of each warp's run.
-#pragma unroll 1
+        // Pass B: each segment again from its prefix: heads write their key,
+        // run ends the run's sum, at run index c - 1.
+#pragma unroll
         for (int sub = 0; sub < kRbkSub; ++sub) {
-            P x[kRbkItems][4];
-            uint32_t hm[kRbkItems], em[kRbkItems];  // head and run-end bits per chunk
+            const int i0 = sub * kRbkSubElems + kRbkSeg * threadIdx.x;
+            const uint32_t m = sm.heads[sub][threadIdx.x];
+            // the first head bit of the next segment (0 past the super-tile)
+            uint32_t mnext = 0u;
+            if (threadIdx.x + 1 < kRbkThreads)
+                mnext = sm.heads[sub][threadIdx.x + 1] & 1u;
+            else if (sub + 1 < kRbkSub)
+                mnext = sm.heads[sub + 1][0] & 1u;
+            uint32_t e = (m >> 1) | (mnext << (kRbkSeg - 1));
+            const int li = lhi - 1 - i0;  // the last valid element, if in this segment
+            if (li >= 0 && li < kRbkSeg)
+                e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
+            else if (li < 0)
+                e = 0u;
+            const int lv = llo - i0;  // elements before the first valid one end nothing
+            if (lv > 0)
+                e &= lv >= kRbkSeg ? 0u : ~((1u << lv) - 1u);
+            if ((m | e) == 0u)
+                continue;  // neither a head nor a run end in this segment
+            P run = P::apply(tp, excl[sub]);
 #pragma unroll
-            for (int j = 0; j < kRbkItems; ++j) {
-                const int c = sub * kSubChunks + warp * 32 * kRbkItems + j * 32 + lane;
-                const uint4 vv4 = lds128(&sm.vals[c]);
-                const uint32_t m = sm.heads[c];
-                const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : 0u;
-                // element i ends a run when i + 1 starts one, or it is the last
-                uint32_t e = (m >> 1) | ((mn & 1u) << 3);
-                const int li = lhi - 1 - 4 * c;  // the last valid element, if in this chunk
-                if (li >= 0 && li < 4)
-                    e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
-                else if (li < 0)
-                    e = 0u;
-                uint32_t vm = 0u;  // valid elements of the chunk
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i = 4 * c + k;
-                    const bool valid = i >= llo && i < lhi;
-                    vm |= (valid ? 1u : 0u) << k;
-                    x[j][k] = P{(m >> k) & 1u, valid ? P::val(word(vv4, k)) : typename P::V(0)};
-                }
-                hm[j] = m;       // heads are valid elements by construction
-                em[j] = e & vm;  // no end for an element outside the array
-#pragma unroll
-                for (int k = 1; k < 4; ++k)
-                    x[j][k] = P::apply(x[j][k - 1], x[j][k]);
-            }
-            P inc[kRbkItems];
-#pragma unroll
-            for (int j = 0; j < kRbkItems; ++j)
-                inc[j] = x[j][3];
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-#pragma unroll
-                for (int j = 0; j < kRbkItems; ++j) {
-                    const P y = inc[j].shfl_up(d);
-                    if (lane >= d)
-                        inc[j] = P::apply(y, inc[j]);
-                }
-            }
-            P pre[kRbkItems];
-            P run = P::ident();
-#pragma unroll
-            for (int j = 0; j < kRbkItems; ++j) {
-                P e = inc[j].shfl_up(1);
-                if (lane == 0)
-                    e = P::ident();
-                pre[j] = P::apply(run, e);
-                run = P::apply(run, inc[j].shfl(31));
-            }
-            if (lane == 0) {
-                sm.warp_c[sub & 1][warp] = run.c;
-                sm.warp_s[sub & 1][warp] = P::bits(run.s);
-            }
-            __syncthreads();
-            P wpre = P::ident(), tot = P::ident();
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                const P t{sm.warp_c[sub & 1][w], P::val(sm.warp_s[sub & 1][w])};
-                if (w < warp)
-                    wpre = P::apply(wpre, t);
-                tot = P::apply(tot, t);
-            }
-            const P base0 = P::apply(carry, wpre);
-            // heads write their key, run ends the run's sum, at run index c - 1
-#pragma unroll
-            for (int j = 0; j < kRbkItems; ++j) {
-                if ((hm[j] | em[j]) == 0u)
-                    continue;
-                const P base = P::apply(base0, pre[j]);
-                const int c = sub * kSubChunks + warp * 32 * kRbkItems + j * 32 + lane;
+            for (int q = 0; q < kRbkSeg / 4; ++q) {
+                const uint4 vv4 = lds128(&sm.vals[i0 / 4 + q]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    if (((hm[j] | em[j]) >> k) & 1u) {
-                        const P p = P::apply(base, x[j][k]);
-                        const uint32_t r = p.c - 1u;
-                        if ((hm[j] >> k) & 1u)
-                            a.keys_out[r] = skey[4 * c + k];
-                        if ((em[j] >> k) & 1u) {
-                            a.vals_out[r] = P::bits(p.s);
-                            if (t0 + 4 * c + k == hi - 1)
-                                *a.num_runs = (int32_t)(r + 1u);
-                        }
+                    const int b = 4 * q + k;
+                    const int i = i0 + b;
+                    const bool h = (m >> b) & 1u;
+                    if (i >= llo && i < lhi)
+                        run = P::apply(run, P{h ? 1u : 0u, P::val(word(vv4, k))});
+                    const uint32_t r = run.c - 1u;
+                    if (h)
+                        a.keys_out[r] = skey[i];
+                    if ((e >> b) & 1u) {
+                        a.vals_out[r] = P::bits(run.s);
+                        if (t0 + i == hi - 1)
+                            *a.num_runs = (int32_t)(r + 1u);
                     }
                 }
             }
-            carry = P::apply(carry, tot);
         }
         fence_proxy_async_smem();  // this thread's shared accesses precede the next bulk copies
     }
