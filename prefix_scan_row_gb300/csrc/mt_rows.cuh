@@ -19,11 +19,17 @@ struct RowArgs {
 };
 
 // One CTA per row; the whole row is one tile of blockDim.x * ITEMS chunks
-// (the block size is chosen per row length, up to 16 warps).
-// (A minimum-blocks bound, even 1, makes the compiler spend more registers
-// here and costs resident CTAs.)
+// (the block size is chosen per row length, up to 16 warps). Up to 3 chunks
+// per thread the kernel fits 40 registers, so 3 blocks of 512 threads (or 6
+// of 256) stay resident: short rows then keep more loads in flight per SM.
+// With 4 chunks that cap would spill, and no bound is given (a bound of 1
+// makes the compiler spend more registers than none).
+template <int ITEMS>
+constexpr int rows_min_blocks() {
+    return ITEMS <= 3 ? 3 : 0;
+}
 template <class S, class Op, int ITEMS>
-__global__ void __launch_bounds__(512) k_scan_rows(RowArgs a) {
+__global__ void __launch_bounds__(512, rows_min_blocks<ITEMS>()) k_scan_rows(RowArgs a) {
     pdl_prologue();
     using T = RowTile<S, Op, ITEMS>;
     __shared__ typename T::Smem sm;
