@@ -48,6 +48,9 @@ struct SegArgs {
 #ifndef MT_STAGED_PAIR_W8
 #define MT_STAGED_PAIR_W8 1  // the same for 8-byte types
 #endif
+#ifndef MT_STAGED_EARLY_LB
+#define MT_STAGED_EARLY_LB 0  // 1: look back before the scan for every type (f64 always does)
+#endif
 #ifndef MT_STAGED_EARLY_W4
 #define MT_STAGED_EARLY_W4 1  // early aggregate for 4-byte accumulators
 #endif
@@ -195,6 +198,31 @@ struct Staged {
         }
     }
 
+    // A unit's final values straight to global memory (the early look-back
+    // form): 16-byte stores for whole chunks when the output has the input's
+    // 16-byte phase, element stores otherwise.
+    template <bool FULL>
+    __device__ __forceinline__ static void store_unit(S *eo, bool aligned_io, int u, int llo, int lhi,
+                                                      const Acc (&x)[EU]) {
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+            const int c = V * u + q;
+            const int o = c * E;
+            Acc part[E];
+#pragma unroll
+            for (int k = 0; k < E; ++k)
+                part[k] = x[q * E + k];
+            if (aligned_io && (FULL || (o >= llo && o + E <= lhi))) {
+                st_v4(reinterpret_cast<uint4 *>(eo) + c, C::pack(part));
+            } else if (FULL || (o < lhi && o + E > llo)) {
+#pragma unroll
+                for (int k = 0; k < E; ++k)
+                    if (FULL || (o + k >= llo && o + k < lhi))
+                        C::store1(eo + o + k, part[k]);
+            }
+        }
+    }
+
     // The super-tile's aggregate (valid in every thread). Any grouping gives
     // the same result for adds of integers, for integer min/max, and for float
     // min/max unless the result is a zero (which of +0/-0 comes first then
@@ -285,8 +313,15 @@ struct Staged {
         }
 
         // Pass 1: sub-tiles in order with a running carry; keep each
-        // element's super-tile-local prefix in shared memory.
+        // element's super-tile-local prefix in shared memory (or, with the
+        // early look-back, start from the super-tile's prefix and store final
+        // results). The early form saves pass 2's combine per element but
+        // exposes the look-back's latency: measured slower wherever memory
+        // bounds the kernel, 12 % faster for f64, which GB300's FP64 rate bounds.
+        constexpr bool kEarlyLB = (MT_STAGED_EARLY_LB || std::is_same<Acc, double>::value) && kEarly;
         Acc carry = ident;
+        if constexpr (kEarlyLB)
+            carry = lookback_prefix<Acc, Op>(a.lb, g, first, agg_total, &sm.prefix[buf]);
 #pragma unroll 1
         for (int sub = 0; sub < SUB; ++sub) {
             Acc x[kU][EU];
@@ -345,10 +380,15 @@ struct Staged {
                         x[j][k] = Op::apply(base, x[j][k - 1]);
                     x[j][0] = base;
                 }
-                put_unit(sm, unit_of(sub, j), x[j]);
+                if constexpr (kEarlyLB)
+                    store_unit<FULL>(eo, a.aligned_io != 0, unit_of(sub, j), llo, lhi, x[j]);
+                else
+                    put_unit(sm, unit_of(sub, j), x[j]);
             }
             carry = Op::apply(carry, agg);
         }
+        if constexpr (kEarlyLB)
+            return;
 
         if constexpr (!kEarly) {
             agg_total = carry;
