@@ -14,25 +14,32 @@
 // run -- and the tile scans pairs with the segmented operator
 //   (c1, s1) + (c2, s2) = (c1 + c2, c2 != 0 ? s2 : s1 + s2),
 // whose inclusive prefix at an element is (runs started so far, sum of the
-// open run). Super-tiles of 8192 keys and values arrive in shared memory by
-// bulk copies. Each thread folds segments of 16 consecutive elements serially
-// (head bits kept as a mask), so only one pair per thread and segment enters
-// the warp and block scans; the super-tile's own pair is published as soon as
-// that scan is done; warp 0 then looks back for the pairs of all earlier
-// super-tiles (packed in 64 bits), and a second pass over each segment writes
-// the results: heads keys_out[c - 1], run ends values_out[c - 1]. No atomics
+// open run). Super-tiles of 4096 keys and values arrive in shared memory by
+// bulk copies. A first pass over the 16-byte chunks (consecutive lanes,
+// consecutive chunks: no bank conflicts) finds each chunk's head bits and its
+// own pair; each thread then folds the pairs of 4 consecutive chunks, so one
+// pair per thread enters the warp and block scans; the super-tile's own pair
+// is published as soon as that scan is done; warp 0 then looks back for the
+// pairs of all earlier super-tiles (packed in 64 bits); every chunk's prefix
+// goes back to shared memory, and a second chunk pass writes the results:
+// heads keys_out[c - 1], run ends values_out[c - 1]. No atomics
 // on the outputs, and sums are added in a fixed order.
+#include <cstddef>
 #include <type_traits>
 
 #include "mt_lookback.cuh"
 
 namespace mt {
 
+#ifndef MT_RBK_TILE
+#define MT_RBK_TILE 4096  // elements per super-tile: 4096 or 8192
+#endif
 constexpr int kRbkThreads = 256;
 constexpr int kRbkSeg = 16;                                       // consecutive elements per thread segment
-constexpr int kRbkSub = 8192 / (256 * kRbkSeg);                   // segments per thread per super-tile
+constexpr int kRbkSub = MT_RBK_TILE / (256 * kRbkSeg);            // segments per thread per super-tile
+static_assert(kRbkSub == 1 || kRbkSub == 2, "super-tile of 4096 or 8192 elements");
 constexpr int kRbkSubElems = kRbkThreads * kRbkSeg;               // elements per sub-tile (4096)
-constexpr int64_t kRbkTE = (int64_t)kRbkSub * kRbkSubElems;       // elements per super-tile (8192)
+constexpr int64_t kRbkTE = (int64_t)kRbkSub * kRbkSubElems;       // elements per super-tile (4096)
 constexpr int kRbkChunks = (int)(kRbkTE / 4);                     // 16-byte chunks per super-tile
 
 struct RbkArgs {
@@ -113,14 +120,20 @@ __device__ __forceinline__ uint32_t word(const uint4 &v, int k) {
 struct RbkSmem {
     uint4 keys[kRbkChunks];
     uint4 vals[kRbkChunks];
+    uint32_t csum[kRbkChunks]; // per chunk: its own open-run sum, then the sum part of its prefix
+    uint32_t ccnt[kRbkChunks]; // per chunk: the count part of its prefix
+    uint8_t heads[kRbkChunks]; // head bits of each chunk (bit k: its element k)
     uint64_t bar;
     unsigned long long tile;
     uint32_t kprev, knext;     // the neighbours' keys (when they exist)
-    uint32_t heads[kRbkSub][kRbkThreads];   // head bits of each segment (bit k: its element k)
     uint32_t warp_c[kRbkSub][kRbkThreads / 32];  // warp totals of the segment scan
     uint32_t warp_s[kRbkSub][kRbkThreads / 32];
     uint64_t prefix;
 };
+// csum and ccnt are read and written 16 bytes at a time, heads 4 at a time
+static_assert(offsetof(RbkSmem, csum) % 16 == 0 && offsetof(RbkSmem, ccnt) % 16 == 0 &&
+                  offsetof(RbkSmem, heads) % 4 == 0 && offsetof(RbkSmem, bar) % 8 == 0,
+              "shared-memory layout of the reduce-by-key kernel");
 
 template <bool KF, bool VF>
 __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
@@ -183,35 +196,49 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
         phase ^= 1u;
         const uint32_t kprev = sm.kprev, knext = sm.knext;
         using P = Seg<VF>;
-        using V = typename P::V;
 
-        // Pass A: each thread folds its segment of 16 consecutive elements of
-        // each sub-tile in order: head bits, and the segment's pair (heads,
-        // sum of the values after its last head -- all of them if none).
-        P seg[kRbkSub];
-#pragma unroll
-        for (int sub = 0; sub < kRbkSub; ++sub) {
-            const int i0 = sub * kRbkSubElems + kRbkSeg * threadIdx.x;
-            uint32_t prev = (i0 - 1 >= llo) ? skey[i0 - 1] : kprev;
+        // Pass A, chunk by chunk (consecutive lanes, consecutive 16-byte
+        // chunks: no bank conflicts): head bits and the chunk's own pair.
+        // The key before a chunk is the last key of the lane to the left.
+#pragma unroll 1
+        for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
+            const uint4 kk = lds128(&sm.keys[c]);
+            const uint4 vv4 = lds128(&sm.vals[c]);
+            uint32_t prev = __shfl_up_sync(kFull, kk.w, 1);
+            if (lane == 0)
+                prev = (4 * c - 1 >= llo) ? skey[4 * c - 1] : kprev;
             uint32_t m = 0u;
             P acc = P::ident();
 #pragma unroll
-            for (int q = 0; q < kRbkSeg / 4; ++q) {
-                const uint4 kk = lds128(&sm.keys[i0 / 4 + q]);
-                const uint4 vv4 = lds128(&sm.vals[i0 / 4 + q]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i = i0 + 4 * q + k;
-                    const uint32_t key = word(kk, k);
-                    if (i >= llo && i < lhi) {
-                        const bool h = t0 + i == lo || keys_differ<KF>(key, prev);
-                        m |= (h ? 1u : 0u) << (4 * q + k);
-                        acc = P::apply(acc, P{h ? 1u : 0u, P::val(word(vv4, k))});
-                    }
-                    prev = key;
+            for (int k = 0; k < 4; ++k) {
+                const int i = 4 * c + k;
+                const uint32_t key = word(kk, k);
+                if (i >= llo && i < lhi) {
+                    const bool h = t0 + i == lo || keys_differ<KF>(key, prev);
+                    m |= (h ? 1u : 0u) << k;
+                    acc = P::apply(acc, P{h ? 1u : 0u, P::val(word(vv4, k))});
                 }
+                prev = key;
             }
-            sm.heads[sub][threadIdx.x] = m;
+            sm.heads[c] = (uint8_t)m;
+            sm.csum[c] = P::bits(acc.s);
+        }
+        __syncthreads();
+
+        // Each thread owns segments of 4 consecutive chunks (16 elements):
+        // their pairs from the chunk pairs, in order.
+        P seg[kRbkSub], cpre[kRbkSub][4];
+#pragma unroll
+        for (int sub = 0; sub < kRbkSub; ++sub) {
+            const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
+            const uint32_t m4 = *reinterpret_cast<const uint32_t *>(&sm.heads[c0]);
+            const uint4 s4 = lds128(reinterpret_cast<const uint4 *>(&sm.csum[c0]));
+            P acc = P::ident();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                cpre[sub][q] = acc;
+                acc = P::apply(acc, P{(uint32_t)__popc((m4 >> (8 * q)) & 0xffu), P::val(word(s4, q))});
+            }
             seg[sub] = acc;
         }
 
@@ -236,7 +263,7 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
                 sm.warp_s[sub][warp] = P::bits(inc.s);
             }
         }
-        __syncthreads();  // warp totals and head bits are written
+        __syncthreads();  // warp totals are written
         P agg = P::ident();
 #pragma unroll
         for (int sub = 0; sub < kRbkSub; ++sub) {
@@ -256,51 +283,57 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
         // Does the super-tile's last element end its run?
         const bool last_ends = lhi > llo && (t0 + lhi == hi || keys_differ<KF>(knext, skey[lhi - 1]));
 
-        // The prefix of the super-tile, looked back for before the outputs.
+        // The prefix of the super-tile, looked back for before the outputs;
+        // then every chunk's prefix, written back by the segment's owner.
         const P tp = P::unpack(lookback_prefix<uint64_t, Op>(a.lb, g, 0, aggp, &sm.prefix));
-
-        // Pass B: each segment again from its prefix: heads write their key,
-        // run ends the run's sum, at run index c - 1.
 #pragma unroll
         for (int sub = 0; sub < kRbkSub; ++sub) {
-            const int i0 = sub * kRbkSubElems + kRbkSeg * threadIdx.x;
-            const uint32_t m = sm.heads[sub][threadIdx.x];
-            // the first head bit of the next segment (0 past the super-tile)
-            uint32_t mnext = 0u;
-            if (threadIdx.x + 1 < kRbkThreads)
-                mnext = sm.heads[sub][threadIdx.x + 1] & 1u;
-            else if (sub + 1 < kRbkSub)
-                mnext = sm.heads[sub + 1][0] & 1u;
-            uint32_t e = (m >> 1) | (mnext << (kRbkSeg - 1));
-            const int li = lhi - 1 - i0;  // the last valid element, if in this segment
-            if (li >= 0 && li < kRbkSeg)
+            const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
+            const P base = P::apply(tp, excl[sub]);
+            uint4 ps, pc;
+            P q0 = P::apply(base, cpre[sub][0]), q1 = P::apply(base, cpre[sub][1]);
+            P q2 = P::apply(base, cpre[sub][2]), q3 = P::apply(base, cpre[sub][3]);
+            ps = make_uint4(P::bits(q0.s), P::bits(q1.s), P::bits(q2.s), P::bits(q3.s));
+            pc = make_uint4(q0.c, q1.c, q2.c, q3.c);
+            sts128(reinterpret_cast<uint4 *>(&sm.csum[c0]), ps);
+            sts128(reinterpret_cast<uint4 *>(&sm.ccnt[c0]), pc);
+        }
+        __syncthreads();
+
+        // Pass B, chunk by chunk again: heads write their key, run ends the
+        // run's sum, at run index c - 1.
+#pragma unroll 1
+        for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
+            const uint32_t m = sm.heads[c];
+            const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : 0u;
+            // element i ends a run when i + 1 starts one, or it is the last
+            uint32_t e = (m >> 1) | ((mn & 1u) << 3);
+            const int li = lhi - 1 - 4 * c;  // the last valid element, if in this chunk
+            if (li >= 0 && li < 4)
                 e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
             else if (li < 0)
                 e = 0u;
-            const int lv = llo - i0;  // elements before the first valid one end nothing
+            const int lv = llo - 4 * c;  // elements before the first valid one end nothing
             if (lv > 0)
-                e &= lv >= kRbkSeg ? 0u : ~((1u << lv) - 1u);
+                e &= lv >= 4 ? 0u : ~((1u << lv) - 1u);
             if ((m | e) == 0u)
-                continue;  // neither a head nor a run end in this segment
-            P run = P::apply(tp, excl[sub]);
+                continue;
+            const uint4 vv4 = lds128(&sm.vals[c]);
+            const uint4 kk = lds128(&sm.keys[c]);
+            P run{sm.ccnt[c], P::val(sm.csum[c])};
 #pragma unroll
-            for (int q = 0; q < kRbkSeg / 4; ++q) {
-                const uint4 vv4 = lds128(&sm.vals[i0 / 4 + q]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int b = 4 * q + k;
-                    const int i = i0 + b;
-                    const bool h = (m >> b) & 1u;
-                    if (i >= llo && i < lhi)
-                        run = P::apply(run, P{h ? 1u : 0u, P::val(word(vv4, k))});
-                    const uint32_t r = run.c - 1u;
-                    if (h)
-                        a.keys_out[r] = skey[i];
-                    if ((e >> b) & 1u) {
-                        a.vals_out[r] = P::bits(run.s);
-                        if (t0 + i == hi - 1)
-                            *a.num_runs = (int32_t)(r + 1u);
-                    }
+            for (int k = 0; k < 4; ++k) {
+                const int i = 4 * c + k;
+                const bool h = (m >> k) & 1u;
+                if (i >= llo && i < lhi)
+                    run = P::apply(run, P{h ? 1u : 0u, P::val(word(vv4, k))});
+                const uint32_t r = run.c - 1u;
+                if (h)
+                    a.keys_out[r] = word(kk, k);
+                if ((e >> k) & 1u) {
+                    a.vals_out[r] = P::bits(run.s);
+                    if (t0 + i == hi - 1)
+                        *a.num_runs = (int32_t)(r + 1u);
                 }
             }
         }
