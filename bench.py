@@ -371,7 +371,7 @@ def run_ours(args, world, rank, local):
                         "copy, all on one stream, CUDA events around the steps")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
-                     "kernel": "k_scan_rows<__nv_bfloat16,OpAdd,4> on [8192,8192] exclusive",
+                     "kernel": "k_scan_rows<__nv_bfloat16,OpAdd,4,256> on [8192,8192] exclusive",
                      "bytes_per_launch": DOM_BYTES, "avg_launch_ms": round(dom_ms, 5),
                      "peak_of": peak_src},
         "clocks": sampler.summary(th0, th1),

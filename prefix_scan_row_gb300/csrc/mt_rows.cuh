@@ -22,14 +22,19 @@ struct RowArgs {
 // (the block size is chosen per row length, up to 16 warps). Up to 3 chunks
 // per thread the kernel fits 40 registers, so 3 blocks of 512 threads (or 6
 // of 256) stay resident: short rows then keep more loads in flight per SM.
-// With 4 chunks that cap would spill, and no bound is given (a bound of 1
-// makes the compiler spend more registers than none).
-template <int ITEMS>
+// With 4 chunks that cap would spill; blocks of at most 256 threads (MAXT)
+// ask for 5 resident blocks (48 registers and a few bytes of spill: 80 KB of
+// loads in flight per SM instead of 64), and 512-thread blocks for no bound
+// (a bound of 1 block of 512 makes the compiler spend more registers than none).
+#ifndef MT_ROWS_B4_256
+#define MT_ROWS_B4_256 5  // resident 256-thread blocks asked for with 4 chunks per thread (48 registers)
+#endif
+template <int ITEMS, int MAXT>
 constexpr int rows_min_blocks() {
-    return ITEMS <= 3 ? 3 : 0;
+    return MAXT == 256 ? (ITEMS == 4 ? MT_ROWS_B4_256 : 0) : (ITEMS <= 3 ? 3 : 0);
 }
-template <class S, class Op, int ITEMS>
-__global__ void __launch_bounds__(512, rows_min_blocks<ITEMS>()) k_scan_rows(RowArgs a) {
+template <class S, class Op, int ITEMS, int MAXT>
+__global__ void __launch_bounds__(MAXT, (rows_min_blocks<ITEMS, MAXT>())) k_scan_rows(RowArgs a) {
     pdl_prologue();
     using T = RowTile<S, Op, ITEMS>;
     __shared__ typename T::Smem sm;
@@ -67,7 +72,11 @@ static constexpr int sub_of() {
 
 template <class S, class Op, int ITEMS>
 static cudaError_t launch_one(const RowArgs &a, int64_t grid, int warps, cudaStream_t st) {
-    return launch_pdl(k_scan_rows<S, Op, ITEMS>, (unsigned)grid, 32 * warps, 0, st, a);
+    if constexpr (ITEMS == 4) {
+        if (warps <= 8)
+            return launch_pdl(k_scan_rows<S, Op, ITEMS, 256>, (unsigned)grid, 32 * warps, 0, st, a);
+    }
+    return launch_pdl(k_scan_rows<S, Op, ITEMS, 512>, (unsigned)grid, 32 * warps, 0, st, a);
 }
 
 template <class S, class Op>
