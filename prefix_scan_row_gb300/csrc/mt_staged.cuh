@@ -16,6 +16,10 @@
 // flight per SM is (resident CTAs) x (super-tile bytes) without spending
 // registers on it. Every super-tile but the first and last of a segment lies
 // wholly inside it; those take a path with no per-chunk range checks.
+// Types whose arithmetic, not memory, bounds the scan (f64: GB300 issues
+// FP64 adds at about 2 per clock per SM) take a leaner form of steps 2-4,
+// tile_lean: per-thread runs of consecutive chunks and about 2 combines per
+// element instead of 5 to 7.
 #pragma once
 
 #include <type_traits>
@@ -49,13 +53,19 @@ struct SegArgs {
 #define MT_STAGED_PAIR_W8 1  // the same for 8-byte types
 #endif
 #ifndef MT_STAGED_EARLY_LB
-#define MT_STAGED_EARLY_LB 0  // 1: look back before the scan for every type (f64 always does)
+#define MT_STAGED_EARLY_LB 0  // 1: look back before the scan
 #endif
 #ifndef MT_STAGED_EARLY_W4
 #define MT_STAGED_EARLY_W4 1  // early aggregate for 4-byte accumulators
 #endif
 #ifndef MT_STAGED_EARLY_W8
 #define MT_STAGED_EARLY_W8 1  // the same for 8-byte accumulators
+#endif
+#ifndef MT_STAGED_LEAN_F64
+#define MT_STAGED_LEAN_F64 1  // f64: per-thread runs (tile_lean)
+#endif
+#ifndef MT_STAGED_LEAN_I64
+#define MT_STAGED_LEAN_I64 0  // the same for 64-bit integers (measured slower: memory bounds them)
 #endif
 
 template <class S, class Op, int ITEMS, int SUB, int THREADS>
@@ -75,6 +85,12 @@ struct Staged {
     // one plane (prefixes as wide as the input) and an even ITEMS.
     static constexpr int V =
         (kPlanes == 1 && ITEMS % 2 == 0 && (sizeof(Acc) == 8 ? MT_STAGED_PAIR_W8 : MT_STAGED_PAIR_W4)) ? 2 : 1;
+    // Types whose combines, not memory, bound the scan take tile_lean: on
+    // GB300 an f64 add issues at about 2 per clock per SM.
+    static constexpr bool kLean =
+        kPlanes == 1 && ((std::is_same<Acc, double>::value && MT_STAGED_LEAN_F64) ||
+                         (sizeof(Acc) == 8 && std::is_integral<Acc>::value && MT_STAGED_LEAN_I64));
+    static constexpr int kRun = kChunks / THREADS;  // tile_lean: chunks per thread, consecutive
     static constexpr int kU = ITEMS / V;  // units per thread per sub-tile
     static constexpr int EU = V * E;      // elements per unit
 
@@ -293,6 +309,132 @@ struct Staged {
         return agg;
     }
 
+    // One super-tile in per-thread runs, for accumulators whose combine is
+    // the bound: thread t owns the kRun consecutive chunks from t * kRun.
+    // Pass 0 folds the run serially; one warp scan of the run totals; warp 0
+    // scans the warp totals, publishes the aggregate and looks back; pass 1
+    // scans the run again from the thread's full prefix and writes the final
+    // values in place; a last pass stores them chunk-coalesced. That is 2
+    // combines per element plus about 7 per run (the sub-tile form takes
+    // 5 to 7 per element). Every combine is in element order, so min and max
+    // give the serial result bit for bit.
+    template <bool FULL>
+    __device__ __forceinline__ static void tile_lean(Smem &sm, const SegArgs &a, int64_t g, int64_t first,
+                                                     S *eo, int llo, int lhi, int buf) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const Acc ident = Op::template identity<Acc>();
+        const int cb = threadIdx.x * kRun;
+
+        // Pass 0: the run's total.
+        Acc tot;
+        {
+            Acc x[E];
+            load<FULL>(sm, cb, llo, lhi, x);
+            tot = x[0];
+#pragma unroll
+            for (int k = 1; k < E; ++k)
+                tot = Op::apply(tot, x[k]);
+        }
+#pragma unroll
+        for (int j = 1; j < kRun; ++j) {
+            Acc x[E];
+            load<FULL>(sm, cb + j, llo, lhi, x);
+#pragma unroll
+            for (int k = 0; k < E; ++k)
+                tot = Op::apply(tot, x[k]);
+        }
+
+        // The runs' exclusive prefixes within the warp.
+        Acc inc = tot;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Acc y = __shfl_up_sync(kFull, inc, d);
+            if (lane >= d)
+                inc = Op::apply(y, inc);
+        }
+        Acc ex = __shfl_up_sync(kFull, inc, 1);
+        if (lane == 0)
+            ex = ident;
+        if (lane == 31)
+            sm.warp_tot[0][warp] = inc;
+        __syncthreads();
+
+        // Warp 0: the warps' exclusive prefixes, the aggregate (published
+        // at once), the look-back, the inclusive prefix.
+        if (warp == 0) {
+            Acc w = lane < kNW ? sm.warp_tot[0][lane] : ident;
+#pragma unroll
+            for (int d = 1; d < kNW; d <<= 1) {
+                const Acc y = __shfl_up_sync(kFull, w, d);
+                if (lane >= d)
+                    w = Op::apply(y, w);
+            }
+            Acc wex = __shfl_up_sync(kFull, w, 1);
+            if (lane == 0)
+                wex = ident;
+            const Acc agg = __shfl_sync(kFull, w, kNW - 1);
+            if (lane < kNW)
+                sm.warp_tot[1][lane] = wex;
+            publish_aggregate<Acc, Op>(a.lb, g, first, agg);
+            Acc pre = ident;
+            if (a.lb.recs != nullptr && g != first) {
+                pre = warp_lookback<Acc, Op>(a.lb.recs, g, first, a.lb.spin_limit);
+                if (lane == 0 && g != a.lb.skip_tile)
+                    Status<Acc>::publish(a.lb.recs + g * Status<Acc>::kSlots, kIncl, Op::apply(pre, agg));
+            }
+            if (lane == 0)
+                sm.prefix[buf] = pre;
+        }
+        __syncthreads();
+
+        // Pass 1: the run scanned from its full prefix, in place.
+        Acc run = Op::apply(Op::apply(sm.prefix[buf], sm.warp_tot[1][warp]), ex);
+#pragma unroll
+        for (int j = 0; j < kRun; ++j) {
+            Acc x[E];
+            load<FULL>(sm, cb + j, llo, lhi, x);
+            if (a.inclusive) {
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    run = Op::apply(run, x[k]);
+                    x[k] = run;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const Acc v = x[k];
+                    x[k] = run;
+                    run = Op::apply(run, v);
+                }
+            }
+            put(sm, cb + j, x);
+        }
+        __syncthreads();
+
+        // Stores: consecutive lanes on consecutive chunks.
+#pragma unroll 1
+        for (int sub = 0; sub < SUB; ++sub) {
+#pragma unroll
+            for (int j = 0; j < ITEMS; ++j) {
+                const int c = chunk_of(sub, j);
+                const int o = c * E;
+                if (!FULL && !(o < lhi && o + E > llo))
+                    continue;
+                const uint4 w = lds128(&sm.stage[c]);
+                if (a.aligned_io && (FULL || (o >= llo && o + E <= lhi))) {
+                    st_v4(reinterpret_cast<uint4 *>(eo) + c, w);
+                } else {
+                    Acc x[E];
+                    C::unpack(w, x);
+#pragma unroll
+                    for (int k = 0; k < E; ++k)
+                        if (FULL || (o + k >= llo && o + k < lhi))
+                            C::store1(eo + o + k, x[k]);
+                }
+            }
+        }
+    }
+
     // One super-tile, from the staged input to the stored outputs.
     //   eo        : output address of the super-tile's virtual element 0
     //   [llo, lhi): the super-tile's valid elements ([0, kTE) when FULL)
@@ -301,6 +443,10 @@ struct Staged {
     template <bool FULL>
     __device__ __forceinline__ static void tile(Smem &sm, const SegArgs &a, int64_t g, int64_t first,
                                                 S *eo, int llo, int lhi, int buf) {
+        if constexpr (kLean) {
+            tile_lean<FULL>(sm, a, g, first, eo, llo, lhi, buf);
+            return;
+        }
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const Acc ident = Op::template identity<Acc>();
 
@@ -317,8 +463,8 @@ struct Staged {
         // early look-back, start from the super-tile's prefix and store final
         // results). The early form saves pass 2's combine per element but
         // exposes the look-back's latency: measured slower wherever memory
-        // bounds the kernel, 12 % faster for f64, which GB300's FP64 rate bounds.
-        constexpr bool kEarlyLB = (MT_STAGED_EARLY_LB || std::is_same<Acc, double>::value) && kEarly;
+        // bounds the kernel.
+        constexpr bool kEarlyLB = MT_STAGED_EARLY_LB && kEarly;
         Acc carry = ident;
         if constexpr (kEarlyLB)
             carry = lookback_prefix<Acc, Op>(a.lb, g, first, agg_total, &sm.prefix[buf]);
