@@ -129,3 +129,31 @@ def test_f64_min_max_signed_zero(mt, first_negative):
         assert_reduce_matches(out, t, n, "f64", op)
         assert np.signbit(out[0].item()) == first_negative
         assert_scan_matches(run_scan(mt, t, n, "f64", op, True), t, n, "f64", op, inclusive=True)
+
+
+@pytest.mark.parametrize("seed", [11, 12])
+def test_f64_min_max_special_values(mt, seed):
+    """f64 min/max over infinities, subnormals, both zeros, values one ulp
+    apart and the extreme finite values: every combine order the kernels use
+    must give the serial result bit for bit. Inputs are NaN-free."""
+    tiny, mn, big = 5e-324, 2.2250738585072014e-308, 1.7976931348623157e308
+    pool = np.array([np.inf, -np.inf, 0.0, -0.0, tiny, -tiny, mn, -mn, np.nextafter(mn, 0.0),
+                     1.0, np.nextafter(1.0, 2.0), np.nextafter(1.0, 0.0), -1.0,
+                     -np.nextafter(1.0, 2.0), -np.nextafter(1.0, 0.0), big, -big, 1e300, -1e300])
+    rng = np.random.default_rng(seed)
+    n = 200_003
+    x = rng.uniform(-1e300, 1e300, n)
+    pick = rng.random(n) < 0.3
+    x[pick] = pool[rng.integers(0, pool.size, int(pick.sum()))]
+    t = torch.from_numpy(x)
+    for op in ("min", "max"):
+        assert_reduce_matches(run_reduce(mt, t, n, "f64", op), t, n, "f64", op)
+        for inclusive in (False, True):
+            assert_scan_matches(run_scan(mt, t, n, "f64", op, inclusive), t, n, "f64", op,
+                                inclusive=inclusive)
+    # Mostly zeros of both signs and the smallest magnitudes: ties everywhere.
+    z = pool[rng.integers(2, 6, n)]
+    tz = torch.from_numpy(z)
+    for op in ("min", "max"):
+        assert_reduce_matches(run_reduce(mt, tz, n, "f64", op), tz, n, "f64", op)
+        assert_scan_matches(run_scan(mt, tz, n, "f64", op, True), tz, n, "f64", op, inclusive=True)
