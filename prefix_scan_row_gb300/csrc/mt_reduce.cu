@@ -32,6 +32,12 @@ constexpr int kRedItems = 8;  // 16-byte chunks per thread per tile: 128 bytes i
 constexpr int kRedTileChunks = kRedThreads * kRedItems;
 constexpr int kRedMaxCtas = 4096;   // partials in the scratch
 constexpr int kRedPartialSlots = 2;  // 8-byte slots per partial (a pair needs two)
+#ifndef MT_RED_F64_ACCS
+#define MT_RED_F64_ACCS 8
+#endif
+// Independent running sums per thread for f64 adds: GB300's FP64 adds are
+// few and slow, and one chain per thread leaves the pipe waiting on results.
+constexpr int kRedF64Accs = MT_RED_F64_ACCS;
 
 struct RedArgs {
     const char *in;
@@ -162,7 +168,11 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
     const int64_t lo = head, hi = head + n;
     const int64_t nchunks = n > 0 ? (hi + E - 1) / E : 0;  // no element: touch nothing
 
-    T acc = F::ident();
+    constexpr int kAccs = (!kChunk && std::is_same<Acc, double>::value) ? kRedF64Accs : 1;
+    T accs[kAccs];
+#pragma unroll
+    for (int i = 0; i < kAccs; ++i)
+        accs[i] = F::ident();
     [[maybe_unused]] ChunkState<Acc> st{Acc(0), kNoChunk};
     if constexpr (kChunk)
         st.v = F::ident_v();
@@ -184,24 +194,27 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
             Acc x[E];
             C::unpack(raw[j], x);
             if constexpr (kChunk) {
-                // the chunk's extreme, earliest first; then the thread's
-                Acc m = F::ident_v();
+                // each element against the thread's extreme (one compare per
+                // element: GB300 compares f64 on its narrow FP64 pipe); strict,
+                // so the earliest chunk with the extreme is kept
 #pragma unroll
                 for (int k = 0; k < E; ++k)
-                    if ((full || (v0 + k >= lo && v0 + k < hi)) && F::better(x[k], m))
-                        m = x[k];
-                if (F::better(m, st.v)) {
-                    st.v = m;
-                    st.c = (uint32_t)c;
-                }
+                    if ((full || (v0 + k >= lo && v0 + k < hi)) && F::better(x[k], st.v)) {
+                        st.v = x[k];
+                        st.c = (uint32_t)c;
+                    }
             } else {
 #pragma unroll
                 for (int k = 0; k < E; ++k)
                     if (full || (v0 + k >= lo && v0 + k < hi))
-                        acc = F::apply(acc, x[k]);
+                        accs[(j * E + k) % kAccs] = F::apply(accs[(j * E + k) % kAccs], x[k]);
             }
         }
     }
+    T acc = accs[0];
+#pragma unroll
+    for (int i = 1; i < kAccs; ++i)
+        acc = F::apply(acc, accs[i]);
     if constexpr (kChunk)
         acc = F::pair(st);
     const T part = block_fold<F>(acc, sm);
