@@ -34,10 +34,13 @@ namespace mt {
 #ifndef MT_RBK_TILE
 #define MT_RBK_TILE 4096  // elements per super-tile: 4096 or 8192
 #endif
-constexpr int kRbkThreads = 256;
+#ifndef MT_RBK_THREADS
+#define MT_RBK_THREADS 256
+#endif
+constexpr int kRbkThreads = MT_RBK_THREADS;
 constexpr int kRbkSeg = 16;                                       // consecutive elements per thread segment
-constexpr int kRbkSub = MT_RBK_TILE / (256 * kRbkSeg);            // segments per thread per super-tile
-static_assert(kRbkSub == 1 || kRbkSub == 2, "super-tile of 4096 or 8192 elements");
+constexpr int kRbkSub = MT_RBK_TILE / (kRbkThreads * kRbkSeg);    // segments per thread per super-tile
+static_assert(kRbkSub >= 1 && kRbkSub * kRbkThreads * kRbkSeg == MT_RBK_TILE, "super-tile shape");
 constexpr int kRbkSubElems = kRbkThreads * kRbkSeg;               // elements per sub-tile (4096)
 constexpr int64_t kRbkTE = (int64_t)kRbkSub * kRbkSubElems;       // elements per super-tile (4096)
 constexpr int kRbkChunks = (int)(kRbkTE / 4);                     // 16-byte chunks per super-tile
@@ -128,6 +131,8 @@ struct RbkSmem {
     uint32_t kprev, knext;     // the neighbours' keys (when they exist)
     uint32_t warp_c[kRbkSub][kRbkThreads / 32];  // warp totals of the segment scan
     uint32_t warp_s[kRbkSub][kRbkThreads / 32];
+    uint32_t wex_c[kRbkSub][kRbkThreads / 32];   // and the warps' exclusive prefixes
+    uint32_t wex_s[kRbkSub][kRbkThreads / 32];
     uint64_t prefix;
 };
 // csum and ccnt are read and written 16 bytes at a time, heads 4 at a time
@@ -135,15 +140,193 @@ static_assert(offsetof(RbkSmem, csum) % 16 == 0 && offsetof(RbkSmem, ccnt) % 16 
                   offsetof(RbkSmem, heads) % 4 == 0 && offsetof(RbkSmem, bar) % 8 == 0,
               "shared-memory layout of the reduce-by-key kernel");
 
+// One staged super-tile: valid elements [llo, lhi) ([0, kRbkTE) when FULL);
+// has_first: it holds the first element (a head whatever its key); has_last:
+// it holds the last one (which ends its run and gives num_runs).
+template <bool KF, bool VF, bool FULL>
+__device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t g, int llo, int lhi,
+                                         bool has_first, bool has_last) {
+    using P = Seg<VF>;
+    using Op = SegOp<VF>;
+    using St = Status<uint64_t>;
+    constexpr int kNW = kRbkThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t *skey = reinterpret_cast<const uint32_t *>(sm.keys);
+    const uint32_t kprev = sm.kprev, knext = sm.knext;
+
+    // Pass A, chunk by chunk (consecutive lanes, consecutive 16-byte chunks:
+    // no bank conflicts): head bits and the sum of the chunk's open run. The
+    // key before a chunk is the last key of the lane to the left.
+#pragma unroll 1
+    for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
+        const uint4 kk = lds128(&sm.keys[c]);
+        const uint4 vv4 = lds128(&sm.vals[c]);
+        uint32_t prev = __shfl_up_sync(kFull, kk.w, 1);
+        if (lane == 0)
+            prev = (4 * c - 1 >= llo) ? skey[4 * c - 1] : kprev;
+        uint32_t m = 0u;
+        typename P::V sum = typename P::V(0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = 4 * c + k;
+            const uint32_t key = word(kk, k);
+            if (FULL || (i >= llo && i < lhi)) {
+                // the first element starts a run whatever its key
+                const bool first = has_first && (FULL ? (k == 0 && c == 0) : i == llo);
+                const bool h = first || keys_differ<KF>(key, prev);
+                m |= (h ? 1u : 0u) << k;
+                const typename P::V v = P::val(word(vv4, k));
+                sum = h ? v : sum + v;
+            }
+            prev = key;
+        }
+        sm.heads[c] = (uint8_t)m;
+        sm.csum[c] = P::bits(sum);
+    }
+    __syncthreads();
+
+    // Each thread owns segments of 4 consecutive chunks (16 elements): their
+    // pairs from the chunk pairs, in order.
+    P seg[kRbkSub], cpre[kRbkSub][4];
+#pragma unroll
+    for (int sub = 0; sub < kRbkSub; ++sub) {
+        const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
+        const uint32_t m4 = *reinterpret_cast<const uint32_t *>(&sm.heads[c0]);
+        const uint4 s4 = lds128(reinterpret_cast<const uint4 *>(&sm.csum[c0]));
+        P acc = P::ident();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            cpre[sub][q] = acc;
+            acc = P::apply(acc, P{(uint32_t)__popc((m4 >> (8 * q)) & 0xffu), P::val(word(s4, q))});
+        }
+        seg[sub] = acc;
+    }
+
+    // The segments' exclusive prefixes in order (sub-tile, then thread):
+    // warp scans; warp 0 scans the warp totals.
+    P ex[kRbkSub];
+#pragma unroll
+    for (int sub = 0; sub < kRbkSub; ++sub) {
+        P inc = seg[sub];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const P y = inc.shfl_up(d);
+            if (lane >= d)
+                inc = P::apply(y, inc);
+        }
+        P e = inc.shfl_up(1);
+        if (lane == 0)
+            e = P::ident();
+        ex[sub] = e;
+        if (lane == 31) {
+            sm.warp_c[sub][warp] = inc.c;
+            sm.warp_s[sub][warp] = P::bits(inc.s);
+        }
+    }
+    __syncthreads();  // warp totals are written
+
+    // Warp 0: the warps' exclusive prefixes, the super-tile's pair (published
+    // at once), the look-back, the inclusive prefix.
+    if (warp == 0) {
+        P agg = P::ident();
+#pragma unroll
+        for (int sub = 0; sub < kRbkSub; ++sub) {
+            P w = lane < kNW ? P{sm.warp_c[sub][lane], P::val(sm.warp_s[sub][lane])} : P::ident();
+#pragma unroll
+            for (int d = 1; d < kNW; d <<= 1) {
+                const P y = w.shfl_up(d);
+                if (lane >= d)
+                    w = P::apply(y, w);
+            }
+            P we = w.shfl_up(1);
+            if (lane == 0)
+                we = P::ident();
+            const P tot = w.shfl(kNW - 1);
+            if (lane < kNW) {
+                const P before = P::apply(agg, we);
+                sm.wex_c[sub][lane] = before.c;
+                sm.wex_s[sub][lane] = P::bits(before.s);
+            }
+            agg = P::apply(agg, tot);
+        }
+        const uint64_t aggp = ((uint64_t)agg.c << 32) | P::bits(agg.s);
+        publish_aggregate<uint64_t, Op>(a.lb, g, 0, aggp);
+        uint64_t pre = 0;  // the identity pair
+        if (a.lb.recs != nullptr && g != 0) {
+            pre = warp_lookback<uint64_t, Op>(a.lb.recs, g, 0, a.lb.spin_limit);
+            if (lane == 0 && g != a.lb.skip_tile)
+                St::publish(a.lb.recs + g * St::kSlots, kIncl, Op::apply(pre, aggp));
+        }
+        if (lane == 0)
+            sm.prefix = pre;
+    }
+    __syncthreads();
+
+    // Every chunk's prefix, written back by the segment's owner.
+    const P tp = P::unpack(sm.prefix);
+#pragma unroll
+    for (int sub = 0; sub < kRbkSub; ++sub) {
+        const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
+        const P base = P::apply(P::apply(tp, P{sm.wex_c[sub][warp], P::val(sm.wex_s[sub][warp])}), ex[sub]);
+        const P q0 = P::apply(base, cpre[sub][0]), q1 = P::apply(base, cpre[sub][1]);
+        const P q2 = P::apply(base, cpre[sub][2]), q3 = P::apply(base, cpre[sub][3]);
+        sts128(reinterpret_cast<uint4 *>(&sm.csum[c0]),
+               make_uint4(P::bits(q0.s), P::bits(q1.s), P::bits(q2.s), P::bits(q3.s)));
+        sts128(reinterpret_cast<uint4 *>(&sm.ccnt[c0]), make_uint4(q0.c, q1.c, q2.c, q3.c));
+    }
+    // Does the super-tile's last element end its run?
+    const bool last_ends = lhi > llo && (has_last || keys_differ<KF>(knext, skey[lhi - 1]));
+    const int c_last = (lhi - 1) >> 2;  // the chunk of the last valid element
+    __syncthreads();
+
+    // Pass B, chunk by chunk again: heads write their key, run ends the
+    // run's sum, at run index c - 1.
+#pragma unroll 1
+    for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
+        const uint32_t m = sm.heads[c];
+        uint32_t e;  // element k ends a run: k + 1 starts one, or k is the last
+        if (FULL) {
+            const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : (last_ends ? 1u : 0u);
+            e = (m >> 1) | ((mn & 1u) << 3);
+        } else {
+            const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : 0u;
+            e = (m >> 1) | ((mn & 1u) << 3);
+            const int li = lhi - 1 - 4 * c;
+            if (li >= 0 && li < 4)
+                e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
+            else if (li < 0)
+                e = 0u;
+            const int lv = llo - 4 * c;  // elements before the first valid one end nothing
+            if (lv > 0)
+                e &= lv >= 4 ? 0u : ~((1u << lv) - 1u);
+        }
+        const uint4 vv4 = lds128(&sm.vals[c]);
+        const uint4 kk = lds128(&sm.keys[c]);
+        P run{sm.ccnt[c], P::val(sm.csum[c])};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = 4 * c + k;
+            const bool h = (m >> k) & 1u;
+            if (FULL || (i >= llo && i < lhi)) {
+                run.c += h ? 1u : 0u;
+                run.s = h ? P::val(word(vv4, k)) : run.s + P::val(word(vv4, k));
+            }
+            const uint32_t r = run.c - 1u;
+            if (h)
+                a.keys_out[r] = word(kk, k);
+            if ((e >> k) & 1u)
+                a.vals_out[r] = P::bits(run.s);
+        }
+        if (has_last && c == c_last)
+            *a.num_runs = (int32_t)run.c;
+    }
+}
+
 template <bool KF, bool VF>
 __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
     pdl_prologue();
-    using Op = SegOp<VF>;
-    constexpr int kNW = kRbkThreads / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(128) unsigned char dsm[];
     RbkSmem &sm = *reinterpret_cast<RbkSmem *>(dsm);
-    const uint32_t *skey = reinterpret_cast<const uint32_t *>(sm.keys);
 
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
@@ -194,149 +377,10 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
             return;
         }
         phase ^= 1u;
-        const uint32_t kprev = sm.kprev, knext = sm.knext;
-        using P = Seg<VF>;
-
-        // Pass A, chunk by chunk (consecutive lanes, consecutive 16-byte
-        // chunks: no bank conflicts): head bits and the chunk's own pair.
-        // The key before a chunk is the last key of the lane to the left.
-#pragma unroll 1
-        for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
-            const uint4 kk = lds128(&sm.keys[c]);
-            const uint4 vv4 = lds128(&sm.vals[c]);
-            uint32_t prev = __shfl_up_sync(kFull, kk.w, 1);
-            if (lane == 0)
-                prev = (4 * c - 1 >= llo) ? skey[4 * c - 1] : kprev;
-            uint32_t m = 0u;
-            P acc = P::ident();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * c + k;
-                const uint32_t key = word(kk, k);
-                if (i >= llo && i < lhi) {
-                    const bool h = t0 + i == lo || keys_differ<KF>(key, prev);
-                    m |= (h ? 1u : 0u) << k;
-                    acc = P::apply(acc, P{h ? 1u : 0u, P::val(word(vv4, k))});
-                }
-                prev = key;
-            }
-            sm.heads[c] = (uint8_t)m;
-            sm.csum[c] = P::bits(acc.s);
-        }
-        __syncthreads();
-
-        // Each thread owns segments of 4 consecutive chunks (16 elements):
-        // their pairs from the chunk pairs, in order.
-        P seg[kRbkSub], cpre[kRbkSub][4];
-#pragma unroll
-        for (int sub = 0; sub < kRbkSub; ++sub) {
-            const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
-            const uint32_t m4 = *reinterpret_cast<const uint32_t *>(&sm.heads[c0]);
-            const uint4 s4 = lds128(reinterpret_cast<const uint4 *>(&sm.csum[c0]));
-            P acc = P::ident();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                cpre[sub][q] = acc;
-                acc = P::apply(acc, P{(uint32_t)__popc((m4 >> (8 * q)) & 0xffu), P::val(word(s4, q))});
-            }
-            seg[sub] = acc;
-        }
-
-        // The segments' exclusive prefixes in order (sub-tile, then thread):
-        // warp scans, warp totals through shared memory.
-        P excl[kRbkSub];
-#pragma unroll
-        for (int sub = 0; sub < kRbkSub; ++sub) {
-            P inc = seg[sub];
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const P y = inc.shfl_up(d);
-                if (lane >= d)
-                    inc = P::apply(y, inc);
-            }
-            P e = inc.shfl_up(1);
-            if (lane == 0)
-                e = P::ident();
-            excl[sub] = e;
-            if (lane == 31) {
-                sm.warp_c[sub][warp] = inc.c;
-                sm.warp_s[sub][warp] = P::bits(inc.s);
-            }
-        }
-        __syncthreads();  // warp totals are written
-        P agg = P::ident();
-#pragma unroll
-        for (int sub = 0; sub < kRbkSub; ++sub) {
-            P before = agg;  // everything before this sub-tile's warp `warp`
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                const P t{sm.warp_c[sub][w], P::val(sm.warp_s[sub][w])};
-                if (w < warp)
-                    before = P::apply(before, t);
-                agg = P::apply(agg, t);
-            }
-            excl[sub] = P::apply(before, excl[sub]);
-        }
-        const uint64_t aggp = ((uint64_t)agg.c << 32) | P::bits(agg.s);
-        publish_aggregate<uint64_t, Op>(a.lb, g, 0, aggp);
-
-        // Does the super-tile's last element end its run?
-        const bool last_ends = lhi > llo && (t0 + lhi == hi || keys_differ<KF>(knext, skey[lhi - 1]));
-
-        // The prefix of the super-tile, looked back for before the outputs;
-        // then every chunk's prefix, written back by the segment's owner.
-        const P tp = P::unpack(lookback_prefix<uint64_t, Op>(a.lb, g, 0, aggp, &sm.prefix));
-#pragma unroll
-        for (int sub = 0; sub < kRbkSub; ++sub) {
-            const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
-            const P base = P::apply(tp, excl[sub]);
-            uint4 ps, pc;
-            P q0 = P::apply(base, cpre[sub][0]), q1 = P::apply(base, cpre[sub][1]);
-            P q2 = P::apply(base, cpre[sub][2]), q3 = P::apply(base, cpre[sub][3]);
-            ps = make_uint4(P::bits(q0.s), P::bits(q1.s), P::bits(q2.s), P::bits(q3.s));
-            pc = make_uint4(q0.c, q1.c, q2.c, q3.c);
-            sts128(reinterpret_cast<uint4 *>(&sm.csum[c0]), ps);
-            sts128(reinterpret_cast<uint4 *>(&sm.ccnt[c0]), pc);
-        }
-        __syncthreads();
-
-        // Pass B, chunk by chunk again: heads write their key, run ends the
-        // run's sum, at run index c - 1.
-#pragma unroll 1
-        for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
-            const uint32_t m = sm.heads[c];
-            const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : 0u;
-            // element i ends a run when i + 1 starts one, or it is the last
-            uint32_t e = (m >> 1) | ((mn & 1u) << 3);
-            const int li = lhi - 1 - 4 * c;  // the last valid element, if in this chunk
-            if (li >= 0 && li < 4)
-                e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
-            else if (li < 0)
-                e = 0u;
-            const int lv = llo - 4 * c;  // elements before the first valid one end nothing
-            if (lv > 0)
-                e &= lv >= 4 ? 0u : ~((1u << lv) - 1u);
-            if ((m | e) == 0u)
-                continue;
-            const uint4 vv4 = lds128(&sm.vals[c]);
-            const uint4 kk = lds128(&sm.keys[c]);
-            P run{sm.ccnt[c], P::val(sm.csum[c])};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * c + k;
-                const bool h = (m >> k) & 1u;
-                if (i >= llo && i < lhi)
-                    run = P::apply(run, P{h ? 1u : 0u, P::val(word(vv4, k))});
-                const uint32_t r = run.c - 1u;
-                if (h)
-                    a.keys_out[r] = word(kk, k);
-                if ((e >> k) & 1u) {
-                    a.vals_out[r] = P::bits(run.s);
-                    if (t0 + i == hi - 1)
-                        *a.num_runs = (int32_t)(r + 1u);
-                }
-            }
-        }
+        if (llo == 0 && lhi == (int)kRbkTE)
+            rbk_tile<KF, VF, true>(sm, a, g, 0, (int)kRbkTE, g == 0, t0 + kRbkTE == hi);
+        else
+            rbk_tile<KF, VF, false>(sm, a, g, llo, lhi, g == 0, t0 + lhi == hi);
         fence_proxy_async_smem();  // this thread's shared accesses precede the next bulk copies
     }
 }
