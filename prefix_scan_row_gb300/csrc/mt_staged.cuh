@@ -61,6 +61,9 @@ struct SegArgs {
 #ifndef MT_STAGED_EARLY_W8
 #define MT_STAGED_EARLY_W8 1  // the same for 8-byte accumulators
 #endif
+#ifndef MT_STAGED_TOT_SHFL
+#define MT_STAGED_TOT_SHFL 1  // pass 1: warp totals scanned by shuffles
+#endif
 #ifndef MT_STAGED_LEAN_F64
 #define MT_STAGED_LEAN_F64 1  // f64: per-thread runs (tile_lean)
 #endif
@@ -504,6 +507,21 @@ struct Staged {
             if (lane == 0)
                 sm.warp_tot[sub & 1][warp] = run;
             __syncthreads();
+#if MT_STAGED_TOT_SHFL
+            // The warp totals scanned across the first kNW lanes (3 steps
+            // instead of 2 kNW combines per thread), in warp order.
+            Acc t = lane < kNW ? sm.warp_tot[sub & 1][lane] : ident;
+#pragma unroll
+            for (int d = 1; d < kNW; d <<= 1) {
+                const Acc y = __shfl_up_sync(kFull, t, d);
+                if (lane >= d)
+                    t = Op::apply(y, t);
+            }
+            Acc wpre = __shfl_sync(kFull, t, (warp + 31) & 31);
+            if (warp == 0)
+                wpre = ident;
+            const Acc agg = __shfl_sync(kFull, t, kNW - 1);
+#else
             Acc wpre = ident, agg = ident;
 #pragma unroll
             for (int w = 0; w < kNW; ++w) {
@@ -512,6 +530,7 @@ struct Staged {
                     wpre = Op::apply(wpre, t);
                 agg = Op::apply(agg, t);
             }
+#endif
             const Acc base0 = Op::apply(carry, wpre);
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
