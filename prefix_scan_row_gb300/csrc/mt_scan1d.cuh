@@ -22,19 +22,30 @@ namespace mt {
 constexpr int kScanItems = MT_SCAN1D_ITEMS;      // 16-byte chunks per thread per tile
 constexpr int kScanThreads = MT_SCAN1D_THREADS;  // threads per CTA
 
+#ifndef MT_SCAN1D_F64_RUN
+#define MT_SCAN1D_F64_RUN 13  // f64: chunks per thread run (one sub-tile)
+#endif
+
+// f64 scans run per-thread runs of consecutive chunks (Staged::tile_lean);
+// an odd run length puts the 8 lanes of each shared-memory wavefront on 8
+// different 16-byte bank groups.
+template <class S>
+static constexpr int items_of() {
+    return std::is_same<S, double>::value ? MT_SCAN1D_F64_RUN : kScanItems;
+}
 template <class S>
 static constexpr int sub_of() {
-    return sizeof(S) == 8 ? MT_SCAN1D_SUB8 : MT_SCAN1D_SUB;
+    return std::is_same<S, double>::value ? 1 : (sizeof(S) == 8 ? MT_SCAN1D_SUB8 : MT_SCAN1D_SUB);
 }
 
 template <class S, class Op>
 static cudaError_t launch_scan(const SegArgs &a, const Launch &L) {
-    return launch_staged<S, Op, kScanItems, sub_of<S>(), kScanThreads>(a, 0, L);
+    return launch_staged<S, Op, items_of<S>(), sub_of<S>(), kScanThreads>(a, 0, L);
 }
 
 template <class S>
 static constexpr int64_t tile_elems_of() {
-    return Staged<S, OpAdd, kScanItems, sub_of<S>(), kScanThreads>::kTE;
+    return Staged<S, OpAdd, items_of<S>(), sub_of<S>(), kScanThreads>::kTE;
 }
 
 template <class S>

@@ -157,8 +157,10 @@ def test_scratch_slots(lib):
     # 6144 elements per super-tile for i64
     assert f(6144, I64, 1) == 4 + 16 * 2
     assert f(6143, I64, 1) == 4 + 16 * 1
-    # u32 as i32; u64 and f64 as i64
-    assert f(12288, 5, 1) == 4 + 16 * 2 and f(6144, 6, 1) == f(6144, 7, 1) == 4 + 16 * 2
+    # u32 as i32; u64 as i64
+    assert f(12288, 5, 1) == 4 + 16 * 2 and f(6144, 6, 1) == 4 + 16 * 2
+    # f64: runs of 13 chunks per thread, 256 x 13 x 2 = 6656 elements per tile
+    assert f(6655, 7, 1) == 4 + 16 and f(6656, 7, 1) == 4 + 16 * 2
     # select: 8192 flags per tile
     assert f(1 << 28, I32, 2) == 4 + 16 * (1 << 15)
     assert f(1, I32, 2) == 4 + 16 * 1
