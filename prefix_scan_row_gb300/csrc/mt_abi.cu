@@ -38,19 +38,19 @@ __global__ void k_reset(uint64_t *words, int64_t nwords, const int32_t *n_dev, i
 }
 
 static int device_sm_count(int *dev_out) {
-    static int cache[128] = {0};
+    static PerDevice cache;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return 0;
     if (dev_out)
         *dev_out = dev;
-    if (cache[dev] == 0) {
-        int c = 0;
+    int c = cache.get(dev);
+    if (c == 0) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
-        cache[dev] = c;
+        cache.set(dev, c);
     }
-    return cache[dev];
+    return c;
 }
 
 static cudaError_t launch_reset(uint64_t *words, int64_t nwords, const int32_t *n_dev,
@@ -141,16 +141,18 @@ bool ptr_reachable(const void *p, int dev, bool *host) {
         return a.devicePointer == p;
     default: {  // unregistered host memory
         *host = true;
-        static int pageable[128] = {0};  // 0 unknown, 1 yes, 2 no
-        if (dev < 0 || dev >= 128)
+        static PerDevice pageable;  // 0 unknown, 1 yes, 2 no
+        if (dev < 0 || dev >= kMaxDevices)
             return false;
-        if (pageable[dev] == 0) {
+        int known = pageable.get(dev);
+        if (known == 0) {
             int v = 0;
             if (cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess)
                 v = 0;
-            pageable[dev] = v ? 1 : 2;
+            known = v ? 1 : 2;
+            pageable.set(dev, known);
         }
-        return pageable[dev] == 1;
+        return known == 1;
     }
     }
 }

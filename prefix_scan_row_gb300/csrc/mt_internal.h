@@ -5,7 +5,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace mt {
+
+constexpr int kMaxDevices = 128;
+
+// A value found once per device (an occupancy, an attribute) and read by any
+// host thread: 0 means not known yet; threads that race on the first call
+// compute and store the same value.
+struct PerDevice {
+    std::atomic<int> v[kMaxDevices];
+    int get(int dev) const { return v[dev].load(std::memory_order_relaxed); }
+    void set(int dev, int x) { v[dev].store(x, std::memory_order_relaxed); }
+};
 
 constexpr int kHeaderSlots = 4;              // scratch header: [0] tile counter, rest reserved
 constexpr uint32_t kDefaultSpin = 1u << 20;  // look-back polls before a waiter gives up

@@ -33,7 +33,7 @@ __global__ void k_noalloc_clear(int64_t nwords) {
 }
 
 static std::mutex g_noalloc_mu;
-static uint64_t *g_noalloc_ptr[128] = {};
+static uint64_t *g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
 // device (with that device current) and cached.
@@ -42,7 +42,7 @@ static cudaError_t noalloc_scratch(uint64_t **out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 128)
+    if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_ptr[dev] == nullptr) {

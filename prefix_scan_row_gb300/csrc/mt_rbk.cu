@@ -387,15 +387,16 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
 
 template <bool KF, bool VF>
 static cudaError_t launch_rbk(const RbkArgs &a, const Launch &L) {
-    static int per_sm[128] = {0};
+    static PerDevice per_sm;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 128)
+    if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     const int bytes = (int)sizeof(RbkSmem);
-    if (per_sm[dev] == 0) {
+    int blocks = per_sm.get(dev);
+    if (blocks == 0) {
         e = cudaFuncSetAttribute(k_reduce_by_key<KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
@@ -407,9 +408,10 @@ static cudaError_t launch_rbk(const RbkArgs &a, const Launch &L) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_reduce_by_key<KF, VF>, kRbkThreads, bytes);
         if (e != cudaSuccess)
             return e;
-        per_sm[dev] = b > 0 ? b : 1;
+        blocks = b > 0 ? b : 1;
+        per_sm.set(dev, blocks);
     }
-    e = launch_pdl(k_reduce_by_key<KF, VF>, (unsigned)(L.sm_count * per_sm[dev]), kRbkThreads, bytes,
+    e = launch_pdl(k_reduce_by_key<KF, VF>, (unsigned)(L.sm_count * blocks), kRbkThreads, bytes,
                    L.stream, a);
     note_launch();
     return e;

@@ -265,21 +265,23 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
 
 template <class S, class Op>
 static cudaError_t launch_reduce(const RedArgs &a, const Launch &L) {
-    static int per_sm[128] = {0};
+    static PerDevice per_sm;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 128)
+    if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (per_sm[dev] == 0) {
+    int blocks = per_sm.get(dev);
+    if (blocks == 0) {
         int b = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_reduce<S, Op>, kRedThreads, 0);
         if (e != cudaSuccess)
             return e;
-        per_sm[dev] = b > 0 ? b : 1;
+        blocks = b > 0 ? b : 1;
+        per_sm.set(dev, blocks);
     }
-    int64_t grid = (int64_t)L.sm_count * per_sm[dev];
+    int64_t grid = (int64_t)L.sm_count * blocks;
     if (grid > kRedMaxCtas)
         grid = kRedMaxCtas;
     e = launch_pdl(k_reduce<S, Op>, (unsigned)grid, kRedThreads, 0, L.stream, a);

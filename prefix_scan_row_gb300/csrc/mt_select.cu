@@ -345,15 +345,16 @@ int select_rec_slots() { return Status<uint32_t>::kSlots; }
 
 template <class VT>
 static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
-    static int per_sm[128] = {0};
+    static PerDevice per_sm;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 128)
+    if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     const int bytes = (int)sizeof(SelStagedSmem<VT>);
-    if (per_sm[dev] == 0) {
+    int blocks = per_sm.get(dev);
+    if (blocks == 0) {
         e = cudaFuncSetAttribute(k_select_staged<VT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
@@ -365,9 +366,10 @@ static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_staged<VT>, kThreads, bytes);
         if (e != cudaSuccess)
             return e;
-        per_sm[dev] = b > 0 ? b : 1;
+        blocks = b > 0 ? b : 1;
+        per_sm.set(dev, blocks);
     }
-    e = launch_pdl(k_select_staged<VT>, (unsigned)(L.sm_count * per_sm[dev]), kThreads, bytes, L.stream, a);
+    e = launch_pdl(k_select_staged<VT>, (unsigned)(L.sm_count * blocks), kThreads, bytes, L.stream, a);
     note_launch();
     return e;
 }
@@ -375,7 +377,6 @@ static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                           uint64_t *scratch, const int32_t *n_dev, int elem_bytes, bool aligned,
                           const Launch &L) {
-    static int per_sm = 0;
     if (aligned || elem_bytes == 8) {  // 8-byte elements: the caller checked the alignment
         SelArgs a;
         a.arr = arr;
@@ -390,12 +391,21 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
         a.lb.spin_limit = L.spin_limit;
         return elem_bytes == 8 ? launch_staged_select<uint64_t>(a, L) : launch_staged_select<uint32_t>(a, L);
     }
-    if (per_sm == 0) {
+    static PerDevice per_sm;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    int blocks = per_sm.get(dev);
+    if (blocks == 0) {
         int b = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select, kThreads, 0);
-        if (e != cudaSuccess)
-            return e;
-        per_sm = b > 0 ? b : 1;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select, kThreads, 0);
+        if (err != cudaSuccess)
+            return err;
+        blocks = b > 0 ? b : 1;
+        per_sm.set(dev, blocks);
     }
     SelArgs a;
     a.arr = arr;
@@ -408,7 +418,7 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
-    const cudaError_t e = launch_pdl(k_select, (unsigned)(L.sm_count * per_sm), kThreads, 0, L.stream, a);
+    const cudaError_t e = launch_pdl(k_select, (unsigned)(L.sm_count * blocks), kThreads, 0, L.stream, a);
     note_launch();
     return e;
 }

@@ -685,14 +685,15 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) k_scan_staged
 template <class S, class Op, int ITEMS, int SUB, int THREADS>
 static cudaError_t launch_staged(const SegArgs &a, int64_t max_ctas, const Launch &L) {
     using G = Staged<S, Op, ITEMS, SUB, THREADS>;
-    static int per_sm[128] = {0};
+    static PerDevice per_sm;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 128)
+    if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (per_sm[dev] == 0) {
+    int blocks = per_sm.get(dev);
+    if (blocks == 0) {
         e = cudaFuncSetAttribute(k_scan_staged<S, Op, ITEMS, SUB, THREADS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmemBytes);
         if (e != cudaSuccess)
@@ -709,9 +710,10 @@ static cudaError_t launch_staged(const SegArgs &a, int64_t max_ctas, const Launc
                                                           THREADS, G::kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        per_sm[dev] = b > 0 ? b : 1;
+        blocks = b > 0 ? b : 1;
+        per_sm.set(dev, blocks);
     }
-    int64_t grid = (int64_t)L.sm_count * per_sm[dev];
+    int64_t grid = (int64_t)L.sm_count * blocks;
     if (max_ctas > 0 && grid > max_ctas)
         grid = max_ctas;
     if (grid < 1)
