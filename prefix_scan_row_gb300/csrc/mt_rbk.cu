@@ -143,9 +143,12 @@ static_assert(offsetof(RbkSmem, csum) % 16 == 0 && offsetof(RbkSmem, ccnt) % 16 
 // One staged super-tile: valid elements [llo, lhi) ([0, kRbkTE) when FULL);
 // has_first: it holds the first element (a head whatever its key); has_last:
 // it holds the last one (which ends its run and gives num_runs).
+// n_live bounds every output index: a valid run index always lies below it,
+// and a prefix left incomplete by a look-back that gave up (the error word is
+// set then) must not send a write outside the outputs.
 template <bool KF, bool VF, bool FULL>
 __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t g, int llo, int lhi,
-                                         bool has_first, bool has_last) {
+                                         bool has_first, bool has_last, uint32_t n_live) {
     using P = Seg<VF>;
     using Op = SegOp<VF>;
     using St = Status<uint64_t>;
@@ -312,13 +315,13 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
                 run.s = h ? P::val(word(vv4, k)) : run.s + P::val(word(vv4, k));
             }
             const uint32_t r = run.c - 1u;
-            if (h)
+            if (h && r < n_live)
                 a.keys_out[r] = word(kk, k);
-            if ((e >> k) & 1u)
+            if (((e >> k) & 1u) && r < n_live)
                 a.vals_out[r] = P::bits(run.s);
         }
         if (has_last && c == c_last)
-            *a.num_runs = (int32_t)run.c;
+            *a.num_runs = (int32_t)(run.c <= n_live ? run.c : n_live);
     }
 }
 
@@ -378,9 +381,9 @@ __global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
         }
         phase ^= 1u;
         if (llo == 0 && lhi == (int)kRbkTE)
-            rbk_tile<KF, VF, true>(sm, a, g, 0, (int)kRbkTE, g == 0, t0 + kRbkTE == hi);
+            rbk_tile<KF, VF, true>(sm, a, g, 0, (int)kRbkTE, g == 0, t0 + kRbkTE == hi, (uint32_t)n);
         else
-            rbk_tile<KF, VF, false>(sm, a, g, llo, lhi, g == 0, t0 + lhi == hi);
+            rbk_tile<KF, VF, false>(sm, a, g, llo, lhi, g == 0, t0 + lhi == hi, (uint32_t)n);
         fence_proxy_async_smem();  // this thread's shared accesses precede the next bulk copies
     }
 }

@@ -6,9 +6,11 @@ record MT_ERR_LOOKBACK_TIMEOUT in the device error word and let the kernel
 finish; mt_scan_status() reports it, and the next call on the same context
 is correct again.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from checks import assert_rows_close, assert_scan_matches, assert_select_matches
 
@@ -79,3 +81,67 @@ def test_select_timeout_reported_then_recovers(mt):
     mt.mt_select(arr, fl, out, num, scratch, n_dev)
     assert mt.mt_scan_status() == 0
     assert_select_matches(out, num, vals, flags, n)
+
+
+@pytest.mark.parametrize("dtype", ["i64", "f64"])
+def test_scan_8byte_timeout_reported_then_recovers(mt, dtype):
+    """8-byte status records (i64), and the per-thread-run form that f64
+    tiles take, whose warp 0 looks back on its own."""
+    n = 1 << 20
+    if dtype == "i64":
+        arr_cpu = workloads.randint((n,), 4, 0, 1 << 20, "i64")
+    else:
+        arr_cpu = workloads.uniform64((n,), 4, -1.0, 1.0)
+    arr = arr_cpu.cuda()
+    try:
+        mt.mt_scan_debug_lookback(skip_publish_tile=3, spin_limit=4096)
+        _scan(mt, arr, n)
+        assert mt.mt_scan_status() == mt.MT_ERR_LOOKBACK_TIMEOUT
+    finally:
+        mt.mt_scan_debug_lookback(-1, 0)
+    out = _scan(mt, arr, n)
+    assert mt.mt_scan_status() == 0
+    assert_scan_matches(out, arr_cpu, n, dtype, "add")
+
+
+def test_select_wide_timeout_reported_then_recovers(mt):
+    n = 1 << 20
+    vals, flags = workloads.select_inputs(n, 0.5, seed=10)
+    arr, fl = vals.to(torch.float64).cuda(), flags.cuda()
+    out = torch.empty_like(arr)
+    num = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
+    n_dev = torch.tensor([n], dtype=torch.int32, device="cuda")
+    try:
+        mt.mt_scan_debug_lookback(skip_publish_tile=2, spin_limit=4096)
+        mt.mt_select_wide(arr, fl, out, num, scratch, n_dev)
+        assert mt.mt_scan_status() == mt.MT_ERR_LOOKBACK_TIMEOUT
+    finally:
+        mt.mt_scan_debug_lookback(-1, 0)
+    mt.mt_select_wide(arr, fl, out, num, scratch, n_dev)
+    assert mt.mt_scan_status() == 0
+    k = int(num.item())
+    want = vals.to(torch.float64)[flags.bool()]
+    assert k == want.numel()
+    assert torch.equal(out[:k].cpu().view(torch.int64), want.view(torch.int64))
+
+
+def test_reduce_by_key_timeout_reported_then_recovers(mt):
+    n = 1 << 20
+    keys, vals = workloads.runs(n, 8.0, 11, "i32", "i32")
+    k, v = keys.cuda(), vals.cuda()
+    ko, vo = torch.empty_like(k), torch.empty_like(v)
+    nr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_REDUCE_BY_KEY)
+    n_dev = torch.tensor([n], dtype=torch.int32, device="cuda")
+    try:
+        mt.mt_scan_debug_lookback(skip_publish_tile=4, spin_limit=4096)
+        mt.mt_reduce_by_key_add(k, v, ko, vo, nr, scratch, n_dev)
+        assert mt.mt_scan_status() == mt.MT_ERR_LOOKBACK_TIMEOUT
+    finally:
+        mt.mt_scan_debug_lookback(-1, 0)
+    mt.mt_reduce_by_key_add(k, v, ko, vo, nr, scratch, n_dev)
+    assert mt.mt_scan_status() == 0
+    want_k, want_v, r = oracle.reduce_by_key_add(keys, vals, n, "i32", "i32")
+    assert int(nr.item()) == r
+    assert np.array_equal(ko[:r].cpu().numpy(), want_k) and np.array_equal(vo[:r].cpu().numpy(), want_v)
