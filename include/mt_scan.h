@@ -6,7 +6,11 @@
  * (or managed) memory owned by the caller. `stream` is a cudaStream_t passed
  * as `void*`; NULL means the legacy default stream. Every call only enqueues
  * work on `stream` and returns without synchronising, except
- * mt_scan_status(), which synchronises the stream it is given.
+ * mt_scan_status(), which synchronises the stream it is given. The enqueueing
+ * calls may therefore be captured in a CUDA graph and replayed (mt_scan_rows
+ * on long rows then records its workspace allocation as a graph node).
+ * Calls on different streams, from any host threads, may run concurrently as
+ * long as they share no output or scratch buffer.
  *
  * Return codes are mt_status values. A negative code from an enqueueing call
  * means nothing was launched (argument errors) or a CUDA launch failed
