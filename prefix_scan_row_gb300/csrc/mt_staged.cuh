@@ -52,23 +52,14 @@ struct SegArgs {
 #ifndef MT_STAGED_PAIR_W8
 #define MT_STAGED_PAIR_W8 1  // the same for 8-byte types
 #endif
-#ifndef MT_STAGED_EARLY_LB
-#define MT_STAGED_EARLY_LB 0  // 1: look back before the scan
-#endif
 #ifndef MT_STAGED_EARLY_W4
 #define MT_STAGED_EARLY_W4 1  // early aggregate for 4-byte accumulators
 #endif
 #ifndef MT_STAGED_EARLY_W8
 #define MT_STAGED_EARLY_W8 1  // the same for 8-byte accumulators
 #endif
-#ifndef MT_STAGED_TOT_SHFL
-#define MT_STAGED_TOT_SHFL 1  // pass 1: warp totals scanned by shuffles
-#endif
 #ifndef MT_STAGED_LEAN_F64
 #define MT_STAGED_LEAN_F64 1  // f64: per-thread runs (tile_lean)
-#endif
-#ifndef MT_STAGED_LEAN_I64
-#define MT_STAGED_LEAN_I64 0  // the same for 64-bit integers (measured slower: memory bounds them)
 #endif
 
 template <class S, class Op, int ITEMS, int SUB, int THREADS>
@@ -89,10 +80,9 @@ struct Staged {
     static constexpr int V =
         (kPlanes == 1 && ITEMS % 2 == 0 && (sizeof(Acc) == 8 ? MT_STAGED_PAIR_W8 : MT_STAGED_PAIR_W4)) ? 2 : 1;
     // Types whose combines, not memory, bound the scan take tile_lean: on
-    // GB300 an f64 add issues at about 2 per clock per SM.
-    static constexpr bool kLean =
-        kPlanes == 1 && ((std::is_same<Acc, double>::value && MT_STAGED_LEAN_F64) ||
-                         (sizeof(Acc) == 8 && std::is_integral<Acc>::value && MT_STAGED_LEAN_I64));
+    // GB300 an f64 add issues at about 2 per clock per SM. (64-bit integers
+    // were measured slower in that form: memory bounds them.)
+    static constexpr bool kLean = kPlanes == 1 && std::is_same<Acc, double>::value && MT_STAGED_LEAN_F64;
     static constexpr int kRun = kChunks / THREADS;  // tile_lean: chunks per thread, consecutive
     static constexpr int kU = ITEMS / V;  // units per thread per sub-tile
     static constexpr int EU = V * E;      // elements per unit
@@ -214,31 +204,6 @@ struct Staged {
             const bool s = pair_swap();
             sts128(&sm.stage[2 * u + (s ? 1 : 0)], pick(s, w[1], w[0]));
             sts128(&sm.stage[2 * u + (s ? 0 : 1)], pick(s, w[0], w[1]));
-        }
-    }
-
-    // A unit's final values straight to global memory (the early look-back
-    // form): 16-byte stores for whole chunks when the output has the input's
-    // 16-byte phase, element stores otherwise.
-    template <bool FULL>
-    __device__ __forceinline__ static void store_unit(S *eo, bool aligned_io, int u, int llo, int lhi,
-                                                      const Acc (&x)[EU]) {
-#pragma unroll
-        for (int q = 0; q < V; ++q) {
-            const int c = V * u + q;
-            const int o = c * E;
-            Acc part[E];
-#pragma unroll
-            for (int k = 0; k < E; ++k)
-                part[k] = x[q * E + k];
-            if (aligned_io && (FULL || (o >= llo && o + E <= lhi))) {
-                st_v4(reinterpret_cast<uint4 *>(eo) + c, C::pack(part));
-            } else if (FULL || (o < lhi && o + E > llo)) {
-#pragma unroll
-                for (int k = 0; k < E; ++k)
-                    if (FULL || (o + k >= llo && o + k < lhi))
-                        C::store1(eo + o + k, part[k]);
-            }
         }
     }
 
@@ -462,15 +427,11 @@ struct Staged {
         }
 
         // Pass 1: sub-tiles in order with a running carry; keep each
-        // element's super-tile-local prefix in shared memory (or, with the
-        // early look-back, start from the super-tile's prefix and store final
-        // results). The early form saves pass 2's combine per element but
-        // exposes the look-back's latency: measured slower wherever memory
-        // bounds the kernel.
-        constexpr bool kEarlyLB = MT_STAGED_EARLY_LB && kEarly;
+        // element's super-tile-local prefix in shared memory. (Looking back
+        // first and storing final values from here saves pass 2's combine per
+        // element but exposes the look-back's latency: measured slower
+        // wherever memory bounds the kernel.)
         Acc carry = ident;
-        if constexpr (kEarlyLB)
-            carry = lookback_prefix<Acc, Op>(a.lb, g, first, agg_total, &sm.prefix[buf]);
 #pragma unroll 1
         for (int sub = 0; sub < SUB; ++sub) {
             Acc x[kU][EU];
@@ -507,7 +468,6 @@ struct Staged {
             if (lane == 0)
                 sm.warp_tot[sub & 1][warp] = run;
             __syncthreads();
-#if MT_STAGED_TOT_SHFL
             // The warp totals scanned across the first kNW lanes (3 steps
             // instead of 2 kNW combines per thread), in warp order.
             Acc t = lane < kNW ? sm.warp_tot[sub & 1][lane] : ident;
@@ -521,16 +481,6 @@ struct Staged {
             if (warp == 0)
                 wpre = ident;
             const Acc agg = __shfl_sync(kFull, t, kNW - 1);
-#else
-            Acc wpre = ident, agg = ident;
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                const Acc t = sm.warp_tot[sub & 1][w];
-                if (w < warp)
-                    wpre = Op::apply(wpre, t);
-                agg = Op::apply(agg, t);
-            }
-#endif
             const Acc base0 = Op::apply(carry, wpre);
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
@@ -545,15 +495,10 @@ struct Staged {
                         x[j][k] = Op::apply(base, x[j][k - 1]);
                     x[j][0] = base;
                 }
-                if constexpr (kEarlyLB)
-                    store_unit<FULL>(eo, a.aligned_io != 0, unit_of(sub, j), llo, lhi, x[j]);
-                else
-                    put_unit(sm, unit_of(sub, j), x[j]);
+                put_unit(sm, unit_of(sub, j), x[j]);
             }
             carry = Op::apply(carry, agg);
         }
-        if constexpr (kEarlyLB)
-            return;
 
         if constexpr (!kEarly) {
             agg_total = carry;

@@ -15,10 +15,6 @@
 
 #include "mt_lookback.cuh"
 
-#ifndef MT_ROWS_TOT_SHFL
-#define MT_ROWS_TOT_SHFL 1  // the warp totals scanned by shuffles (0: a serial fold per warp)
-#endif
-
 namespace mt {
 
 template <class S, class Op, int ITEMS>
@@ -115,7 +111,6 @@ struct RowTile {
         __syncthreads();
 
         // This warp's exclusive prefix: the totals of the warps before it.
-#if MT_ROWS_TOT_SHFL
         const int nw = (int)(blockDim.x >> 5);
         Acc t = lane < nw ? sm.warp_tot[lane] : ident;
 #pragma unroll
@@ -127,11 +122,6 @@ struct RowTile {
         Acc wpre = __shfl_sync(kFull, t, (warp + 31) & 31);
         if (warp == 0)
             wpre = ident;
-#else
-        Acc wpre = ident;
-        for (int w = 0; w < warp; ++w)
-            wpre = Op::apply(wpre, sm.warp_tot[w]);
-#endif
 
         // Outputs: inclusive base + s_k, or exclusive base + s_{k-1} with base
         // itself at k = 0 (the one-slot shift of scan.rs's exclusive kernel).
