@@ -14,15 +14,15 @@
 // run -- and the tile scans pairs with the segmented operator
 //   (c1, s1) + (c2, s2) = (c1 + c2, c2 != 0 ? s2 : s1 + s2),
 // whose inclusive prefix at an element is (runs started so far, sum of the
-// open run). Super-tiles of 4096 keys and values arrive in shared memory by
-// bulk copies. A first pass over the 16-byte chunks (consecutive lanes,
-// consecutive chunks: no bank conflicts) finds each chunk's head bits and its
-// own pair; each thread then folds the pairs of 4 consecutive chunks, so one
-// pair per thread enters the warp and block scans; the super-tile's own pair
-// is published as soon as that scan is done; warp 0 then looks back for the
-// pairs of all earlier super-tiles (packed in 64 bits); every chunk's prefix
-// goes back to shared memory, and a second chunk pass writes the results:
-// heads keys_out[c - 1], run ends values_out[c - 1]. No atomics
+// open run). Super-tiles of 6144 keys and values arrive in shared memory by
+// bulk copies. Each thread owns units of 8 consecutive elements (two 16-byte
+// chunks, read in an order that keeps shared memory free of bank conflicts):
+// a first pass finds each unit's head bits and its pair, warp scans and a
+// scan of the warp totals give every unit its prefix inside the super-tile,
+// the super-tile's pair is published at once, and warp 0 looks back for the
+// pairs of all earlier super-tiles (packed in 64 bits). A second pass over
+// the units writes the results: heads keys_out[c - 1], run ends
+// values_out[c - 1]. No atomics
 // on the outputs, and sums are added in a fixed order.
 #include <cstddef>
 #include <type_traits>
@@ -32,18 +32,15 @@
 namespace mt {
 
 #ifndef MT_RBK_TILE
-#define MT_RBK_TILE 4096  // elements per super-tile: 4096 or 8192
+#define MT_RBK_TILE 6144  // elements per super-tile (a multiple of 2048)
 #endif
-#ifndef MT_RBK_THREADS
-#define MT_RBK_THREADS 256
-#endif
-constexpr int kRbkThreads = MT_RBK_THREADS;
-constexpr int kRbkSeg = 16;                                       // consecutive elements per thread segment
-constexpr int kRbkSub = MT_RBK_TILE / (kRbkThreads * kRbkSeg);    // segments per thread per super-tile
-static_assert(kRbkSub >= 1 && kRbkSub * kRbkThreads * kRbkSeg == MT_RBK_TILE, "super-tile shape");
-constexpr int kRbkSubElems = kRbkThreads * kRbkSeg;               // elements per sub-tile (4096)
-constexpr int64_t kRbkTE = (int64_t)kRbkSub * kRbkSubElems;       // elements per super-tile (4096)
+constexpr int kRbkThreads = 256;
+constexpr int kRbkUnitElems = 8;                                  // a unit: two adjacent 16-byte chunks
+constexpr int kRbkSub = MT_RBK_TILE / (kRbkThreads * kRbkUnitElems);  // units per thread per super-tile
+static_assert(kRbkSub >= 1 && kRbkSub * kRbkThreads * kRbkUnitElems == MT_RBK_TILE, "super-tile shape");
+constexpr int64_t kRbkTE = MT_RBK_TILE;                           // elements per super-tile
 constexpr int kRbkChunks = (int)(kRbkTE / 4);                     // 16-byte chunks per super-tile
+constexpr int kRbkUnits = (int)(kRbkTE / kRbkUnitElems);          // units per super-tile
 
 struct RbkArgs {
     const char *keys;   // keys and values share their 16-byte phase
@@ -119,37 +116,52 @@ __device__ __forceinline__ uint32_t word(const uint4 &v, int k) {
 }
 
 // Shared state of one CTA: the super-tile's keys and values (bulk-copied),
-// the keys just before and after it, and the block's scratch.
+// the keys just before and after it, each unit's head bits, and the block's
+// scratch.
 struct RbkSmem {
     uint4 keys[kRbkChunks];
     uint4 vals[kRbkChunks];
-    uint32_t csum[kRbkChunks]; // per chunk: its own open-run sum, then the sum part of its prefix
-    uint32_t ccnt[kRbkChunks]; // per chunk: the count part of its prefix
-    uint8_t heads[kRbkChunks]; // head bits of each chunk (bit k: its element k)
+    uint8_t heads[kRbkUnits];  // head bits of each unit (bit k: its element k)
     uint64_t bar;
     unsigned long long tile;
     uint32_t kprev, knext;     // the neighbours' keys (when they exist)
-    uint32_t warp_c[kRbkSub][kRbkThreads / 32];  // warp totals of the segment scan
+    uint32_t warp_c[kRbkSub][kRbkThreads / 32];  // warp totals of each sub-tile's scan
     uint32_t warp_s[kRbkSub][kRbkThreads / 32];
-    uint32_t wex_c[kRbkSub][kRbkThreads / 32];   // and the warps' exclusive prefixes
-    uint32_t wex_s[kRbkSub][kRbkThreads / 32];
     uint64_t prefix;
 };
-// csum and ccnt are read and written 16 bytes at a time, heads 4 at a time
-static_assert(offsetof(RbkSmem, csum) % 16 == 0 && offsetof(RbkSmem, ccnt) % 16 == 0 &&
-                  offsetof(RbkSmem, heads) % 4 == 0 && offsetof(RbkSmem, bar) % 8 == 0,
-              "shared-memory layout of the reduce-by-key kernel");
+static_assert(offsetof(RbkSmem, bar) % 8 == 0, "shared-memory layout of the reduce-by-key kernel");
+
+// Unit u (chunks 2u and 2u + 1) of a staged array. Lanes 4-7 of every group
+// of 8 read the second chunk first, so the 8 lanes that share a wavefront
+// touch 8 different 16-byte bank groups.
+__device__ __forceinline__ void load_unit(const uint4 *base, int u, uint4 &c0, uint4 &c1) {
+    const bool sw = (threadIdx.x >> 2) & 1;
+    const uint4 p = lds128(&base[2 * u + (sw ? 1 : 0)]);
+    const uint4 q = lds128(&base[2 * u + (sw ? 0 : 1)]);
+    c0 = sw ? q : p;
+    c1 = sw ? p : q;
+}
+__device__ __forceinline__ uint32_t word8(const uint4 &c0, const uint4 &c1, int k) {
+    return k < 4 ? word(c0, k) : word(c1, k - 4);
+}
 
 // One staged super-tile: valid elements [llo, lhi) ([0, kRbkTE) when FULL);
 // has_first: it holds the first element (a head whatever its key); has_last:
-// it holds the last one (which ends its run and gives num_runs).
-// n_live bounds every output index: a valid run index always lies below it,
-// and a prefix left incomplete by a look-back that gave up (the error word is
-// set then) must not send a write outside the outputs.
+// it holds the last one (which ends its run and gives num_runs). n_live
+// bounds every output index: a valid run index always lies below it, and a
+// prefix left incomplete by a look-back that gave up (the error word is set
+// then) must not send a write outside the outputs.
+//
+// Thread t owns unit s * 256 + t of sub-tile s. Pass 1 finds each unit's
+// head bits and its pair (heads, sum of the open run), and scans the pairs
+// (warps by shuffles, then the warp totals across lanes, sub-tiles in
+// order); warp 0 publishes the super-tile's pair and looks back. Pass 2
+// reads each unit again and writes its outputs from the unit's full prefix.
 template <bool KF, bool VF, bool FULL>
 __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t g, int llo, int lhi,
                                          bool has_first, bool has_last, uint32_t n_live) {
     using P = Seg<VF>;
+    using V = typename P::V;
     using Op = SegOp<VF>;
     using St = Status<uint64_t>;
     constexpr int kNW = kRbkThreads / 32;
@@ -157,60 +169,37 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
     const uint32_t *skey = reinterpret_cast<const uint32_t *>(sm.keys);
     const uint32_t kprev = sm.kprev, knext = sm.knext;
 
-    // Pass A, chunk by chunk (consecutive lanes, consecutive 16-byte chunks:
-    // no bank conflicts): head bits and the sum of the chunk's open run. The
-    // key before a chunk is the last key of the lane to the left.
-#pragma unroll 1
-    for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
-        const uint4 kk = lds128(&sm.keys[c]);
-        const uint4 vv4 = lds128(&sm.vals[c]);
-        uint32_t prev = __shfl_up_sync(kFull, kk.w, 1);
-        if (lane == 0)
-            prev = (4 * c - 1 >= llo) ? skey[4 * c - 1] : kprev;
-        uint32_t m = 0u;
-        typename P::V sum = typename P::V(0);
+    // Pass 1. The key before a unit is the last key of the lane to the left.
+    uint32_t mh[kRbkSub];
+    P ex[kRbkSub];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = 4 * c + k;
-            const uint32_t key = word(kk, k);
+    for (int s = 0; s < kRbkSub; ++s) {
+        const int u = s * kRbkThreads + threadIdx.x;
+        uint4 k0, k1, v0, v1;
+        load_unit(sm.keys, u, k0, k1);
+        load_unit(sm.vals, u, v0, v1);
+        uint32_t prev = __shfl_up_sync(kFull, k1.w, 1);
+        if (lane == 0)
+            prev = (8 * u - 1 >= llo) ? skey[8 * u - 1] : kprev;
+        uint32_t m = 0u;
+        V sum = V(0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = 8 * u + k;
+            const uint32_t key = word8(k0, k1, k);
             if (FULL || (i >= llo && i < lhi)) {
                 // the first element starts a run whatever its key
-                const bool first = has_first && (FULL ? (k == 0 && c == 0) : i == llo);
+                const bool first = has_first && (FULL ? (k == 0 && u == 0) : i == llo);
                 const bool h = first || keys_differ<KF>(key, prev);
                 m |= (h ? 1u : 0u) << k;
-                const typename P::V v = P::val(word(vv4, k));
+                const V v = P::val(word8(v0, v1, k));
                 sum = h ? v : sum + v;
             }
             prev = key;
         }
-        sm.heads[c] = (uint8_t)m;
-        sm.csum[c] = P::bits(sum);
-    }
-    __syncthreads();
-
-    // Each thread owns segments of 4 consecutive chunks (16 elements): their
-    // pairs from the chunk pairs, in order.
-    P seg[kRbkSub], cpre[kRbkSub][4];
-#pragma unroll
-    for (int sub = 0; sub < kRbkSub; ++sub) {
-        const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
-        const uint32_t m4 = *reinterpret_cast<const uint32_t *>(&sm.heads[c0]);
-        const uint4 s4 = lds128(reinterpret_cast<const uint4 *>(&sm.csum[c0]));
-        P acc = P::ident();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            cpre[sub][q] = acc;
-            acc = P::apply(acc, P{(uint32_t)__popc((m4 >> (8 * q)) & 0xffu), P::val(word(s4, q))});
-        }
-        seg[sub] = acc;
-    }
-
-    // The segments' exclusive prefixes in order (sub-tile, then thread):
-    // warp scans; warp 0 scans the warp totals.
-    P ex[kRbkSub];
-#pragma unroll
-    for (int sub = 0; sub < kRbkSub; ++sub) {
-        P inc = seg[sub];
+        sm.heads[u] = (uint8_t)m;
+        mh[s] = m;
+        P inc{(uint32_t)__popc(m), sum};
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const P y = inc.shfl_up(d);
@@ -220,39 +209,38 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
         P e = inc.shfl_up(1);
         if (lane == 0)
             e = P::ident();
-        ex[sub] = e;
+        ex[s] = e;
         if (lane == 31) {
-            sm.warp_c[sub][warp] = inc.c;
-            sm.warp_s[sub][warp] = P::bits(inc.s);
+            sm.warp_c[s][warp] = inc.c;
+            sm.warp_s[s][warp] = P::bits(inc.s);
         }
     }
-    __syncthreads();  // warp totals are written
+    __syncthreads();  // warp totals and head bits are written
 
-    // Warp 0: the warps' exclusive prefixes, the super-tile's pair (published
-    // at once), the look-back, the inclusive prefix.
-    if (warp == 0) {
-        P agg = P::ident();
+    // Each unit's prefix inside the super-tile: the warp totals of each
+    // sub-tile scanned across the first kNW lanes, sub-tiles in order.
+    P base[kRbkSub];
+    P carry = P::ident();
 #pragma unroll
-        for (int sub = 0; sub < kRbkSub; ++sub) {
-            P w = lane < kNW ? P{sm.warp_c[sub][lane], P::val(sm.warp_s[sub][lane])} : P::ident();
+    for (int s = 0; s < kRbkSub; ++s) {
+        P t = lane < kNW ? P{sm.warp_c[s][lane], P::val(sm.warp_s[s][lane])} : P::ident();
 #pragma unroll
-            for (int d = 1; d < kNW; d <<= 1) {
-                const P y = w.shfl_up(d);
-                if (lane >= d)
-                    w = P::apply(y, w);
-            }
-            P we = w.shfl_up(1);
-            if (lane == 0)
-                we = P::ident();
-            const P tot = w.shfl(kNW - 1);
-            if (lane < kNW) {
-                const P before = P::apply(agg, we);
-                sm.wex_c[sub][lane] = before.c;
-                sm.wex_s[sub][lane] = P::bits(before.s);
-            }
-            agg = P::apply(agg, tot);
+        for (int d = 1; d < kNW; d <<= 1) {
+            const P y = t.shfl_up(d);
+            if (lane >= d)
+                t = P::apply(y, t);
         }
-        const uint64_t aggp = ((uint64_t)agg.c << 32) | P::bits(agg.s);
+        P wpre = t.shfl((warp + 31) & 31);
+        if (warp == 0)
+            wpre = P::ident();
+        base[s] = P::apply(P::apply(carry, wpre), ex[s]);
+        carry = P::apply(carry, t.shfl(kNW - 1));
+    }
+
+    // Warp 0: the super-tile's pair (published at once), the look-back, the
+    // inclusive prefix.
+    if (warp == 0) {
+        const uint64_t aggp = ((uint64_t)carry.c << 32) | P::bits(carry.s);
         publish_aggregate<uint64_t, Op>(a.lb, g, 0, aggp);
         uint64_t pre = 0;  // the identity pair
         if (a.lb.recs != nullptr && g != 0) {
@@ -263,70 +251,63 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
         if (lane == 0)
             sm.prefix = pre;
     }
-    __syncthreads();
-
-    // Every chunk's prefix, written back by the segment's owner.
-    const P tp = P::unpack(sm.prefix);
-#pragma unroll
-    for (int sub = 0; sub < kRbkSub; ++sub) {
-        const int c0 = 4 * (sub * kRbkThreads + threadIdx.x);
-        const P base = P::apply(P::apply(tp, P{sm.wex_c[sub][warp], P::val(sm.wex_s[sub][warp])}), ex[sub]);
-        const P q0 = P::apply(base, cpre[sub][0]), q1 = P::apply(base, cpre[sub][1]);
-        const P q2 = P::apply(base, cpre[sub][2]), q3 = P::apply(base, cpre[sub][3]);
-        sts128(reinterpret_cast<uint4 *>(&sm.csum[c0]),
-               make_uint4(P::bits(q0.s), P::bits(q1.s), P::bits(q2.s), P::bits(q3.s)));
-        sts128(reinterpret_cast<uint4 *>(&sm.ccnt[c0]), make_uint4(q0.c, q1.c, q2.c, q3.c));
-    }
     // Does the super-tile's last element end its run?
     const bool last_ends = lhi > llo && (has_last || keys_differ<KF>(knext, skey[lhi - 1]));
-    const int c_last = (lhi - 1) >> 2;  // the chunk of the last valid element
+    const int u_last = (lhi - 1) >> 3;  // the unit of the last valid element
     __syncthreads();
+    const P tp = P::unpack(sm.prefix);
 
-    // Pass B, chunk by chunk again: heads write their key, run ends the
-    // run's sum, at run index c - 1.
-#pragma unroll 1
-    for (int c = threadIdx.x; c < kRbkChunks; c += kRbkThreads) {
-        const uint32_t m = sm.heads[c];
+    // Pass 2: heads write their key, run ends the run's sum, at run index
+    // c - 1.
+#pragma unroll
+    for (int s = 0; s < kRbkSub; ++s) {
+        const int u = s * kRbkThreads + threadIdx.x;
+        const uint32_t m = mh[s];
         uint32_t e;  // element k ends a run: k + 1 starts one, or k is the last
         if (FULL) {
-            const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : (last_ends ? 1u : 0u);
-            e = (m >> 1) | ((mn & 1u) << 3);
+            const uint32_t mn = (u + 1 < kRbkUnits) ? sm.heads[u + 1] : (last_ends ? 1u : 0u);
+            e = (m >> 1) | ((mn & 1u) << 7);
         } else {
-            const uint32_t mn = (c + 1 < kRbkChunks) ? sm.heads[c + 1] : 0u;
-            e = (m >> 1) | ((mn & 1u) << 3);
-            const int li = lhi - 1 - 4 * c;
-            if (li >= 0 && li < 4)
+            const uint32_t mn = (u + 1 < kRbkUnits) ? sm.heads[u + 1] : 0u;
+            e = (m >> 1) | ((mn & 1u) << 7);
+            const int li = lhi - 1 - 8 * u;
+            if (li >= 0 && li < 8)
                 e = (e & ((1u << li) - 1u)) | ((last_ends ? 1u : 0u) << li);
             else if (li < 0)
                 e = 0u;
-            const int lv = llo - 4 * c;  // elements before the first valid one end nothing
+            const int lv = llo - 8 * u;  // elements before the first valid one end nothing
             if (lv > 0)
-                e &= lv >= 4 ? 0u : ~((1u << lv) - 1u);
+                e &= lv >= 8 ? 0u : ~((1u << lv) - 1u);
         }
-        const uint4 vv4 = lds128(&sm.vals[c]);
-        const uint4 kk = lds128(&sm.keys[c]);
-        P run{sm.ccnt[c], P::val(sm.csum[c])};
+        uint4 k0, k1, v0, v1;
+        load_unit(sm.keys, u, k0, k1);
+        load_unit(sm.vals, u, v0, v1);
+        P run = P::apply(tp, base[s]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = 4 * c + k;
+        for (int k = 0; k < 8; ++k) {
+            const int i = 8 * u + k;
             const bool h = (m >> k) & 1u;
             if (FULL || (i >= llo && i < lhi)) {
+                const V v = P::val(word8(v0, v1, k));
                 run.c += h ? 1u : 0u;
-                run.s = h ? P::val(word(vv4, k)) : run.s + P::val(word(vv4, k));
+                run.s = h ? v : run.s + v;
             }
             const uint32_t r = run.c - 1u;
             if (h && r < n_live)
-                a.keys_out[r] = word(kk, k);
+                a.keys_out[r] = word8(k0, k1, k);
             if (((e >> k) & 1u) && r < n_live)
                 a.vals_out[r] = P::bits(run.s);
         }
-        if (has_last && c == c_last)
+        if (has_last && u == u_last)
             *a.num_runs = (int32_t)(run.c <= n_live ? run.c : n_live);
     }
 }
 
+#ifndef MT_RBK_MINB
+#define MT_RBK_MINB 0  // resident CTAs per SM asked of the compiler (0: no bound)
+#endif
 template <bool KF, bool VF>
-__global__ void __launch_bounds__(kRbkThreads) k_reduce_by_key(RbkArgs a) {
+__global__ void __launch_bounds__(kRbkThreads, MT_RBK_MINB) k_reduce_by_key(RbkArgs a) {
     pdl_prologue();
     extern __shared__ __align__(128) unsigned char dsm[];
     RbkSmem &sm = *reinterpret_cast<RbkSmem *>(dsm);

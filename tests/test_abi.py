@@ -167,8 +167,8 @@ def test_scratch_slots(lib):
     # reduce: a header and one partial slot per CTA, whatever the capacity
     assert f(1 << 28, I32, 3) == f(0, F32, 3) == f(5, I64, 3) == f(7, 7, 3) == 4 + 2 * 4096
     assert f(10, BF16, 3) == -1
-    # reduce by key: 4096 elements per super-tile (plus up to 3 of head phase)
-    assert f(4093, 0, 4) == 4 + 16 and f(4094, 0, 4) == 4 + 32 and f(0, 0, 4) == 4
+    # reduce by key: 6144 elements per super-tile (plus up to 3 of head phase)
+    assert f(6141, 0, 4) == 4 + 16 and f(6142, 0, 4) == 4 + 32 and f(0, 0, 4) == 4
 
 
 def test_strerror_and_counter(lib):
