@@ -283,28 +283,38 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
         load_unit(sm.keys, u, k0, k1);
         load_unit(sm.vals, u, v0, v1);
         P run = P::apply(tp, base[s]);
+        // The unit's run indices lie in [run.c - 1, run.c + popc(m) - 1]: when
+        // that range is inside [0, n_live) no store needs its own check.
+        const bool inside = run.c >= 1u && run.c + (uint32_t)__popc(m) <= n_live;
+        auto outputs = [&](auto checked) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = 8 * u + k;
-            const bool h = (m >> k) & 1u;
-            if (FULL || (i >= llo && i < lhi)) {
-                const V v = P::val(word8(v0, v1, k));
-                run.c += h ? 1u : 0u;
-                run.s = h ? v : run.s + v;
+            for (int k = 0; k < 8; ++k) {
+                const int i = 8 * u + k;
+                const bool h = (m >> k) & 1u;
+                if (FULL || (i >= llo && i < lhi)) {
+                    const V v = P::val(word8(v0, v1, k));
+                    run.c += h ? 1u : 0u;
+                    run.s = h ? v : run.s + v;
+                }
+                const uint32_t r = run.c - 1u;
+                const bool ok = !decltype(checked)::value || r < n_live;
+                if (h && ok)
+                    a.keys_out[r] = word8(k0, k1, k);
+                if (((e >> k) & 1u) && ok)
+                    a.vals_out[r] = P::bits(run.s);
             }
-            const uint32_t r = run.c - 1u;
-            if (h && r < n_live)
-                a.keys_out[r] = word8(k0, k1, k);
-            if (((e >> k) & 1u) && r < n_live)
-                a.vals_out[r] = P::bits(run.s);
-        }
+        };
+        if (inside)
+            outputs(std::false_type{});
+        else
+            outputs(std::true_type{});
         if (has_last && u == u_last)
             *a.num_runs = (int32_t)(run.c <= n_live ? run.c : n_live);
     }
 }
 
 #ifndef MT_RBK_MINB
-#define MT_RBK_MINB 0  // resident CTAs per SM asked of the compiler (0: no bound)
+#define MT_RBK_MINB 4  // resident CTAs per SM asked of the compiler (64 registers)
 #endif
 template <bool KF, bool VF>
 __global__ void __launch_bounds__(kRbkThreads, MT_RBK_MINB) k_reduce_by_key(RbkArgs a) {
