@@ -447,7 +447,24 @@ def run_suite(args):
     def wanted(name):
         return args.only is None or any(o in name for o in args.only.split("|"))
 
-    def timeit(name, fn, nbytes, elems, reps=20):
+    def sustained(fns, nbytes, rounds=20):
+        """Back-to-back calls rotating over buffer sets that together exceed
+        twice the L2, between one event pair: the throughput of a stream of
+        calls, each launch overlapping its neighbours' ramp and drain."""
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(rounds):
+            for f in fns:
+                f()
+        b.record()
+        b.synchronize()
+        ms = a.elapsed_time(b) / (rounds * len(fns))
+        return nbytes / (ms / 1e3) / 1e9
+
+    def timeit(name, fn, nbytes, elems, reps=20, rotate=None):
         if not wanted(name):
             return
         small = nbytes < 2 * L2_BYTES
@@ -475,6 +492,10 @@ def run_suite(args):
              "frac_measured": round(gbs / peak, 3), "frac_datasheet_8000_gbs": round(gbs / 8000.0, 3),
              "Gelem/s": round(elems / (med / 1e3) / 1e9, 2),
              "l2_flushed": small, "host_enqueue_hidden": True}
+        if rotate is not None:
+            sg = sustained(rotate, nbytes)
+            r.update({"back_to_back_GB/s": round(sg, 1), "back_to_back_frac_measured": round(sg / peak, 3),
+                      "back_to_back_buffer_sets": len(rotate)})
         rows_out.append(r)
         print(json.dumps(r), flush=True)
 
@@ -489,10 +510,14 @@ def run_suite(args):
             continue
         x = (workloads.rows_f32(r, n) if d == "f32" else workloads.rows_half(r, n, d)).to(dev)
         o = torch.empty_like(x)
+        sets = -(-2 * L2_BYTES // call_bytes(r, n, d))  # buffer sets for the back-to-back figure
+        xs = [x] + [x.clone() for _ in range(sets - 1)]
+        os_ = [o] + [torch.empty_like(x) for _ in range(sets - 1)]
         for inc in incs:
             timeit(f"{name} {'incl' if inc else 'excl'}", lambda: mt.mt_scan_rows(x, o, inc),
-                   call_bytes(r, n, d), r * n)
-        del x, o
+                   call_bytes(r, n, d), r * n,
+                   rotate=[lambda xi=xi, oi=oi: mt.mt_scan_rows(xi, oi, inc) for xi, oi in zip(xs, os_)])
+        del x, o, xs, os_
     # the product / max / min row scans on the same shapes
     for name, (r, n, d), inc in [
             ("rows_op {} f32 [1024,4096] incl", (1024, 4096, "f32"), True),
