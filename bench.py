@@ -15,8 +15,9 @@ Printed: one JSON line (rank 0). Besides the device-timed value it carries
 `e2e` (the same metric through the C ABI with host buffers: pinned host ->
 device copy, the four calls, device -> host copy, every step), `roofline` for
 the dominant kernel (the [8192, 8192] bf16 launch), `cpu_baseline` (the CPU
-oracle, single-threaded, on a bounded sample), `clocks` sampled during the
-timed region and `gpu_launches` counted by the library.
+oracle, single-threaded, on a bounded sample), `cpu_all_cores` (an all-core
+C row scan on the host, a second baseline), `clocks` sampled during the timed
+region and `gpu_launches` counted by the library.
 
 `--impl reference` times the CPU oracle instead (the only reference this
 library has), on the same workload, metric and unit.
@@ -247,6 +248,26 @@ def cpu_baseline(host, target_s=12.0):
                       f"({elems} elements, {nbytes} algorithmic bytes), plain C, 1 thread"}
 
 
+def cpu_all_cores(host, reps=5):
+    """A second CPU baseline: the step's four row scans by an all-core C scan
+    (pthreads, f32 accumulation; oracle/mt_cpu_allcore.c), median of `reps`
+    whole steps. Not the oracle, and not a target."""
+    from oracle import allcore
+    cores = allcore.cores()
+    outs = [None] * len(host)
+    times = []
+    for _ in range(reps + 1):
+        t0 = time.perf_counter()
+        for i, (h, (_, r, n, d, inc)) in enumerate(zip(host, CALLS)):
+            outs[i] = allcore.scan_rows(h, d, inc, cores, out=outs[i])
+        times.append(time.perf_counter() - t0)
+    secs = statistics.median(times[1:])  # the first pass pages the buffers in
+    return {"value": STEP_BYTES / secs / 1e9, "unit": UNIT, "cores": cores,
+            "kind": "all-core C row scan (pthreads, f32 accumulation); a baseline, not the oracle",
+            "elements_per_s": STEP_ELEMS / secs, "seconds_per_step": round(secs, 4),
+            "sample": f"the whole step (4 tensors, {STEP_ELEMS} elements), median of {reps}"}
+
+
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
@@ -388,6 +409,7 @@ def run_ours(args, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host)
+        line["cpu_all_cores"] = cpu_all_cores(host)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
