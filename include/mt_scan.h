@@ -266,9 +266,10 @@ int mt_reduce_by_key_add(const void *keys_in, const void *values_in, void *keys_
 /*
  * mt_scan_scratch_slots -- number of 8-byte scratch slots that
  * mt_exclusive_scan / mt_inclusive_scan (kind MT_SCRATCH_SCAN, with their
- * dtype), mt_select (kind MT_SCRATCH_SELECT, dtype ignored) or mt_reduce
- * (kind MT_SCRATCH_REDUCE, with its dtype; the same size for every
- * capacity) needs for any live count up to `capacity`. Plain host
+ * dtype), mt_select / mt_select_wide (kind MT_SCRATCH_SELECT, dtype
+ * ignored), mt_reduce (kind MT_SCRATCH_REDUCE, with its dtype; the same size
+ * for every capacity) or mt_reduce_by_key_add (kind MT_SCRATCH_REDUCE_BY_KEY,
+ * dtype ignored) needs for any live count up to `capacity`. Plain host
  * arithmetic, no device access ([algos] "Scratch space": ask first, then
  * allocate). Returns -1 for a negative capacity or an unknown kind/dtype.
  */
