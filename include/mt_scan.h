@@ -140,13 +140,13 @@ int mt_scan_rows_op(const void *inp, void *out, int64_t rows, int64_t n, int dty
  * left-to-right loop. Inputs are assumed NaN-free (NaN order is unspecified).
  *
  * arr, out : device arrays of `dtype`, aligned to the element size: MT_I32,
- *            MT_I64 or MT_F32, and the rest of [algos]'s list ("the new
- *            functional API covers {i32, u32, f32, i64, u64, f64}"): MT_U32
- *            and MT_U64 (add wraps; min/max compare as unsigned, identities
+ *            MT_I64 or MT_F32, and the other dtypes [algos] lists for its
+ *            scans ("qd.algorithms.PrefixSumExecutor": i32, u32, f32, i64,
+ *            u64 and f64): MT_U32 and MT_U64 (add wraps; min/max compare as unsigned, identities
  *            UINT_MAX and 0) and MT_F64 (as f32: identities +-inf, earliest
  *            element on ties, sums grouped differently from a left-to-right
- *            loop). out must not be arr ([algos]: "No in-place scan") ->
- *            MT_ERR_ALIAS; other overlaps are undefined.
+ *            loop). out must not be arr ([algos] forbids scanning in place,
+ *            "Semantics") -> MT_ERR_ALIAS; other overlaps are undefined.
  * scratch  : device memory of at least
  *            mt_scan_scratch_slots(capacity, dtype, MT_SCRATCH_SCAN) 8-byte
  *            slots, 16-byte aligned. It needs no initialisation ([algos]

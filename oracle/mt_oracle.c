@@ -293,8 +293,8 @@ int oracle_scan_rows_op(const void *inp, void *out, double *prefix64, int64_t ro
 }
 
 /* ------------------------------------------------------------------------
- * The 1-D scans for the unsigned and f64 dtypes of [algos] ("the new
- * functional API covers {i32, u32, f32, i64, u64, f64}"): the recurrence
+ * The 1-D scans for the unsigned and f64 dtypes that [algos] lists beside
+ * i32, i64 and f32 (section "qd.algorithms.PrefixSumExecutor"): the recurrence
  * lp[0] = identity, lp[i+1] = op(lp[i], x[i]); the exclusive form stores
  * lp[i], the inclusive one lp[i+1]. For f64 add, `prefix64` / `abs64` (when
  * non-null) receive the long double prefix rounded to double and the running

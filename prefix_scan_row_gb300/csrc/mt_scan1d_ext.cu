@@ -1,6 +1,6 @@
-// mt_scan1d_ext.cu -- the device-wide 1-D scans for u32, u64 and f64 (the
-// Quadrants "Algorithms" user guide: "the new functional API covers {i32,
-// u32, f32, i64, u64, f64}"). Unsigned add wraps modulo 2^width and min/max
+// mt_scan1d_ext.cu -- the device-wide 1-D scans for u32, u64 and f64, the
+// dtypes the Quadrants "Algorithms" user guide lists beside i32, i64 and f32
+// for its scans (section "qd.algorithms.PrefixSumExecutor"). Unsigned add wraps modulo 2^width and min/max
 // compare as unsigned (identities UINT_MAX and 0); f64 follows f32 (identity
 // +-inf, earliest element on ties, sums grouped differently from a
 // left-to-right loop). Same staged kernel as mt_scan1d.cu.
