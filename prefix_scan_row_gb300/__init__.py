@@ -122,6 +122,13 @@ def _ptr(t) -> int:
     return 0 if t is None else (t if isinstance(t, int) else t.data_ptr())
 
 
+def _contiguous(**tensors) -> None:
+    """The library sees flat memory: a strided view would be read as such."""
+    for name, t in tensors.items():
+        if isinstance(t, torch.Tensor) and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
 def mt_scan_rows(inp: torch.Tensor, out: torch.Tensor, inclusive: bool, stream=None) -> None:
     """Row-wise sum scan of a contiguous 2-D (or 1-D = one row) CUDA tensor."""
     if inp.dim() == 1:
@@ -160,6 +167,7 @@ def mt_exclusive_scan(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tenso
         raise ValueError("out must have arr's dtype")
     if n_dev.dtype != torch.int32:
         raise ValueError("n_dev must be an int32 device tensor")
+    _contiguous(arr=arr, out=out, scratch=scratch)
     code = DTYPE_CODE.get(arr.dtype, -99)
     _check(lib.mt_exclusive_scan(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code,
                                  OP_CODE[op], _stream(stream)), "mt_exclusive_scan")
@@ -172,6 +180,7 @@ def mt_inclusive_scan(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tenso
         raise ValueError("out must have arr's dtype")
     if n_dev.dtype != torch.int32:
         raise ValueError("n_dev must be an int32 device tensor")
+    _contiguous(arr=arr, out=out, scratch=scratch)
     code = DTYPE_CODE.get(arr.dtype, -99)
     _check(lib.mt_inclusive_scan(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code,
                                  OP_CODE[op], _stream(stream)), "mt_inclusive_scan")
@@ -184,6 +193,7 @@ def mt_reduce(arr: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor, n_dev
         raise ValueError("out must have arr's dtype")
     if n_dev.dtype != torch.int32:
         raise ValueError("n_dev must be an int32 device tensor")
+    _contiguous(arr=arr, scratch=scratch)
     code = DTYPE_CODE.get(arr.dtype, -99)
     _check(lib.mt_reduce(_ptr(arr), _ptr(out), _ptr(scratch), _ptr(n_dev), code, OP_CODE[op],
                          _stream(stream)), "mt_reduce")
@@ -196,6 +206,7 @@ def mt_select(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out
         raise ValueError("select copies 4-byte elements")
     if flags.dtype != torch.uint8 or num_out.dtype != torch.int32 or n_dev.dtype != torch.int32:
         raise ValueError("flags must be uint8, num_out and n_dev int32")
+    _contiguous(arr=arr, flags=flags, out=out, scratch=scratch)
     _check(lib.mt_select(_ptr(arr), _ptr(flags), _ptr(out), _ptr(num_out), _ptr(scratch),
                          _ptr(n_dev), _stream(stream)), "mt_select")
 
@@ -208,6 +219,7 @@ def mt_select_wide(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, nu
         raise ValueError("select copies 4- or 8-byte elements; out must match arr")
     if flags.dtype != torch.uint8 or num_out.dtype != torch.int32 or n_dev.dtype != torch.int32:
         raise ValueError("flags must be uint8, num_out and n_dev int32")
+    _contiguous(arr=arr, flags=flags, out=out, scratch=scratch)
     _check(lib.mt_select_wide(_ptr(arr), _ptr(flags), _ptr(out), _ptr(num_out), _ptr(scratch),
                               _ptr(n_dev), eb, _stream(stream)), "mt_select_wide")
 
@@ -220,6 +232,8 @@ def mt_reduce_by_key_add(keys_in: torch.Tensor, values_in: torch.Tensor, keys_ou
         raise ValueError("outputs must have their inputs' dtypes")
     if num_runs.dtype != torch.int32 or n_dev.dtype != torch.int32:
         raise ValueError("num_runs and n_dev must be int32")
+    _contiguous(keys_in=keys_in, values_in=values_in, keys_out=keys_out, values_out=values_out,
+                scratch=scratch)
     _check(lib.mt_reduce_by_key_add(_ptr(keys_in), _ptr(values_in), _ptr(keys_out), _ptr(values_out),
                                     _ptr(num_runs), _ptr(scratch), _ptr(n_dev),
                                     DTYPE_CODE.get(keys_in.dtype, -99), DTYPE_CODE.get(values_in.dtype, -99),
