@@ -590,6 +590,21 @@ def run_suite(args):
         timeit(f"select f32 n={ns} p={p}", lambda: mt.mt_select(v, f, o, num, scr, nd),
                5 * ns + 4 * k, ns)
         del v, f, o, scr
+    for p in (0.5, 0.01):  # values 4 bytes past a 16-byte boundary: the unstaged kernel
+        if not wanted(f"select f32 misaligned n={ns} p={p}"):
+            continue
+        v, f = workloads.select_inputs(ns, p)
+        k = int(f.sum())
+        vb = torch.empty(ns + 4, dtype=torch.float32, device=dev)
+        vm = vb[1:1 + ns]
+        vm.copy_(v.to(dev))
+        f = f.to(dev)
+        o = torch.empty(ns, dtype=torch.float32, device=dev)
+        num = torch.zeros(1, dtype=torch.int32, device=dev)
+        scr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_SELECT, device=dev)
+        timeit(f"select f32 misaligned n={ns} p={p}", lambda: mt.mt_select(vm, f, o, num, scr, nd),
+               5 * ns + 4 * k, ns)
+        del v, vb, vm, f, o, scr
     for p in (0.5, 0.01):  # 8-byte elements: the same flags, f64 values
         if not wanted(f"select_wide f64 n={ns} p={p}"):
             continue
