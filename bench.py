@@ -590,7 +590,7 @@ def run_suite(args):
         timeit(f"select f32 n={ns} p={p}", lambda: mt.mt_select(v, f, o, num, scr, nd),
                5 * ns + 4 * k, ns)
         del v, f, o, scr
-    for p in (0.5, 0.01):  # values 4 bytes past a 16-byte boundary: the unstaged kernel
+    for p in (0.5, 0.01):  # values 4 bytes past a 16-byte boundary, flags at the boundary
         if not wanted(f"select f32 misaligned n={ns} p={p}"):
             continue
         v, f = workloads.select_inputs(ns, p)

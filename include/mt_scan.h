@@ -207,7 +207,10 @@ int mt_reduce(const void *arr, void *out, void *scratch, const int32_t *n_dev, i
  *
  * arr      : device array of n 4-byte elements (4-byte aligned).
  * flags    : device array of n uint8 flags, each exactly 0 or 1 (any other
- *            value is undefined behaviour, as on the page).
+ *            value is undefined behaviour, as on the page); any alignment.
+ *            Flags and values are read in whole 16-byte-aligned blocks, so a
+ *            few bytes on either side of each array (in the same 16-byte
+ *            blocks, hence the same pages) are read and ignored.
  * out      : device array with room for n elements; only out[0:*num_out] is
  *            written, the rest is left untouched. out must not overlap arr.
  * num_out  : device pointer to one int32.
@@ -223,13 +226,11 @@ int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out
 
 /*
  * mt_select_wide -- mt_select for elements of 4 or 8 bytes (elem_bytes),
- * copied bit for bit: [algos] "qd.algorithms.select" takes no dtype ("the
- * scatter is dtype-agnostic") and its API covers 32- and 64-bit scalars.
- * Arguments, scratch (MT_SCRATCH_SELECT), results and errors are those of
- * mt_select, with arr and out aligned to elem_bytes. 8-byte elements are
- * bulk-copied, so arr and flags must then be 16-byte aligned
- * (MT_ERR_ALIGN otherwise; allocations from cudaMalloc or torch are). An
- * elem_bytes other than 4 or 8 is MT_ERR_ARG.
+ * copied bit for bit: [algos] "qd.algorithms.select" takes no dtype (its
+ * scatter moves elements without looking at their type) and its API covers
+ * 32- and 64-bit scalars. Arguments, scratch (MT_SCRATCH_SELECT), results
+ * and errors are those of mt_select, with arr and out aligned to elem_bytes
+ * (MT_ERR_ALIGN otherwise). An elem_bytes other than 4 or 8 is MT_ERR_ARG.
  */
 int mt_select_wide(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                    void *scratch, const int32_t *n_dev, int elem_bytes, void *stream);

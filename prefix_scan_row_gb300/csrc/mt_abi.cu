@@ -306,9 +306,6 @@ static int select_call(const void *arr, const uint8_t *flags, void *out, int32_t
     if (((uintptr_t)arr % elem_bytes) != 0 || ((uintptr_t)out % elem_bytes) != 0 ||
         ((uintptr_t)num_out % 4) != 0 || ((uintptr_t)scratch % 16) != 0 || ((uintptr_t)n_dev % 4) != 0)
         return MT_ERR_ALIGN;
-    const bool aligned = ((uintptr_t)arr % 16 == 0) && ((uintptr_t)flags % 16 == 0);
-    if (elem_bytes == 8 && !aligned)
-        return MT_ERR_ALIGN;  // 8-byte elements are bulk-copied: arr and flags 16-byte aligned
     Launch L;
     int dev = 0;
     if (!make_launch(stream, &L, &dev))
@@ -319,7 +316,7 @@ static int select_call(const void *arr, const uint8_t *flags, void *out, int32_t
     if (launch_reset(sw, 0, n_dev, select_tile_elems(), 1, 0, select_rec_slots(), num_out, L) !=
         cudaSuccess)
         return MT_ERR_CUDA;
-    return select_launch(arr, flags, out, num_out, sw, n_dev, elem_bytes, aligned, L) == cudaSuccess
+    return select_launch(arr, flags, out, num_out, sw, n_dev, elem_bytes, L) == cudaSuccess
                ? MT_OK
                : MT_ERR_CUDA;
 }

@@ -119,8 +119,7 @@ cudaError_t rbk_take_error(int *code);
 int64_t select_tile_elems();
 int select_rec_slots();
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
-                          uint64_t *scratch, const int32_t *n_dev, int elem_bytes, bool aligned,
-                          const Launch &L);
+                          uint64_t *scratch, const int32_t *n_dev, int elem_bytes, const Launch &L);
 cudaError_t select_take_error(int *code);
 
 }  // namespace mt

@@ -5,20 +5,16 @@
 // order, in a dense prefix of out; num_out receives the count; the tail of
 // out is untouched. The page realises it as a scan of the flags into an
 // N-slot index buffer, a scatter pass and a one-thread count pass. Here one
-// persistent kernel does all three per tile: it counts the tile's flags,
-// gets the tile's output offset from the decoupled look-back, packs the
-// selected words in shared memory and writes them out as one contiguous run.
-// A value word is only read when one of its four flags is set, so sparse
-// flags skip most of the value bytes.
-//
-// When flags and values are 16-byte aligned, k_select_staged instead brings
-// each tile's flags and values into shared memory with two bulk copies and
-// publishes the tile's count as soon as they land. Each warp then packs its
-// selected words in place at the start of its own range of the tile, walking
-// its elements 32 at a time (lane i reads element i of each step, a ballot
-// ranks the selected lanes, so the writes are consecutive: no bank
-// conflicts). The look-back comes last, then each warp copies its packed run
-// out with coalesced stores. k_select serves the other alignments.
+// persistent kernel, k_select_staged, does all three per tile: it brings the
+// tile's flags and values into shared memory with two bulk copies, publishes
+// the tile's count as soon as the flags land, and gets the tile's output
+// offset from the decoupled look-back. Each warp packs its selected words in
+// place at the start of its own range of the tile, walking its elements 32
+// at a time (lane i reads element i of each step, a ballot ranks the
+// selected lanes, so the writes are consecutive: no bank conflicts). The
+// look-back comes last, then each warp copies its packed run out with
+// coalesced stores. Flags and values may sit at any offset from a 16-byte
+// boundary; the copies are widened to the boundaries around the tile.
 #include "mt_lookback.cuh"
 
 namespace mt {
@@ -30,27 +26,15 @@ constexpr int kSelItems = MT_SEL_ITEMS;  // flag chunks (16 flags) per thread
 constexpr int kSelChunks = kThreads * kSelItems;
 constexpr int64_t kSelTE = (int64_t)kSelChunks * 16;  // elements per tile (8192)
 
-struct SelSmem {
-    uint32_t warp_tot[kWarps];
-    uint32_t prefix;
-    unsigned long long tile;
-    uint32_t vals[kSelTE];  // the tile's selected words, packed
-};
-
 struct SelArgs {
-    const void *arr;  // 4-byte (k_select, k_select_staged<uint32_t>) or 8-byte elements
+    const void *arr;  // 4-byte (k_select_staged<uint32_t>) or 8-byte elements
     const uint8_t *flags;
     void *out;
     int32_t *num_out;
     const int32_t *n_dev;
     unsigned long long *counter;
-    int aligned;  // flags and arr both 16-byte aligned
     LookBack lb;
 };
-
-__device__ __forceinline__ uint32_t word_of(const uint4 &v, int w) {
-    return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
-}
 
 __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
     if (nbytes >= 4)
@@ -60,140 +44,20 @@ __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
     return w & ((1u << (8 * (int)nbytes)) - 1u);
 }
 
-__global__ void __launch_bounds__(kThreads) k_select(SelArgs a) {
-    pdl_prologue();
-    __shared__ SelSmem sm;
-    const uint32_t *arr = static_cast<const uint32_t *>(a.arr);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t n32 = *a.n_dev;
-    const int64_t n = n32 > 0 ? n32 : 0;
-    const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
-    for (;;) {
-        if (threadIdx.x == 0)
-            sm.tile = atomicAdd(a.counter, 1ull);
-        __syncthreads();  // also: every thread is done with the previous tile's sm.vals
-        const int64_t g = (int64_t)sm.tile;
-        if (g >= ntiles)
-            break;
-        const int64_t t0 = g * kSelTE;
-
-        // Flags: 16 per chunk; bytes at or past n read as 0.
-        uint4 f[kSelItems];
-#pragma unroll
-        for (int j = 0; j < kSelItems; ++j) {
-            const int64_t e0 = t0 + (int64_t)(warp * 32 * kSelItems + j * 32 + lane) * 16;
-            f[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (e0 < n) {
-                if (a.aligned) {
-                    f[j] = ld_stream(reinterpret_cast<const uint4 *>(a.flags) + e0 / 16);
-                } else {
-                    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                    for (int b = 0; b < 16; ++b)
-                        if (e0 + b < n)
-                            w[b >> 2] |= (uint32_t)a.flags[e0 + b] << (8 * (b & 3));
-                    f[j] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                const int64_t valid = n - e0;
-                f[j].x = keep_low_bytes(f[j].x, valid);
-                f[j].y = keep_low_bytes(f[j].y, valid - 4);
-                f[j].z = keep_low_bytes(f[j].z, valid - 8);
-                f[j].w = keep_low_bytes(f[j].w, valid - 12);
-            }
-        }
-        // Values: one 16-byte word group per 4 flags, read only if one is set.
-        uint4 v[kSelItems][4];
-#pragma unroll
-        for (int j = 0; j < kSelItems; ++j) {
-            const int64_t e0 = t0 + (int64_t)(warp * 32 * kSelItems + j * 32 + lane) * 16;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t fw = word_of(f[j], w);
-                v[j][w] = make_uint4(0u, 0u, 0u, 0u);
-                if (fw != 0u) {
-                    if (a.aligned) {
-                        v[j][w] = ld_stream(reinterpret_cast<const uint4 *>(arr) + (e0 + 4 * w) / 4);
-                    } else {
-                        uint32_t t[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            if ((fw >> (8 * b)) & 0xffu)
-                                t[b] = arr[e0 + 4 * w + b];
-                        v[j][w] = make_uint4(t[0], t[1], t[2], t[3]);
-                    }
-                }
-            }
-        }
-
-        // Counts per chunk (flags are exactly 0/1, so a popcount counts them).
-        uint32_t inc[kSelItems];
-#pragma unroll
-        for (int j = 0; j < kSelItems; ++j)
-            inc[j] = __popc(f[j].x) + __popc(f[j].y) + __popc(f[j].z) + __popc(f[j].w);
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-#pragma unroll
-            for (int j = 0; j < kSelItems; ++j) {
-                const uint32_t y = __shfl_up_sync(kFull, inc[j], d);
-                if (lane >= d)
-                    inc[j] += y;
-            }
-        }
-        uint32_t pre[kSelItems];
-        uint32_t run = 0u;
-#pragma unroll
-        for (int j = 0; j < kSelItems; ++j) {
-            uint32_t e = __shfl_up_sync(kFull, inc[j], 1);
-            if (lane == 0)
-                e = 0u;
-            pre[j] = run + e;
-            run += __shfl_sync(kFull, inc[j], 31);
-        }
-        if (lane == 0)
-            sm.warp_tot[warp] = run;
-        __syncthreads();
-        uint32_t wpre = 0u, agg = 0u;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const uint32_t t = sm.warp_tot[w];
-            if (w < warp)
-                wpre += t;
-            agg += t;
-        }
-        const uint32_t G = tile_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
-
-        // Pack the selected words of the tile in input order.
-#pragma unroll
-        for (int j = 0; j < kSelItems; ++j) {
-            uint32_t off = wpre + pre[j];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t fw = word_of(f[j], w);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    if ((fw >> (8 * b)) & 0xffu) {
-                        sm.vals[off] = word_of(v[j][w], b);
-                        ++off;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        // One contiguous run per tile: coalesced 4-byte stores.
-        uint32_t *dst = static_cast<uint32_t *>(a.out) + G;
-        for (uint32_t i = threadIdx.x; i < agg; i += kThreads)
-            dst[i] = sm.vals[i];
-        if (g == ntiles - 1 && threadIdx.x == 0)
-            *a.num_out = (int32_t)(G + agg);
-    }
-}
-
-// ---- staged variant (16-byte aligned flags and values) ----------------------
+// ---- staged kernel (any alignment) -------------------------------------------
 // VT: the element type, copied bit for bit (4 or 8 bytes).
+//
+// The bulk copies start at the 16-byte boundary at or below the tile's first
+// flag and first value and end at the boundary at or above its last ones:
+// those 16-byte blocks share a page with the tile's own bytes, so the wider
+// copy reads nothing that could fault. Flag byte b of the copy holds element
+// b - hf and value slot v holds element v - hv, where hf and hv are the
+// arrays' offsets from the boundary (the same for every tile, which holds a
+// multiple of 16 elements).
 template <class VT>
 struct SelStagedSmem {
-    uint4 flags[kSelChunks];  // 16 flags per chunk
-    VT vals[kSelTE];          // the tile's values; each warp packs its selected ones in place
+    uint4 flags[kSelChunks + 2];  // 16 flags per chunk, hf leading bytes, slack for the last warp
+    VT vals[kSelTE + 16 / sizeof(VT)];  // the tile's values; each warp packs its selected ones in place
     uint64_t bar_f;           // the flags' copy
     uint64_t bar_v;           // the values' copy
     int64_t tile;
@@ -201,34 +65,48 @@ struct SelStagedSmem {
     uint32_t prefix;
 };
 
+// The bytes of a 16-byte flag chunk whose positions lie in [lo, hi).
+__device__ __forceinline__ uint4 keep_byte_range(uint4 f, int lo, int hi) {
+    f.x = keep_low_bytes(f.x, hi) & ~keep_low_bytes(0xffffffffu, lo);
+    f.y = keep_low_bytes(f.y, hi - 4) & ~keep_low_bytes(0xffffffffu, lo - 4);
+    f.z = keep_low_bytes(f.z, hi - 8) & ~keep_low_bytes(0xffffffffu, lo - 8);
+    f.w = keep_low_bytes(f.w, hi - 12) & ~keep_low_bytes(0xffffffffu, lo - 12);
+    return f;
+}
+
 // One staged tile: count and publish the count, pack each warp's selected
 // words in place, look back for the tile's output offset, copy the packed
-// runs out. FULL: the tile holds kSelTE elements, so no flag or element needs
-// a range check. (Looking back before the packing, overlapped with it, was
-// measured slower: the look-back then meets more predecessors that have
-// only published their counts.)
+// runs out. Warp w owns the flag bytes [1024 w, 1024 (w + 1)) of the copy
+// (the last warp also the copy's extra chunk when hf + elems passes the
+// tile) and packs the elements they hold. FAST: a full tile with hf = hv =
+// 0, so no flag or element needs a range check. (Looking back before the
+// packing, overlapped with it, was measured slower: the look-back then meets
+// more predecessors that have only published their counts.)
 // Returns false when the values' copy did not complete in time (the caller
 // records the error and drains it).
-template <bool FULL, class VT>
+template <bool FAST, class VT>
 __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs &a, int64_t g,
-                                            int64_t ntiles, int elems, uint32_t phase) {
+                                            int64_t ntiles, int elems, int hf_, int hv_, uint32_t phase) {
+    constexpr int kTE = (int)kSelTE;
+    const int hf = FAST ? 0 : hf_, hv = FAST ? 0 : hv_;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // Count: popcounts of this thread's 16-flag chunks (flags past n are 0).
+    const int hi = hf + elems;  // one past the copy's last flag byte of the tile
+    const bool extra = !FAST && warp == kWarps - 1 && hi > kTE;
+    // Count: popcounts of this warp's 16-flag chunks, bytes outside [hf, hi) masked.
     uint32_t mine = 0u;
 #pragma unroll
     for (int j = 0; j < kSelItems; ++j) {
         const int c = warp * 32 * kSelItems + j * 32 + lane;
-        const int valid = elems - c * 16;
-        if (FULL || valid > 0) {
+        if (FAST || 16 * c < hi) {
             uint4 f = lds128(&sm.flags[c]);
-            if (!FULL) {
-                f.x = keep_low_bytes(f.x, valid);
-                f.y = keep_low_bytes(f.y, valid - 4);
-                f.z = keep_low_bytes(f.z, valid - 8);
-                f.w = keep_low_bytes(f.w, valid - 12);
-            }
+            if (!FAST)
+                f = keep_byte_range(f, hf - 16 * c, hi - 16 * c);
             mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
         }
+    }
+    if (extra && lane == 0) {
+        const uint4 f = keep_byte_range(lds128(&sm.flags[kSelChunks]), 0, hi - kTE);
+        mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
     }
     // The tile's count, published as soon as the flags are in.
     uint32_t wsum = mine;
@@ -255,42 +133,59 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     if (__syncthreads_or(!ok))
         return false;
 
-    // Pack this warp's selected words in place, in element order. A write
-    // goes to a slot at or before every element this warp reads later, and
-    // a warp step reads all its lanes before any of them writes.
+    // Pack this warp's selected words in place, in element order, from the
+    // slot of its first element on. A write goes to a slot at or before
+    // every slot this warp reads later and inside this warp's own slots; the
+    // warp barrier orders a step's reads before its writes.
     const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
     const int wstart = warp * 32 * kSelItems * 16;
+    const int ebase = FAST ? wstart : max(wstart - hf, 0);
+    VT *const run = sm.vals + hv + ebase;
     const unsigned lt = (1u << lane) - 1u;
     uint32_t cnt = 0u;
-#pragma unroll
-    for (int step = 0; step < kSelItems * 16; ++step) {
-        const int e = wstart + step * 32 + lane;
-        const bool sel = (FULL || e < elems) && fb[e] != 0;
+    auto step = [&](int s) {
+        const int b = wstart + s * 32 + lane;
+        const int e = b - hf;
+        const bool sel = (FAST || (unsigned)e < (unsigned)elems) && fb[b] != 0;
         const unsigned bal = __ballot_sync(kFull, sel);
-        const VT val = sm.vals[e];
+        VT val = 0;
         if (sel)
-            sm.vals[wstart + cnt + __popc(bal & lt)] = val;
+            val = sm.vals[hv + e];
+        __syncwarp();
+        if (sel)
+            run[cnt + __popc(bal & lt)] = val;
         cnt += __popc(bal);
-    }
+    };
+#pragma unroll
+    for (int s = 0; s < kSelItems * 16; ++s)
+        step(s);
+    if (extra)  // warp-uniform
+        step(kSelItems * 16);
     __syncwarp();
     // The tile's output offset (the look-back ends with a block barrier).
     const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
     VT *dst = static_cast<VT *>(a.out) + G + wpre;
     for (uint32_t i = lane; i < cnt; i += 32)
-        dst[i] = sm.vals[wstart + i];
+        dst[i] = run[i];
     if (g == ntiles - 1 && threadIdx.x == 0)
         *a.num_out = (int32_t)(G + agg);
     return true;
 }
 
+// Resident blocks per SM: shared memory allows 5 (4-byte values) or 3
+// (8-byte values); the bound keeps the registers within that.
 template <class VT>
-__global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
+__global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_staged(SelArgs a) {
     pdl_prologue();
     extern __shared__ __align__(128) unsigned char dsm[];
     SelStagedSmem<VT> &sm = *reinterpret_cast<SelStagedSmem<VT> *>(dsm);
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
     const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
+    // Offsets from the 16-byte boundary below (arr is aligned to its element size).
+    const int hf = (int)(reinterpret_cast<uintptr_t>(a.flags) & 15u);
+    const int hvb = (int)(reinterpret_cast<uintptr_t>(a.arr) & 15u);
+    const int hv = hvb / (int)sizeof(VT);
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar_f, 1);
         mbar_init(&sm.bar_v, 1);
@@ -308,12 +203,13 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
         const int elems = (int)((n - t0 < kSelTE) ? n - t0 : kSelTE);
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
-            const uint32_t fb = (uint32_t)((elems + 15) / 16 * 16);
-            const uint32_t vb = (uint32_t)(((int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
-            mbar_arrive_expect_tx(&sm.bar_f, fb);
-            bulk_g2s(&sm.flags[0], a.flags + t0, fb, &sm.bar_f);
-            mbar_arrive_expect_tx(&sm.bar_v, vb);
-            bulk_g2s(&sm.vals[0], static_cast<const VT *>(a.arr) + t0, vb, &sm.bar_v);
+            const uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
+            const uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
+            const unsigned char *vsrc = static_cast<const unsigned char *>(a.arr) + t0 * (int64_t)sizeof(VT);
+            mbar_arrive_expect_tx(&sm.bar_f, fbytes);
+            bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
+            mbar_arrive_expect_tx(&sm.bar_v, vbytes);
+            bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
         }
         // Warp 0 waits for the flags; the block barrier passes the
         // completion (and the copied bytes) on to the other warps. The
@@ -324,8 +220,9 @@ __global__ void __launch_bounds__(kThreads) k_select_staged(SelArgs a) {
         if (__syncthreads_or(!ok))
             ok = false;  // every thread: the flags did not arrive
         else
-            ok = (elems == kSelTE) ? select_tile<true, VT>(sm, a, g, ntiles, elems, phase)
-                                   : select_tile<false, VT>(sm, a, g, ntiles, elems, phase);
+            ok = (elems == kSelTE && hf == 0 && hvb == 0)
+                     ? select_tile<true, VT>(sm, a, g, ntiles, elems, hf, hv, phase)
+                     : select_tile<false, VT>(sm, a, g, ntiles, elems, hf, hv, phase);
         if (!ok) {  // block-uniform
             if (threadIdx.x == 0) {
                 atomicCAS(&g_mt_err, 0, kErrTimeout);
@@ -375,38 +272,7 @@ static cudaError_t launch_staged_select(const SelArgs &a, const Launch &L) {
 }
 
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
-                          uint64_t *scratch, const int32_t *n_dev, int elem_bytes, bool aligned,
-                          const Launch &L) {
-    if (aligned || elem_bytes == 8) {  // 8-byte elements: the caller checked the alignment
-        SelArgs a;
-        a.arr = arr;
-        a.flags = flags;
-        a.out = out;
-        a.num_out = num_out;
-        a.n_dev = n_dev;
-        a.counter = reinterpret_cast<unsigned long long *>(scratch);
-        a.aligned = 1;
-        a.lb.recs = scratch + kHeaderSlots;
-        a.lb.skip_tile = L.skip_tile;
-        a.lb.spin_limit = L.spin_limit;
-        return elem_bytes == 8 ? launch_staged_select<uint64_t>(a, L) : launch_staged_select<uint32_t>(a, L);
-    }
-    static PerDevice per_sm;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess)
-        return err;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    int blocks = per_sm.get(dev);
-    if (blocks == 0) {
-        int b = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select, kThreads, 0);
-        if (err != cudaSuccess)
-            return err;
-        blocks = b > 0 ? b : 1;
-        per_sm.set(dev, blocks);
-    }
+                          uint64_t *scratch, const int32_t *n_dev, int elem_bytes, const Launch &L) {
     SelArgs a;
     a.arr = arr;
     a.flags = flags;
@@ -414,13 +280,10 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
     a.num_out = num_out;
     a.n_dev = n_dev;
     a.counter = reinterpret_cast<unsigned long long *>(scratch);
-    a.aligned = aligned ? 1 : 0;
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
-    const cudaError_t e = launch_pdl(k_select, (unsigned)(L.sm_count * blocks), kThreads, 0, L.stream, a);
-    note_launch();
-    return e;
+    return elem_bytes == 8 ? launch_staged_select<uint64_t>(a, L) : launch_staged_select<uint32_t>(a, L);
 }
 
 cudaError_t select_take_error(int *code) {

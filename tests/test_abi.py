@@ -126,9 +126,9 @@ def test_select_wide_host_checks(lib):
     assert f(A, B, S, N, S, N, 3, None) == ARG
     assert f(A, B, S, N, S, N, 16, None) == ARG
     assert f(A, B, A, N, S, N, 8, None) == ALIAS
-    assert f(A + 4, B, S, N, S, N, 8, None) == ALIGN
-    assert f(A + 8, B, S, N, S, N, 8, None) == ALIGN  # 8-byte elements need 16-byte arr
-    assert f(A, B + 1, S, N, S, N, 8, None) == ALIGN  # ... and 16-byte flags
+    assert f(A + 4, B, S, N, S, N, 8, None) == ALIGN  # 8-byte elements: arr 8-byte aligned
+    assert f(A, B, S + 4, N, S, N, 8, None) == ALIGN  # ... and out
+    # (any 8-byte-aligned arr and any flags offset pass these checks: the GPU tests cover them)
 
 
 def test_reduce_by_key_host_checks(lib):

@@ -104,10 +104,10 @@ def test_fuzz_select(mt, case):
     nd = torch.tensor([n], dtype=torch.int32, device="cuda")
     num = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     scr = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
-    if wide:  # 8-byte elements, 16-byte-aligned buffers
+    if wide:  # 8-byte elements at any 8-byte offsets
         v64 = v_cpu.to(torch.float64)
-        arr, fl = v64.cuda(), f_cpu.cuda()
-        out = torch.zeros_like(arr)
+        arr, fl = to_dev(v64, int(rng.integers(2))), to_dev(f_cpu, int(rng.integers(16)))
+        out = to_dev(torch.zeros_like(v64), int(rng.integers(2)))
         mt.mt_select_wide(arr, fl, out, num, scr, nd)
         torch.cuda.synchronize()
         assert mt.mt_scan_status() == 0

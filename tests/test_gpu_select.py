@@ -71,6 +71,19 @@ def test_select_misaligned(mt, offs, p):
     assert_select_matches(out, num, vals, flags, n)
 
 
+@pytest.mark.parametrize("arr_off", [1, 2, 3])
+@pytest.mark.parametrize("flag_off", [1, 4, 9, 15])
+@pytest.mark.parametrize("n", [1, 8177, 8192, 8193, 2 * 8192 + 15])
+@pytest.mark.parametrize("p", [0.5, 1.0])
+def test_select_16_byte_phases_at_tile_edges(mt, arr_off, flag_off, n, p):
+    """Every tile of a misaligned input takes the masked path; at these sizes
+    the flags' copy of a tile also spills into one more 16-byte chunk."""
+    vals = workloads.uniform((n,), 33 + n, -1.0, 1.0, "f32")
+    flags = workloads.bernoulli_u8(n, p, 34 + n)
+    out, num = run_select(mt, vals, flags, n, arr_off, flag_off, arr_off)
+    assert_select_matches(out, num, vals, flags, n)
+
+
 def test_select_bit_patterns(mt):
     """Any 32-bit pattern (NaNs, -0.0, denormals) is copied unchanged."""
     n = 40000

@@ -88,17 +88,31 @@ def test_select_wide_full_size(mt):
     check(out, k, vals, flags, n)
 
 
-def test_select_wide_alignment_rules(mt):
-    n = 1000
-    base = torch.zeros(n + 4, dtype=torch.int64, device="cuda")
-    fl = torch.ones(n + 16, dtype=torch.uint8, device="cuda")
-    out = torch.zeros(n, dtype=torch.int64, device="cuda")
-    num = torch.zeros(1, dtype=torch.int32, device="cuda")
-    scr = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
-    nd = torch.tensor([n], dtype=torch.int32, device="cuda")
-    for arr, flags in ((base[1:n + 1], fl[:n]), (base[:n], fl[3:n + 3])):  # 8-aligned arr / odd flags
-        with pytest.raises(mt.ScanError) as ei:
-            mt.mt_select_wide(arr, flags, out, num, scr, nd)
-        assert ei.value.code == mt.MT_ERR_ALIGN
-    torch.cuda.synchronize()
-    assert mt.mt_scan_status() == 0
+@pytest.mark.parametrize("arr_off", [0, 1])
+@pytest.mark.parametrize("flag_off", [0, 1, 8, 15])
+@pytest.mark.parametrize("n", [1, 8177, 8192, 8193, 3 * 8192 - 1])
+def test_select_wide_any_16_byte_phase(mt, arr_off, flag_off, n):
+    """Values 8 bytes past a 16-byte boundary and flags at any offset: the
+    bulk copies start at the boundary below and the tile's ends are masked
+    (n covers the tile size and the sizes where the flags' copy of a tile
+    spills into one more 16-byte chunk)."""
+    vals = workloads.randint((n,), 70 + n, -(2**62), 2**62, "i64")
+    for p in (0.5, 1.0):
+        flags = workloads.bernoulli_u8(n, p, 71 + n)
+        abuf = torch.zeros(n + arr_off, dtype=torch.int64, device="cuda")
+        arr = abuf[arr_off:]
+        arr.copy_(vals.cuda())
+        fbuf = torch.zeros(n + flag_off, dtype=torch.uint8, device="cuda")
+        fl = fbuf[flag_off:]
+        fl.copy_(flags.cuda())
+        obuf = torch.full((n + 17,), SENT, dtype=torch.int64, device="cuda")
+        out = obuf[1:n + 1]
+        num = torch.full((1,), -9, dtype=torch.int32, device="cuda")
+        scr = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
+        nd = torch.tensor([n], dtype=torch.int32, device="cuda")
+        mt.mt_select_wide(arr, fl, out, num, scr, nd)
+        torch.cuda.synchronize()
+        assert mt.mt_scan_status() == 0
+        k = int(num.item())
+        assert obuf[0].item() == SENT and torch.all(obuf[1 + k:] == SENT).item()
+        check(out, k, vals, flags, n)
