@@ -687,7 +687,8 @@ int64_t oracle_select(const uint32_t *arr, const uint8_t *flags, uint32_t *out, 
 
 /* ------------------------------------------------------------------------
  * The same compaction for elements of `elem_bytes` bytes (4 or 8), copied
- * byte for byte ([algos] select: no dtype, the scatter is dtype-agnostic).
+ * byte for byte ([algos] select takes no dtype: its scatter moves elements
+ * without looking at their type).
  * Returns the count, or -1 for another element size.
  * ---------------------------------------------------------------------- */
 int64_t oracle_select_wide(const void *arr, const uint8_t *flags, void *out, int64_t n, int elem_bytes)
