@@ -200,12 +200,20 @@ def select(arr, flags, n: int):
 
 
 def select_wide(arr, flags, n: int, elem_bytes: int):
-    """Stream compaction of 4- or 8-byte elements; returns (out[0:num_out] as
-    u32/u64 bit patterns, num_out)."""
-    w = np.uint32 if elem_bytes == 4 else np.uint64
-    a = np.ascontiguousarray(_np(arr)[:n]).view(w)
+    """Stream compaction of elements of elem_bytes bytes; returns
+    (out[0:num_out], num_out). out holds u32 / u64 bit patterns for 4- / 8-byte
+    elements, else a [num_out, elem_bytes] uint8 array (one struct per row).
+    arr is any array whose first n * elem_bytes bytes are the n elements."""
     f = np.ascontiguousarray(_np(flags)[:n]).view(np.uint8)
-    out = np.empty((max(n, 1),), dtype=w)
+    if elem_bytes in (4, 8):
+        w = np.uint32 if elem_bytes == 4 else np.uint64
+        a = np.ascontiguousarray(_np(arr)[:n]).view(w)
+        out = np.empty((max(n, 1),), dtype=w)
+    else:
+        a = np.ascontiguousarray(_np(arr)).reshape(-1).view(np.uint8)[:n * elem_bytes]
+        if a.size != n * elem_bytes:
+            raise ValueError("arr holds fewer than n elements")
+        out = np.empty((max(n, 1), max(elem_bytes, 1)), dtype=np.uint8)
     k = lib().oracle_select_wide(_ptr(a), _ptr(f), _ptr(out), n, elem_bytes)
     if k < 0:
         raise ValueError("oracle_select_wide rejected its arguments")

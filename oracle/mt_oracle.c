@@ -686,14 +686,15 @@ int64_t oracle_select(const uint32_t *arr, const uint8_t *flags, uint32_t *out, 
 }
 
 /* ------------------------------------------------------------------------
- * The same compaction for elements of `elem_bytes` bytes (4 or 8), copied
- * byte for byte ([algos] select takes no dtype: its scatter moves elements
- * without looking at their type).
- * Returns the count, or -1 for another element size.
+ * The same compaction for elements of `elem_bytes` bytes, copied byte for
+ * byte ([algos] select takes no dtype: its scatter moves elements without
+ * looking at their type, field by field for struct elements, so scalars of
+ * 4 or 8 bytes and structs of any size are compacted alike).
+ * Returns the count, or -1 for elem_bytes < 1.
  * ---------------------------------------------------------------------- */
 int64_t oracle_select_wide(const void *arr, const uint8_t *flags, void *out, int64_t n, int elem_bytes)
 {
-    if (elem_bytes != 4 && elem_bytes != 8)
+    if (elem_bytes < 1)
         return -1;
     int64_t j = 0;
     for (int64_t i = 0; i < n; ++i) {

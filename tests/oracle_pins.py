@@ -708,6 +708,31 @@ def pin_select_wide():
         assert k == len(want) and out.tolist() == want
 
 
+def pin_select_struct_elements():
+    """Struct elements ([algos] select: the scatter copies each field): a
+    compaction of structs equals the compaction of each field column with
+    the same flags, and a plain Python filter on tiny inputs."""
+    rng = np.random.default_rng(61)
+    for words in (3, 4, 6, 9, 64):  # 12- to 256-byte structs of 32-bit fields
+        for n in (0, 1, 7, 300, 2000):
+            arr = rng.integers(0, 2**32, (n, words), dtype=np.uint64).astype(np.uint32)
+            flags = (rng.random(n) < 0.4).astype(np.uint8)
+            out, k = oracle.select_wide(arr, flags, n, 4 * words)
+            assert k == int(flags.sum())
+            got = out.view(np.uint32).reshape(k, words)
+            for w in range(words):
+                col, kc = oracle.select(np.ascontiguousarray(arr[:, w]), flags, n)
+                assert kc == k and np.array_equal(got[:, w], col), (words, n, w)
+            if n <= 7:
+                want = [list(map(int, arr[i])) for i in range(n) if flags[i] == 1]
+                assert got.tolist() == want
+    # an element size that is not a multiple of 4 (3-byte records) by brute force
+    rec = rng.integers(0, 256, (50, 3), dtype=np.uint8)
+    flags = (rng.random(50) < 0.5).astype(np.uint8)
+    out, k = oracle.select_wide(rec, flags, 50, 3)
+    assert out.tolist() == [list(map(int, rec[i])) for i in range(50) if flags[i] == 1]
+
+
 # ---------------------------------------------------------------------------
 # Reduce by key
 # ---------------------------------------------------------------------------
