@@ -486,7 +486,7 @@ def run_suite(args):
         ms = a.elapsed_time(b) / (rounds * len(fns))
         return nbytes / (ms / 1e3) / 1e9
 
-    def timeit(name, fn, nbytes, elems, reps=20, rotate=None):
+    def timeit(name, fn, nbytes, elems, reps=20, rotate=None, touched=None):
         if not wanted(name):
             return
         small = nbytes < 2 * L2_BYTES
@@ -514,6 +514,10 @@ def run_suite(args):
              "frac_measured": round(gbs / peak, 3), "frac_datasheet_8000_gbs": round(gbs / 8000.0, 3),
              "Gelem/s": round(elems / (med / 1e3) / 1e9, 2),
              "l2_flushed": small, "host_enqueue_hidden": True}
+        if touched is not None:  # the bytes the launch actually moves (values read only when selected)
+            tg = touched / (med / 1e3) / 1e9
+            r.update({"touched_bytes": int(touched), "touched_GB/s": round(tg, 1),
+                      "touched_frac_measured": round(tg / peak, 3)})
         if rotate is not None:
             sg = sustained(rotate, nbytes)
             r.update({"back_to_back_GB/s": round(sg, 1), "back_to_back_frac_measured": round(sg / peak, 3),
@@ -617,6 +621,28 @@ def run_suite(args):
         timeit(f"select_wide f64 n={ns} p={p}", lambda: mt.mt_select_wide(v, f, o, num, scr, nd),
                9 * ns + 8 * k, ns)
         del v, f, o, scr
+    for words in (3, 4):  # struct elements (12- and 16-byte vectors): flags staged, values read once selected
+        for p in (0.5, 0.01):
+            name = f"select_wide struct {4 * words}B n={ns} p={p}"
+            if not wanted(name):
+                continue
+            v, f = workloads.select_inputs(ns, p)
+            k = int(f.sum())
+            v = v.to(dev).view(torch.int32).unsqueeze(1).expand(ns, words).contiguous()
+            f = f.to(dev)
+            o = torch.empty_like(v)
+            num = torch.zeros(1, dtype=torch.int32, device=dev)
+            scr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_SELECT, device=dev)
+            # 32-byte sectors of arr holding part of a selected struct (the only value bytes read)
+            sel = torch.nonzero(f).flatten().to(torch.int64)
+            sec = torch.zeros((4 * words * ns + 31) // 32, dtype=torch.bool, device=dev)
+            sec[(4 * words * sel) // 32] = True
+            sec[(4 * words * sel + 4 * words - 1) // 32] = True
+            touched = ns + 32 * int(sec.sum()) + 4 * words * k
+            del sel, sec
+            timeit(name, lambda: mt.mt_select_wide(v, f, o, num, scr, nd), (1 + 4 * words) * ns + 4 * words * k, ns,
+                   touched=touched)
+            del v, f, o, scr
     # reduce by key: i32 keys in runs of mean length 8, f32 values
     nr = workloads.SELECT_N // args.scale
     if wanted(f"reduce_by_key i32/f32 n={nr} mean_run=8"):

@@ -225,12 +225,16 @@ int mt_select(const void *arr, const uint8_t *flags, void *out, int32_t *num_out
               void *scratch, const int32_t *n_dev, void *stream);
 
 /*
- * mt_select_wide -- mt_select for elements of 4 or 8 bytes (elem_bytes),
- * copied bit for bit: [algos] "qd.algorithms.select" takes no dtype (its
- * scatter moves elements without looking at their type) and its API covers
- * 32- and 64-bit scalars. Arguments, scratch (MT_SCRATCH_SELECT), results
- * and errors are those of mt_select, with arr and out aligned to elem_bytes
- * (MT_ERR_ALIGN otherwise). An elem_bytes other than 4 or 8 is MT_ERR_ARG.
+ * mt_select_wide -- mt_select for elements of elem_bytes bytes, copied bit
+ * for bit: [algos] "qd.algorithms.select" takes no dtype (its scatter moves
+ * elements without looking at their type, field by field for structs) and
+ * covers 32- and 64-bit scalars and struct element types. elem_bytes is 4,
+ * 8, or a struct of 3 to 64 32-bit words (12 to 256 bytes, a multiple of 4;
+ * MT_ERR_ARG otherwise). Arguments, scratch (MT_SCRATCH_SELECT), results and
+ * errors are those of mt_select; arr and out are aligned to 8 bytes for
+ * 8-byte elements and to 4 bytes otherwise (MT_ERR_ALIGN). Struct elements
+ * are read straight from arr, only those selected (4- and 8-byte elements
+ * are staged through shared memory with the flags).
  */
 int mt_select_wide(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                    void *scratch, const int32_t *n_dev, int elem_bytes, void *stream);

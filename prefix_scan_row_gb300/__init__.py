@@ -26,6 +26,7 @@ Names and arguments follow the C ABI:
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -213,10 +214,12 @@ def mt_select(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out
 
 def mt_select_wide(arr: torch.Tensor, flags: torch.Tensor, out: torch.Tensor, num_out: torch.Tensor,
                    scratch: torch.Tensor, n_dev: torch.Tensor, stream=None) -> None:
-    """Stream compaction of 4- or 8-byte elements (the element size of arr)."""
-    eb = arr.element_size()
-    if out.element_size() != eb or eb not in (4, 8):
-        raise ValueError("select copies 4- or 8-byte elements; out must match arr")
+    """Stream compaction of 4- or 8-byte elements, or of structs: a 1-D arr
+    holds one element per entry, an [n, ...] arr one struct per row (its
+    trailing dimensions), copied bit for bit."""
+    eb = arr.element_size() * math.prod(arr.shape[1:])
+    if out.element_size() * math.prod(out.shape[1:]) != eb:
+        raise ValueError("out's elements must have arr's size")
     if flags.dtype != torch.uint8 or num_out.dtype != torch.int32 or n_dev.dtype != torch.int32:
         raise ValueError("flags must be uint8, num_out and n_dev int32")
     _contiguous(arr=arr, flags=flags, out=out, scratch=scratch)

@@ -298,12 +298,14 @@ extern "C" int mt_reduce(const void *arr, void *out, void *scratch, const int32_
 // mt_select and mt_select_wide share their checks and kernels.
 static int select_call(const void *arr, const uint8_t *flags, void *out, int32_t *num_out, void *scratch,
                        const int32_t *n_dev, int elem_bytes, void *stream) {
+    // 4- or 8-byte scalars, or structs of 3 to 64 32-bit words
     if (arr == nullptr || flags == nullptr || out == nullptr || num_out == nullptr ||
-        scratch == nullptr || n_dev == nullptr || (elem_bytes != 4 && elem_bytes != 8))
+        scratch == nullptr || n_dev == nullptr || elem_bytes < 4 || elem_bytes > 256 || elem_bytes % 4 != 0)
         return MT_ERR_ARG;
     if (arr == out)
         return MT_ERR_ALIAS;
-    if (((uintptr_t)arr % elem_bytes) != 0 || ((uintptr_t)out % elem_bytes) != 0 ||
+    const int align = elem_bytes == 8 ? 8 : 4;  // structs are read as 32-bit words
+    if (((uintptr_t)arr % align) != 0 || ((uintptr_t)out % align) != 0 ||
         ((uintptr_t)num_out % 4) != 0 || ((uintptr_t)scratch % 16) != 0 || ((uintptr_t)n_dev % 4) != 0)
         return MT_ERR_ALIGN;
     Launch L;

@@ -74,6 +74,32 @@ __device__ __forceinline__ uint4 keep_byte_range(uint4 f, int lo, int hi) {
     return f;
 }
 
+// This thread's share of a tile's selected count: popcounts of its 16-flag
+// chunks of the copy (warp w owns the flag bytes [1024 w, 1024 (w + 1)); the
+// last warp also the copy's extra chunk when hf + elems passes the tile),
+// bytes outside [hf, hf + elems) masked. FAST: hf = 0 and a full tile.
+template <bool FAST>
+__device__ __forceinline__ uint32_t count_flags(const uint4 *flags, int warp, int lane, int hf, int elems) {
+    constexpr int kTE = (int)kSelTE;
+    const int hi = hf + elems;  // one past the copy's last flag byte of the tile
+    uint32_t mine = 0u;
+#pragma unroll
+    for (int j = 0; j < kSelItems; ++j) {
+        const int c = warp * 32 * kSelItems + j * 32 + lane;
+        if (FAST || 16 * c < hi) {
+            uint4 f = lds128(&flags[c]);
+            if (!FAST)
+                f = keep_byte_range(f, hf - 16 * c, hi - 16 * c);
+            mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
+        }
+    }
+    if (!FAST && warp == kWarps - 1 && lane == 0 && hi > kTE) {
+        const uint4 f = keep_byte_range(lds128(&flags[kSelChunks]), 0, hi - kTE);
+        mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
+    }
+    return mine;
+}
+
 // One staged tile: count and publish the count, pack each warp's selected
 // words in place, look back for the tile's output offset, copy the packed
 // runs out. Warp w owns the flag bytes [1024 w, 1024 (w + 1)) of the copy
@@ -92,22 +118,7 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hi = hf + elems;  // one past the copy's last flag byte of the tile
     const bool extra = !FAST && warp == kWarps - 1 && hi > kTE;
-    // Count: popcounts of this warp's 16-flag chunks, bytes outside [hf, hi) masked.
-    uint32_t mine = 0u;
-#pragma unroll
-    for (int j = 0; j < kSelItems; ++j) {
-        const int c = warp * 32 * kSelItems + j * 32 + lane;
-        if (FAST || 16 * c < hi) {
-            uint4 f = lds128(&sm.flags[c]);
-            if (!FAST)
-                f = keep_byte_range(f, hf - 16 * c, hi - 16 * c);
-            mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
-        }
-    }
-    if (extra && lane == 0) {
-        const uint4 f = keep_byte_range(lds128(&sm.flags[kSelChunks]), 0, hi - kTE);
-        mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
-    }
+    const uint32_t mine = count_flags<FAST>(sm.flags, warp, lane, hf, elems);
     // The tile's count, published as soon as the flags are in.
     uint32_t wsum = mine;
 #pragma unroll
@@ -237,6 +248,267 @@ __global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_st
     }
 }
 
+// ---- struct elements ----------------------------------------------------------
+// Elements of W 32-bit words (W >= 3: 12 to 256 bytes, 4-byte aligned), as
+// the page's select takes struct element types and copies them field by
+// field. A tile of 8192 elements would need up to 2 MB of shared memory for
+// its values, so only the flags are staged: the tile's count is published,
+// the look-back gives its output offset, and then each warp copies its
+// selected elements straight from arr to out. Each warp first takes the
+// ballots of its 32 steps of 32 elements (lane s keeps step s's ballot and
+// the count of selected elements before it). A warp with many selected
+// elements then walks its 1024 W consecutive words with lane-consecutive
+// words (coalesced loads and stores, several loads in flight per lane, the
+// words of unselected elements skipped); a warp with few has each lane copy
+// one selected element, found by a search over those counts, so a sparse
+// selection reads little more than its own sectors. WT: W known at compile
+// time (0: W and its reciprocal, for word -> element, at run time).
+struct SelWordsSmem {
+    uint4 flags[kSelChunks + 2];  // as in SelStagedSmem
+    uint64_t bar_f;
+    int64_t tile;
+    uint32_t red[kWarps];
+    uint32_t prefix;
+};
+
+struct SelWords {
+    int words;       // W
+    uint32_t recip;  // ceil(2^32 / W): word j of a step belongs to element umulhi(j, recip)
+};
+
+template <bool FAST, int WT>
+__device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArgs &a, int W_rt, uint32_t recip,
+                                                  int64_t g, int64_t ntiles, int elems, int hf_) {
+    constexpr int kTE = (int)kSelTE;
+    const int W = WT != 0 ? WT : W_rt;
+    const int hf = FAST ? 0 : hf_;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t mine = count_flags<FAST>(sm.flags, warp, lane, hf, elems);
+    uint32_t wsum = mine;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        wsum += __shfl_xor_sync(kFull, wsum, d);
+    if (lane == 0)
+        sm.red[warp] = wsum;
+    __syncthreads();
+    uint32_t agg = 0u, wpre = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t t = sm.red[w];
+        if (w < warp)
+            wpre += t;
+        agg += t;
+    }
+    publish_aggregate<uint32_t, OpAdd>(a.lb, g, 0, agg);
+    // The tile's output offset (the look-back ends with a block barrier).
+    const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
+
+    const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
+    const uint32_t *src = static_cast<const uint32_t *>(a.arr);
+    uint32_t *dst = static_cast<uint32_t *>(a.out);
+    const int wstart = warp * 32 * kSelItems * 16;
+    const int64_t t0 = g * kSelTE;
+    static_assert(kSelItems * 16 == 32, "a warp's flag bytes are 32 steps of 32");
+    // The ballots of the warp's 32 steps of 32 elements: lane s keeps step
+    // s's ballot and the number of selected elements in the steps before s.
+    unsigned my_bal = 0u;
+#pragma unroll 8
+    for (int st = 0; st < 32; ++st) {
+        const int bb = wstart + st * 32 + lane;
+        const int e = bb - hf;
+        const bool sel = (FAST || (unsigned)e < (unsigned)elems) && fb[bb] != 0;
+        const unsigned bal = __ballot_sync(kFull, sel);
+        if (lane == st)
+            my_bal = bal;
+    }
+    uint32_t my_before = __popc(my_bal);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, my_before, d);
+        if (lane >= d)
+            my_before += y;
+    }
+    const uint32_t warp_cnt = __shfl_sync(kFull, my_before, 31);
+    my_before -= __popc(my_bal);  // exclusive
+    // The warp's 1024 elements are 1024 W consecutive words of arr. Lanes
+    // walk them 32 words apart, R words each per round: all R loads (only
+    // words of selected elements) before the R stores, so a warp keeps R
+    // loads in flight. Word q belongs to the warp's element le = q / W, of
+    // step le / 32; its packed place is the step's count before it plus the
+    // selected lanes of its step below it.
+    const int64_t ibase = (t0 + wstart - hf) * (int64_t)W;  // word 0 of the warp's element 0
+    const uint32_t obase = G + wpre;
+#ifndef MT_SEL_WORDS_R
+#define MT_SEL_WORDS_R 8
+#endif
+#ifndef MT_SEL_WORDS_SPARSE
+#define MT_SEL_WORDS_SPARSE 512
+#endif
+    constexpr int R = MT_SEL_WORDS_R;
+    // per-element rounds (warp_cnt / 32) against word rounds (1024 W / 32 R), halved
+    if (warp_cnt * (uint32_t)R <= (uint32_t)MT_SEL_WORDS_SPARSE * (uint32_t)W) {
+        // Few selected: lane k copies the warp's k-th selected element, all
+        // its words loaded before any is stored (the words of one element
+        // are adjacent; different elements rarely share a sector here).
+        for (uint32_t k0 = 0; k0 < warp_cnt; k0 += 32) {
+            const uint32_t k = k0 + lane;
+            int st = 0;  // the step holding selected element k: the last with my_before <= k
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1)
+                if (__shfl_sync(kFull, my_before, st + d) <= k)
+                    st += d;
+            const unsigned bal = __shfl_sync(kFull, my_bal, st);
+            int rk = (int)(k - __shfl_sync(kFull, my_before, st));  // its rank within the step
+            if (k < warp_cnt) {
+                int pos = 0;  // the rk-th set bit of bal
+#pragma unroll
+                for (int w = 16; w > 0; w >>= 1) {
+                    const int c = __popc((bal >> pos) & ((1u << w) - 1u));
+                    if (rk >= c) {
+                        rk -= c;
+                        pos += w;
+                    }
+                }
+                const int64_t in = ibase + (int64_t)(st * 32 + pos) * W;
+                const int64_t o = (int64_t)(obase + k) * W;
+                constexpr int C = WT != 0 ? WT : 8;  // words in flight per lane
+#pragma unroll 1
+                for (int w0 = 0; w0 < W; w0 += C) {
+                    uint32_t v[C];
+#pragma unroll
+                    for (int w = 0; w < C; ++w)
+                        if (WT != 0 || w0 + w < W)
+                            v[w] = __ldg(src + in + w0 + w);
+#pragma unroll
+                    for (int w = 0; w < C; ++w)
+                        if (WT != 0 || w0 + w < W)
+                            dst[o + w0 + w] = v[w];
+                }
+            }
+        }
+    } else {
+        // Many selected: the warp's 1024 elements are 1024 W consecutive
+        // words of arr. Lanes walk them 32 words apart, R words each per
+        // round: all R loads (only words of selected elements) before the R
+        // stores, so a warp keeps R loads in flight. Word q belongs to the
+        // warp's element le = q / W, of step le / 32; its packed place is the
+        // step's count before it plus the selected lanes of its step below it.
+        const int total = 1024 * W;  // a multiple of 32 R
+#pragma unroll 1
+        for (int q0 = 0; q0 < total; q0 += 32 * R) {
+            uint32_t v[R];
+            unsigned bl[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int q = q0 + 32 * r + lane;
+                const int le = WT != 0 ? q / (WT != 0 ? WT : 1) : (int)__umulhi((uint32_t)q, recip);  // exact: q < 2^32 / W
+                bl[r] = __shfl_sync(kFull, my_bal, le >> 5);
+                v[r] = 0u;
+                if ((bl[r] >> (le & 31)) & 1u)
+                    v[r] = __ldg(src + ibase + q);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int q = q0 + 32 * r + lane;
+                const int le = WT != 0 ? q / (WT != 0 ? WT : 1) : (int)__umulhi((uint32_t)q, recip);
+                const uint32_t before = __shfl_sync(kFull, my_before, le >> 5);
+                const int l = le & 31;
+                if ((bl[r] >> l) & 1u)
+                    dst[(int64_t)(obase + before + __popc(bl[r] & ((1u << l) - 1u))) * W + (q - le * W)] = v[r];
+            }
+        }
+    }
+    // The copy's extra chunk (last warp only, when hf + elems passes the tile).
+    if (!FAST && warp == kWarps - 1 && hf + elems > kTE) {
+        const int bb = wstart + 1024 + lane;
+        const int e = bb - hf;
+        const bool sel = (unsigned)e < (unsigned)elems && fb[bb] != 0;
+        const unsigned bal = __ballot_sync(kFull, sel);
+        const int64_t xbase = (t0 + wstart + 1024 - hf) * (int64_t)W;
+        const uint32_t xo = obase + warp_cnt;
+        for (int j = lane; j < 32 * W; j += 32) {
+            const int el = WT != 0 ? j / (WT != 0 ? WT : 1) : (int)__umulhi((uint32_t)j, recip);
+            if ((bal >> el) & 1u)
+                dst[(int64_t)(xo + __popc(bal & ((1u << el) - 1u))) * W + (j - el * W)] = src[xbase + j];
+        }
+    }
+    if (g == ntiles - 1 && threadIdx.x == 0)
+        *a.num_out = (int32_t)(G + agg);
+}
+
+template <int WT>
+#ifndef MT_SEL_WORDS_MINB
+#define MT_SEL_WORDS_MINB 4
+#endif
+__global__ void __launch_bounds__(kThreads, MT_SEL_WORDS_MINB) k_select_words(SelArgs a, SelWords sw) {
+    pdl_prologue();
+    __shared__ __align__(128) SelWordsSmem sm;
+    const int32_t n32 = *a.n_dev;
+    const int64_t n = n32 > 0 ? n32 : 0;
+    const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
+    const int hf = (int)(reinterpret_cast<uintptr_t>(a.flags) & 15u);
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar_f, 1);
+        fence_mbar_init();
+    }
+    uint32_t phase = 0;
+    for (;;) {
+        if (threadIdx.x == 0)
+            sm.tile = (int64_t)atomicAdd(a.counter, 1ull);
+        __syncthreads();  // tile id visible; everyone is done with the last tile
+        const int64_t g = sm.tile;
+        if (g >= ntiles)
+            break;
+        const int64_t t0 = g * kSelTE;
+        const int elems = (int)((n - t0 < kSelTE) ? n - t0 : kSelTE);
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            const uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
+            mbar_arrive_expect_tx(&sm.bar_f, fbytes);
+            bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
+        }
+        bool ok = true;
+        if (threadIdx.x < 32)
+            ok = mbar_wait(&sm.bar_f, phase, kCopyWaitLimit);
+        if (__syncthreads_or(!ok)) {  // block-uniform: the flags did not arrive
+            if (threadIdx.x == 0) {
+                atomicCAS(&g_mt_err, 0, kErrTimeout);
+                mbar_wait(&sm.bar_f, phase, kCopyWaitLimit);  // drain the copy before leaving
+            }
+            return;
+        }
+        if (elems == kSelTE && hf == 0)
+            select_words_tile<true, WT>(sm, a, sw.words, sw.recip, g, ntiles, elems, hf);
+        else
+            select_words_tile<false, WT>(sm, a, sw.words, sw.recip, g, ntiles, elems, hf);
+        phase ^= 1u;
+        fence_proxy_async_smem();  // this thread's shared reads precede the next bulk copy
+    }
+}
+
+template <int WT>
+static cudaError_t launch_words_select(const SelArgs &a, const SelWords &sw, const Launch &L) {
+    static PerDevice per_sm;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    int blocks = per_sm.get(dev);
+    if (blocks == 0) {
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_words<WT>, kThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        blocks = b > 0 ? b : 1;
+        per_sm.set(dev, blocks);
+    }
+    e = launch_pdl(k_select_words<WT>, (unsigned)(L.sm_count * blocks), kThreads, 0, L.stream, a, sw);
+    note_launch();
+    return e;
+}
+
 int64_t select_tile_elems() { return kSelTE; }
 int select_rec_slots() { return Status<uint32_t>::kSlots; }
 
@@ -283,7 +555,23 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
-    return elem_bytes == 8 ? launch_staged_select<uint64_t>(a, L) : launch_staged_select<uint32_t>(a, L);
+    if (elem_bytes == 4)
+        return launch_staged_select<uint32_t>(a, L);
+    if (elem_bytes == 8)
+        return launch_staged_select<uint64_t>(a, L);
+    SelWords sw;
+    sw.words = elem_bytes / 4;
+    sw.recip = (uint32_t)((0x100000000ull + (uint64_t)sw.words - 1u) / (uint64_t)sw.words);
+    switch (sw.words) {  // the struct sizes the page names: 3, 4 and 6 words; others at run time
+    case 3:
+        return launch_words_select<3>(a, sw, L);
+    case 4:
+        return launch_words_select<4>(a, sw, L);
+    case 6:
+        return launch_words_select<6>(a, sw, L);
+    default:
+        return launch_words_select<0>(a, sw, L);
+    }
 }
 
 cudaError_t select_take_error(int *code) {

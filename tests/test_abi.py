@@ -124,7 +124,10 @@ def test_select_host_checks(lib):
 def test_select_wide_host_checks(lib):
     f = lib.mt_select_wide
     assert f(A, B, S, N, S, N, 3, None) == ARG
-    assert f(A, B, S, N, S, N, 16, None) == ARG
+    assert f(A, B, S, N, S, N, 0, None) == ARG
+    assert f(A, B, S, N, S, N, 6, None) == ARG    # structs are whole 32-bit words
+    assert f(A, B, S, N, S, N, 260, None) == ARG  # at most 64 words
+    assert f(A + 2, B, S, N, S, N, 12, None) == ALIGN  # structs: 4-byte aligned arr
     assert f(A, B, A, N, S, N, 8, None) == ALIAS
     assert f(A + 4, B, S, N, S, N, 8, None) == ALIGN  # 8-byte elements: arr 8-byte aligned
     assert f(A, B, S + 4, N, S, N, 8, None) == ALIGN  # ... and out

@@ -126,6 +126,32 @@ def test_select_wide_timeout_reported_then_recovers(mt):
     assert torch.equal(out[:k].cpu().view(torch.int64), want.view(torch.int64))
 
 
+@pytest.mark.parametrize("words", [3, 5])
+def test_select_struct_timeout_reported_then_recovers(mt, words):
+    """Struct elements (flags staged, values read after the look-back), with
+    W known at compile time (3) and at run time (5)."""
+    n = 1 << 20
+    vals = workloads.randint((n, words), 11, -(2**31), 2**31 - 1, "i32")
+    flags = workloads.bernoulli_u8(n, 0.5, 12)
+    arr, fl = vals.cuda(), flags.cuda()
+    out = torch.empty_like(arr)
+    num = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
+    n_dev = torch.tensor([n], dtype=torch.int32, device="cuda")
+    try:
+        mt.mt_scan_debug_lookback(skip_publish_tile=2, spin_limit=4096)
+        mt.mt_select_wide(arr, fl, out, num, scratch, n_dev)
+        assert mt.mt_scan_status() == mt.MT_ERR_LOOKBACK_TIMEOUT
+    finally:
+        mt.mt_scan_debug_lookback(-1, 0)
+    mt.mt_select_wide(arr, fl, out, num, scratch, n_dev)
+    assert mt.mt_scan_status() == 0
+    k = int(num.item())
+    want = vals[flags.bool()]
+    assert k == want.shape[0]
+    assert torch.equal(out[:k].cpu(), want)
+
+
 def test_reduce_by_key_timeout_reported_then_recovers(mt):
     n = 1 << 20
     keys, vals = workloads.runs(n, 8.0, 11, "i32", "i32")

@@ -126,6 +126,31 @@ def test_fuzz_select(mt, case):
 
 
 @pytest.mark.parametrize("case", range(16))
+def test_fuzz_select_struct(mt, case):
+    """Struct elements of 3 to 64 words at random 4-byte offsets of arr and
+    out, flags at any offset, every selection density from none to all."""
+    rng = np.random.default_rng(6500 + case)
+    words = [3, 4, 5, 6, 7, 8, 12, 33, 64][rng.integers(9)]
+    n = log_uniform(rng, 1, (1 << 22) // words)
+    p = [0.0, 0.003, 0.05, 0.3, 0.9, 1.0][rng.integers(6)]
+    vals = workloads.randint((n * words,), 6600 + case, -(2**31), 2**31 - 1, "i32")
+    flags = workloads.bernoulli_u8(n, p, 6700 + case)
+    arr = to_dev(vals, int(rng.integers(4))).view(n, words)
+    fl = to_dev(flags, int(rng.integers(16)))
+    out = to_dev(torch.zeros_like(vals), int(rng.integers(4))).view(n, words)
+    num = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    scr = mt.alloc_scratch(n, torch.int32, mt.MT_SCRATCH_SELECT)
+    nd = torch.tensor([n], dtype=torch.int32, device="cuda")
+    mt.mt_select_wide(arr, fl, out, num, scr, nd)
+    torch.cuda.synchronize()
+    assert mt.mt_scan_status() == 0
+    ref, k = oracle.select_wide(vals.numpy(), flags.numpy(), n, 4 * words)
+    assert int(num.item()) == k
+    got = out[:k].cpu().numpy().view(np.uint8).reshape(k, 4 * words)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("case", range(16))
 def test_fuzz_reduce_by_key(mt, case):
     rng = np.random.default_rng(7000 + case)
     n = log_uniform(rng, 1, 1 << 21)

@@ -116,3 +116,76 @@ def test_select_wide_any_16_byte_phase(mt, arr_off, flag_off, n):
         k = int(num.item())
         assert obuf[0].item() == SENT and torch.all(obuf[1 + k:] == SENT).item()
         check(out, k, vals, flags, n)
+
+
+def run_select_struct(mt, vals, flags, n, arr_off=0, flag_off=0, out_off=0):
+    """vals: [cap, W] int32 on the CPU (one struct per row); the device
+    copies start arr_off / flag_off / out_off elements (32-bit words for
+    arr and out, bytes for flags) past a 16-byte boundary."""
+    cap, words = vals.shape
+    abuf = torch.zeros(cap * words + arr_off, dtype=torch.int32, device="cuda")
+    arr = abuf[arr_off:].view(cap, words)
+    arr.copy_(vals.cuda())
+    fbuf = torch.zeros(cap + flag_off, dtype=torch.uint8, device="cuda")
+    fl = fbuf[flag_off:]
+    fl.copy_(flags.cuda())
+    obuf = torch.full((cap * words + out_off + 16,), 0x7BADBAD0, dtype=torch.int32, device="cuda")
+    out = obuf[out_off:out_off + cap * words].view(cap, words)
+    num = torch.full((1,), -9, dtype=torch.int32, device="cuda")
+    scr = mt.alloc_scratch(max(cap, 1), torch.int32, mt.MT_SCRATCH_SELECT)
+    scr.fill_(-1)
+    nd = torch.tensor([n], dtype=torch.int32, device="cuda")
+    mt.mt_select_wide(arr, fl, out, num, scr, nd)
+    torch.cuda.synchronize()
+    assert mt.mt_scan_status() == 0
+    k = int(num.item())
+    assert torch.all(obuf[out_off + k * words:] == 0x7BADBAD0).item(), "tail of out was touched"
+    assert torch.all(obuf[:out_off] == 0x7BADBAD0).item()
+    ref, kr = oracle.select_wide(vals.numpy(), flags.numpy(), n, 4 * words)
+    assert k == kr, f"num_out {k} != {kr}"
+    got = out[:k].cpu().contiguous().numpy().view(np.uint8).reshape(k, 4 * words)
+    bad = np.nonzero((got != ref).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} mismatched structs; first at {bad[0] if bad.size else -1}"
+
+
+@pytest.mark.parametrize("words", [3, 4, 5, 6, 64])  # 12 to 256 bytes; 5 and 64: W at run time
+@pytest.mark.parametrize("n", [0, 1, 17, 8191, 8192, 8193, 100003])
+@pytest.mark.parametrize("p", [0.01, 0.5, 1.0])
+def test_select_struct_sizes(mt, words, n, p):
+    cap = n + 29
+    if words == 64 and n > 10000:
+        cap = n + 1
+    vals = workloads.randint((cap, words), n + 7 * words, -(2**31), 2**31 - 1, "i32")
+    flags = workloads.bernoulli_u8(cap, p, n + 8)
+    run_select_struct(mt, vals, flags, n)
+
+
+@pytest.mark.parametrize("words", [3, 4, 5])
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 7, 0), (0, 0, 3), (3, 15, 1)])
+@pytest.mark.parametrize("n", [8177, 8193, 3 * 8192 - 1])
+def test_select_struct_offsets_and_tile_edges(mt, words, offs, n):
+    """arr and out 4 bytes to 12 bytes past a 16-byte boundary, flags at any
+    offset; the sizes put the flags' extra 16-byte chunk at a tile's end."""
+    vals = workloads.randint((n, words), 90 + words, -(2**31), 2**31 - 1, "i32")
+    for p in (0.5, 1.0):
+        flags = workloads.bernoulli_u8(n, p, 91 + n)
+        run_select_struct(mt, vals, flags, n, *offs)
+
+
+def test_select_struct_large(mt):
+    """2^24 12-byte structs (a 3-word vector) at p = 0.5; successive
+    structs start at every 4-byte phase of a 16-byte boundary."""
+    n = 1 << 24
+    vals = workloads.randint((n, 3), 95, -(2**31), 2**31 - 1, "i32")
+    flags = workloads.bernoulli_u8(n, 0.5, 96)
+    run_select_struct(mt, vals, flags, n)
+
+
+def test_select_struct_float_fields_move_as_bits(mt):
+    """A 16-byte struct of f32 fields (NaN payloads, -0.0) copied bit for bit."""
+    n = 50000
+    bits = workloads.randint((n, 4), 97, -(2**31), 2**31 - 1, "i32")
+    bits[::5, 1] = 0x7FC0BEEF
+    bits[::3, 2] = -(2**31)
+    flags = workloads.bernoulli_u8(n, 0.3, 98)
+    run_select_struct(mt, bits, flags, n)
