@@ -256,13 +256,9 @@ __global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_st
 // the look-back gives its output offset, and then each warp copies its
 // selected elements straight from arr to out. Each warp first takes the
 // ballots of its 32 steps of 32 elements (lane s keeps step s's ballot and
-// the count of selected elements before it). A warp with many selected
-// elements then walks its 1024 W consecutive words with lane-consecutive
-// words (coalesced loads and stores, several loads in flight per lane, the
-// words of unselected elements skipped); a warp with few has each lane copy
-// one selected element, found by a search over those counts, so a sparse
-// selection reads little more than its own sectors. WT: W known at compile
-// time (0: W and its reciprocal, for word -> element, at run time).
+// the count of selected elements before it); then lane k copies the warp's
+// k-th selected element, E elements per lane per round, all their words in
+// flight together. WT: W known at compile time (0: at run time).
 struct SelWordsSmem {
     uint4 flags[kSelChunks + 2];  // as in SelStagedSmem
     uint64_t bar_f;
@@ -272,12 +268,21 @@ struct SelWordsSmem {
 };
 
 struct SelWords {
-    int words;       // W
-    uint32_t recip;  // ceil(2^32 / W): word j of a step belongs to element umulhi(j, recip)
+    int words;  // W
 };
 
+// Selected elements per lane per round, and resident CTAs per SM asked of
+// the compiler, per struct size (measured at p = 0.5 and 0.01 on 2^28
+// structs: 12 bytes best at 3 and 5, 16 bytes at 3 and 4; no spills).
+__host__ __device__ constexpr int sel_words_e(int wt) { return wt == 3 || wt == 4 ? 3 : (wt == 6 ? 2 : 1); }
+#ifndef MT_SEL_WORDS_MINB
+__host__ __device__ constexpr int sel_words_minb(int wt) { return wt == 3 ? 5 : 4; }
+#else
+__host__ __device__ constexpr int sel_words_minb(int) { return MT_SEL_WORDS_MINB; }
+#endif
+
 template <bool FAST, int WT>
-__device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArgs &a, int W_rt, uint32_t recip,
+__device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArgs &a, int W_rt,
                                                   int64_t g, int64_t ntiles, int elems, int hf_) {
     constexpr int kTE = (int)kSelTE;
     const int W = WT != 0 ? WT : W_rt;
@@ -338,20 +343,24 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
     // selected lanes of its step below it.
     const int64_t ibase = (t0 + wstart - hf) * (int64_t)W;  // word 0 of the warp's element 0
     const uint32_t obase = G + wpre;
-#ifndef MT_SEL_WORDS_R
-#define MT_SEL_WORDS_R 8
+    // Lane k of a round copies the warp's k-th selected element: a 5-step
+    // shuffle search over the step counts finds its step, a 5-step popcount
+    // search in that step's ballot its lane. Every lane has work at any
+    // density, the search is paid once per element (not per word), and E
+    // elements' W words are all loaded before any is stored. The words of one
+    // element are adjacent and the elements of a round nearly so, so the
+    // round's loads and stores touch few sectors beyond the ones they need.
+#ifdef MT_SEL_WORDS_E
+    constexpr int E = MT_SEL_WORDS_E;
+#else
+    constexpr int E = sel_words_e(WT);  // selected elements per lane per round
 #endif
-#ifndef MT_SEL_WORDS_SPARSE
-#define MT_SEL_WORDS_SPARSE 512
-#endif
-    constexpr int R = MT_SEL_WORDS_R;
-    // per-element rounds (warp_cnt / 32) against word rounds (1024 W / 32 R), halved
-    if (warp_cnt * (uint32_t)R <= (uint32_t)MT_SEL_WORDS_SPARSE * (uint32_t)W) {
-        // Few selected: lane k copies the warp's k-th selected element, all
-        // its words loaded before any is stored (the words of one element
-        // are adjacent; different elements rarely share a sector here).
-        for (uint32_t k0 = 0; k0 < warp_cnt; k0 += 32) {
-            const uint32_t k = k0 + lane;
+    constexpr int C = WT != 0 ? WT : 8;  // words in flight per element (run time W: chunks of 8)
+    for (uint32_t k0 = 0; k0 < warp_cnt; k0 += 32 * E) {
+        int el[E];  // the warp-local element of this lane's x-th selected element, -1 past the count
+#pragma unroll
+        for (int x = 0; x < E; ++x) {
+            const uint32_t k = k0 + 32 * x + lane;
             int st = 0;  // the step holding selected element k: the last with my_before <= k
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1)
@@ -359,77 +368,48 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
                     st += d;
             const unsigned bal = __shfl_sync(kFull, my_bal, st);
             int rk = (int)(k - __shfl_sync(kFull, my_before, st));  // its rank within the step
-            if (k < warp_cnt) {
-                int pos = 0;  // the rk-th set bit of bal
+            int pos = 0;  // the rk-th set bit of bal
 #pragma unroll
-                for (int w = 16; w > 0; w >>= 1) {
-                    const int c = __popc((bal >> pos) & ((1u << w) - 1u));
-                    if (rk >= c) {
-                        rk -= c;
-                        pos += w;
-                    }
-                }
-                const int64_t in = ibase + (int64_t)(st * 32 + pos) * W;
-                const int64_t o = (int64_t)(obase + k) * W;
-                constexpr int C = WT != 0 ? WT : 8;  // words in flight per lane
-#pragma unroll 1
-                for (int w0 = 0; w0 < W; w0 += C) {
-                    uint32_t v[C];
-#pragma unroll
-                    for (int w = 0; w < C; ++w)
-                        if (WT != 0 || w0 + w < W)
-                            v[w] = __ldg(src + in + w0 + w);
-#pragma unroll
-                    for (int w = 0; w < C; ++w)
-                        if (WT != 0 || w0 + w < W)
-                            dst[o + w0 + w] = v[w];
+            for (int w = 16; w > 0; w >>= 1) {
+                const int c = __popc((bal >> pos) & ((1u << w) - 1u));
+                if (rk >= c) {
+                    rk -= c;
+                    pos += w;
                 }
             }
+            el[x] = k < warp_cnt ? st * 32 + pos : -1;
         }
-    } else {
-        // Many selected: the warp's 1024 elements are 1024 W consecutive
-        // words of arr. Lanes walk them 32 words apart, R words each per
-        // round: all R loads (only words of selected elements) before the R
-        // stores, so a warp keeps R loads in flight. Word q belongs to the
-        // warp's element le = q / W, of step le / 32; its packed place is the
-        // step's count before it plus the selected lanes of its step below it.
-        const int total = 1024 * W;  // a multiple of 32 R
 #pragma unroll 1
-        for (int q0 = 0; q0 < total; q0 += 32 * R) {
-            uint32_t v[R];
-            unsigned bl[R];
+        for (int w0 = 0; w0 < W; w0 += C) {
+            uint32_t v[E][C];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int q = q0 + 32 * r + lane;
-                const int le = WT != 0 ? q / (WT != 0 ? WT : 1) : (int)__umulhi((uint32_t)q, recip);  // exact: q < 2^32 / W
-                bl[r] = __shfl_sync(kFull, my_bal, le >> 5);
-                v[r] = 0u;
-                if ((bl[r] >> (le & 31)) & 1u)
-                    v[r] = __ldg(src + ibase + q);
-            }
+            for (int x = 0; x < E; ++x)
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int q = q0 + 32 * r + lane;
-                const int le = WT != 0 ? q / (WT != 0 ? WT : 1) : (int)__umulhi((uint32_t)q, recip);
-                const uint32_t before = __shfl_sync(kFull, my_before, le >> 5);
-                const int l = le & 31;
-                if ((bl[r] >> l) & 1u)
-                    dst[(int64_t)(obase + before + __popc(bl[r] & ((1u << l) - 1u))) * W + (q - le * W)] = v[r];
+                for (int w = 0; w < C; ++w)
+                    if (el[x] >= 0 && (WT != 0 || w0 + w < W))
+                        v[x][w] = __ldg(src + ibase + (int64_t)el[x] * W + w0 + w);
+#pragma unroll
+            for (int x = 0; x < E; ++x) {
+                const int64_t o = (int64_t)(obase + k0 + 32 * x + lane) * W + w0;
+#pragma unroll
+                for (int w = 0; w < C; ++w)
+                    if (el[x] >= 0 && (WT != 0 || w0 + w < W))
+                        dst[o + w] = v[x][w];
             }
         }
     }
-    // The copy's extra chunk (last warp only, when hf + elems passes the tile).
+    // The copy's extra chunk (last warp only, when hf + elems passes the
+    // tile): at most 15 elements, one per lane.
     if (!FAST && warp == kWarps - 1 && hf + elems > kTE) {
         const int bb = wstart + 1024 + lane;
         const int e = bb - hf;
         const bool sel = (unsigned)e < (unsigned)elems && fb[bb] != 0;
         const unsigned bal = __ballot_sync(kFull, sel);
-        const int64_t xbase = (t0 + wstart + 1024 - hf) * (int64_t)W;
-        const uint32_t xo = obase + warp_cnt;
-        for (int j = lane; j < 32 * W; j += 32) {
-            const int el = WT != 0 ? j / (WT != 0 ? WT : 1) : (int)__umulhi((uint32_t)j, recip);
-            if ((bal >> el) & 1u)
-                dst[(int64_t)(xo + __popc(bal & ((1u << el) - 1u))) * W + (j - el * W)] = src[xbase + j];
+        if (sel) {
+            const int64_t in = ibase + (int64_t)(1024 + lane) * W;
+            const int64_t o = (int64_t)(obase + warp_cnt + __popc(bal & ((1u << lane) - 1u))) * W;
+            for (int w = 0; w < W; ++w)
+                dst[o + w] = __ldg(src + in + w);
         }
     }
     if (g == ntiles - 1 && threadIdx.x == 0)
@@ -437,10 +417,7 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
 }
 
 template <int WT>
-#ifndef MT_SEL_WORDS_MINB
-#define MT_SEL_WORDS_MINB 4
-#endif
-__global__ void __launch_bounds__(kThreads, MT_SEL_WORDS_MINB) k_select_words(SelArgs a, SelWords sw) {
+__global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(SelArgs a, SelWords sw) {
     pdl_prologue();
     __shared__ __align__(128) SelWordsSmem sm;
     const int32_t n32 = *a.n_dev;
@@ -478,9 +455,9 @@ __global__ void __launch_bounds__(kThreads, MT_SEL_WORDS_MINB) k_select_words(Se
             return;
         }
         if (elems == kSelTE && hf == 0)
-            select_words_tile<true, WT>(sm, a, sw.words, sw.recip, g, ntiles, elems, hf);
+            select_words_tile<true, WT>(sm, a, sw.words, g, ntiles, elems, hf);
         else
-            select_words_tile<false, WT>(sm, a, sw.words, sw.recip, g, ntiles, elems, hf);
+            select_words_tile<false, WT>(sm, a, sw.words, g, ntiles, elems, hf);
         phase ^= 1u;
         fence_proxy_async_smem();  // this thread's shared reads precede the next bulk copy
     }
@@ -561,7 +538,6 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
         return launch_staged_select<uint64_t>(a, L);
     SelWords sw;
     sw.words = elem_bytes / 4;
-    sw.recip = (uint32_t)((0x100000000ull + (uint64_t)sw.words - 1u) / (uint64_t)sw.words);
     switch (sw.words) {  // the struct sizes the page names: 3, 4 and 6 words; others at run time
     case 3:
         return launch_words_select<3>(a, sw, L);
