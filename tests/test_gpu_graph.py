@@ -29,6 +29,10 @@ def test_calls_replay_in_a_cuda_graph(mt):
     fl = torch.empty(n, dtype=torch.uint8, device="cuda")
     keys = torch.empty(n, dtype=i32, device="cuda")
     vals = torch.empty(n, dtype=i32, device="cuda")
+    st = torch.empty((n, 3), dtype=i32, device="cuda")  # 12-byte structs
+    sto = torch.empty_like(st)
+    num3 = torch.zeros(1, dtype=i32, device="cuda")
+    st_scr = mt.alloc_scratch(n, i32, mt.MT_SCRATCH_SELECT)
     so, lo, lo2 = torch.empty_like(short_rows), torch.empty_like(long_rows), torch.empty_like(long_rows)
     ao, vo, ko, kvo = torch.empty_like(a), torch.empty_like(v), torch.empty_like(keys), torch.empty_like(vals)
     red = torch.empty(1, dtype=i32, device="cuda")
@@ -47,6 +51,7 @@ def test_calls_replay_in_a_cuda_graph(mt):
         mt.mt_exclusive_scan(a, ao, scan_scr, nd, "add")
         mt.mt_reduce(a, red, red_scr, nd, "max")
         mt.mt_select(v, fl, vo, num, sel_scr, nd)
+        mt.mt_select_wide(st, fl, sto, num3, st_scr, nd)
         mt.mt_reduce_by_key_add(keys, vals, ko, kvo, nr, rbk_scr, nd)
 
     def fill(seed):
@@ -57,6 +62,8 @@ def test_calls_replay_in_a_cuda_graph(mt):
         }
         x["v"], x["fl"] = workloads.select_inputs(n, 0.3, seed + 3)
         x["keys"], x["vals"] = workloads.runs(n, 5.0, seed + 4, "i32", "i32")
+        x["st"] = workloads.randint((n, 3), seed + 5, -(2**31), 2**31 - 1, "i32")
+        st.copy_(x["st"])
         short_rows.copy_(x["short"])
         long_rows.copy_(x["long"])
         a.copy_(x["a"])
@@ -73,6 +80,9 @@ def test_calls_replay_in_a_cuda_graph(mt):
         assert_scan_matches(ao, x["a"], n, "i32", "add")
         assert_reduce_matches(red, x["a"], n, "i32", "max")
         assert_select_matches(vo, num, x["v"], x["fl"], n)
+        ref3, k3 = oracle.select_wide(x["st"].numpy(), x["fl"].numpy(), n, 12)
+        assert int(num3.item()) == k3
+        assert np.array_equal(sto[:k3].cpu().numpy().view(np.uint8).reshape(k3, 12), ref3)
         want_k, want_v, r = oracle.reduce_by_key_add(x["keys"], x["vals"], n, "i32", "i32")
         assert int(nr.item()) == r
         assert np.array_equal(ko[:r].cpu().numpy(), want_k)
