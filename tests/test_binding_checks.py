@@ -47,3 +47,17 @@ def test_dtype_and_shape_mismatches_are_refused():
         mt.mt_scan_rows(torch.zeros(2, 8), torch.zeros(2, 9), True)
     with pytest.raises(ValueError):
         mt.mt_scan_rows(torch.zeros(4, 8)[:, ::2], torch.zeros(4, 4), True)
+
+
+def test_select_wide_struct_sizes_must_match():
+    """An [n, W] tensor is n structs of W elements; out's structs must have
+    arr's size (a 12-byte arr into 8-byte or 16-byte out is refused)."""
+    nd, one = torch.zeros(1, dtype=I32), torch.zeros(1, dtype=I32)
+    scr = torch.zeros(64, dtype=torch.int64)
+    fl = torch.zeros(8, dtype=torch.uint8)
+    arr = torch.zeros(8, 3, dtype=I32)
+    for out in (torch.zeros(8, dtype=torch.int64), torch.zeros(8, 4, dtype=I32), torch.zeros(8, 6, dtype=torch.int16)[:, :3]):
+        with pytest.raises(ValueError):
+            mt.mt_select_wide(arr, fl, out, one, scr, nd)
+    with pytest.raises(ValueError, match="arr must be contiguous"):
+        mt.mt_select_wide(torch.zeros(8, 6, dtype=I32)[:, :3], fl, torch.zeros(8, 3, dtype=I32), one, scr, nd)
