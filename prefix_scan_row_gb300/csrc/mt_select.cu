@@ -335,12 +335,6 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
     }
     const uint32_t warp_cnt = __shfl_sync(kFull, my_before, 31);
     my_before -= __popc(my_bal);  // exclusive
-    // The warp's 1024 elements are 1024 W consecutive words of arr. Lanes
-    // walk them 32 words apart, R words each per round: all R loads (only
-    // words of selected elements) before the R stores, so a warp keeps R
-    // loads in flight. Word q belongs to the warp's element le = q / W, of
-    // step le / 32; its packed place is the step's count before it plus the
-    // selected lanes of its step below it.
     const int64_t ibase = (t0 + wstart - hf) * (int64_t)W;  // word 0 of the warp's element 0
     const uint32_t obase = G + wpre;
     // Lane k of a round copies the warp's k-th selected element: a 5-step
