@@ -621,7 +621,7 @@ def run_suite(args):
         timeit(f"select_wide f64 n={ns} p={p}", lambda: mt.mt_select_wide(v, f, o, num, scr, nd),
                9 * ns + 8 * k, ns)
         del v, f, o, scr
-    for words in (3, 4):  # struct elements (12- and 16-byte vectors): flags staged, values read once selected
+    for words in (3, 4, 6, 8):  # struct elements (12- to 32-byte structs): flags staged, values read once selected
         for p in (0.5, 0.01):
             name = f"select_wide struct {4 * words}B n={ns} p={p}"
             if not wanted(name):

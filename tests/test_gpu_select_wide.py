@@ -148,7 +148,7 @@ def run_select_struct(mt, vals, flags, n, arr_off=0, flag_off=0, out_off=0):
     assert bad.size == 0, f"{bad.size} mismatched structs; first at {bad[0] if bad.size else -1}"
 
 
-@pytest.mark.parametrize("words", [3, 4, 5, 6, 64])  # 12 to 256 bytes; 5 and 64: W at run time
+@pytest.mark.parametrize("words", [3, 4, 5, 6, 8, 64])  # 12 to 256 bytes; 5 and 64: W at run time
 @pytest.mark.parametrize("n", [0, 1, 17, 8191, 8192, 8193, 100003])
 @pytest.mark.parametrize("p", [0.01, 0.5, 1.0])
 def test_select_struct_sizes(mt, words, n, p):
@@ -160,7 +160,7 @@ def test_select_struct_sizes(mt, words, n, p):
     run_select_struct(mt, vals, flags, n)
 
 
-@pytest.mark.parametrize("words", [3, 4, 5])
+@pytest.mark.parametrize("words", [3, 4, 5, 8])
 @pytest.mark.parametrize("offs", [(1, 0, 0), (0, 7, 0), (0, 0, 3), (3, 15, 1)])
 @pytest.mark.parametrize("n", [8177, 8193, 3 * 8192 - 1])
 def test_select_struct_offsets_and_tile_edges(mt, words, offs, n):
