@@ -269,6 +269,7 @@ struct SelWordsSmem {
 
 struct SelWords {
     int words;  // W
+    int vec;    // W a multiple of 4 and arr, out 16-byte aligned: copy 16-byte vectors
 };
 
 // Selected elements per lane per round, and resident CTAs per SM asked of
@@ -282,7 +283,7 @@ __host__ __device__ constexpr int sel_words_minb(int) { return MT_SEL_WORDS_MINB
 #endif
 
 template <bool FAST, int WT>
-__device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArgs &a, int W_rt,
+__device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArgs &a, int W_rt, int vec,
                                                   int64_t g, int64_t ntiles, int elems, int hf_) {
     constexpr int kTE = (int)kSelTE;
     const int W = WT != 0 ? WT : W_rt;
@@ -373,6 +374,31 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
             }
             el[x] = k < warp_cnt ? st * 32 + pos : -1;
         }
+        if (WT == 0 && vec) {  // launch-uniform: 16-byte loads and stores (W at run time: 8 words and up)
+            const uint4 *src4 = reinterpret_cast<const uint4 *>(src);
+            uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
+            const int W4 = W / 4;
+            constexpr int C4 = C / 4 > 0 ? C / 4 : 1;  // (only W at run time takes this branch: C = 8)
+#pragma unroll 1
+            for (int w0 = 0; w0 < W4; w0 += C4) {
+                uint4 v[E][C4];
+#pragma unroll
+                for (int x = 0; x < E; ++x)
+#pragma unroll
+                    for (int w = 0; w < C4; ++w)
+                        if (el[x] >= 0 && (WT != 0 || w0 + w < W4))
+                            v[x][w] = __ldg(src4 + ibase / 4 + (int64_t)el[x] * W4 + w0 + w);
+#pragma unroll
+                for (int x = 0; x < E; ++x) {
+                    const int64_t o = (int64_t)(obase + k0 + 32 * x + lane) * W4 + w0;
+#pragma unroll
+                    for (int w = 0; w < C4; ++w)
+                        if (el[x] >= 0 && (WT != 0 || w0 + w < W4))
+                            dst4[o + w] = v[x][w];
+                }
+            }
+            continue;
+        }
 #pragma unroll 1
         for (int w0 = 0; w0 < W; w0 += C) {
             uint32_t v[E][C];
@@ -449,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(S
             return;
         }
         if (elems == kSelTE && hf == 0)
-            select_words_tile<true, WT>(sm, a, sw.words, g, ntiles, elems, hf);
+            select_words_tile<true, WT>(sm, a, sw.words, sw.vec, g, ntiles, elems, hf);
         else
-            select_words_tile<false, WT>(sm, a, sw.words, g, ntiles, elems, hf);
+            select_words_tile<false, WT>(sm, a, sw.words, sw.vec, g, ntiles, elems, hf);
         phase ^= 1u;
         fence_proxy_async_smem();  // this thread's shared reads precede the next bulk copy
     }
@@ -532,6 +558,8 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
         return launch_staged_select<uint64_t>(a, L);
     SelWords sw;
     sw.words = elem_bytes / 4;
+    sw.vec = (elem_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(arr) % 16 == 0 &&
+              reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1 : 0;
     switch (sw.words) {  // the struct sizes the page names: 3, 4 and 6 words; others at run time
     case 3:
         return launch_words_select<3>(a, sw, L);
