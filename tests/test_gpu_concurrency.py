@@ -60,6 +60,20 @@ def make_jobs(mt, t):
     jobs.append((lambda s: mt.mt_select(v, fl, vo, num, sscr, nd, stream=s),
                  lambda: assert_select_matches(vo, num, v_cpu, fl_cpu, cap)))
 
+    words = 3 + (t % 3) * 2  # 12-, 20- and 28-byte structs (W = 5, 7 at run time)
+    st_cpu = workloads.randint((cap, words), 450 + t, -(2**31), 2**31 - 1, "i32")
+    st = st_cpu.cuda()
+    sto = torch.empty_like(st)
+    num3 = torch.zeros(1, dtype=i32, device="cuda")
+    st_scr = mt.alloc_scratch(cap, i32, mt.MT_SCRATCH_SELECT)
+
+    def check_struct():
+        ref, k3 = oracle.select_wide(st_cpu.numpy(), fl_cpu.numpy(), cap, 4 * words)
+        assert int(num3.item()) == k3
+        assert np.array_equal(sto[:k3].cpu().numpy().view(np.uint8).reshape(k3, 4 * words), ref)
+
+    jobs.append((lambda s: mt.mt_select_wide(st, fl, sto, num3, st_scr, nd, stream=s), check_struct))
+
     k_cpu, kv_cpu = workloads.runs(cap, 6.0, 500 + t, "i32", "i32")
     k, kv = k_cpu.cuda(), kv_cpu.cuda()
     ko, kvo = torch.empty_like(k), torch.empty_like(kv)
