@@ -1,6 +1,7 @@
-"""All-core CPU row scan (``mt_cpu_allcore.c``, pthreads) -- a MEASUREMENT
-BASELINE for ``bench.py``'s CPU leg only. It is not the oracle (the oracle
-stays single-threaded and fp64) and the GPU product never imports it."""
+"""All-core CPU scans (``cpu_allcore.c``, pthreads): the row scan and the
+1-D exclusive scan -- a MEASUREMENT BASELINE for ``bench.py``'s CPU leg only.
+It is not the oracle (the oracle stays single-threaded and fp64) and the GPU
+product never imports it."""
 from __future__ import annotations
 
 import ctypes
@@ -10,9 +11,10 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "mt_cpu_allcore.c")
+_SRC = os.path.join(_HERE, "cpu_allcore.c")
 _LIB = os.path.join(_HERE, "libcpuallcore.so")
-_DT = {"f32": 0, "bf16": 1, "f16": 2}
+_DT = {"f32": 0, "bf16": 1, "f16": 2, "i32": 3, "i64": 4}
+_OP = {"add": 0, "min": 1, "max": 2}
 _lib = None
 
 
@@ -33,6 +35,9 @@ def _get():
         L.cpu_allcore_scan_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.cpu_allcore_scan_rows.restype = ctypes.c_int
+        L.cpu_allcore_exclusive_scan.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int]
+        L.cpu_allcore_exclusive_scan.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -60,4 +65,19 @@ def scan_rows(x, dtype: str, inclusive: bool, threads: int, out=None) -> np.ndar
                                       threads)
     if rc != 0:
         raise RuntimeError("cpu_allcore_scan_rows failed")
+    return y
+
+
+def exclusive_scan(x, n: int, dtype: str, op: str, threads: int, out=None) -> np.ndarray:
+    """Exclusive scan of the first n elements of a 1-D i32/i64/f32 array (a
+    CPU torch tensor or numpy array); returns out (the first n written)."""
+    if hasattr(x, "numpy"):
+        x = x.numpy()
+    a = np.ascontiguousarray(x)
+    if a.ndim != 1 or n < 0 or n > a.shape[0]:
+        raise ValueError("exclusive_scan: a 1-D array with at least n elements")
+    y = np.empty_like(a) if out is None else out
+    rc = _get().cpu_allcore_exclusive_scan(a.ctypes.data, y.ctypes.data, n, _DT[dtype], _OP[op], threads)
+    if rc != 0:
+        raise RuntimeError("cpu_allcore_exclusive_scan failed")
     return y

@@ -1,13 +1,16 @@
-"""The all-core CPU row scan that bench.py reports as a second CPU baseline
-must compute the row scan: checked against the oracle with the GPU path's
-tolerances, and its bf16/f16 rounding against torch's conversions."""
+"""The all-core CPU scans that bench.py reports as a second CPU baseline must
+compute the scans: the row scan checked against the oracle with the GPU
+path's tolerances and its bf16/f16 rounding against torch's conversions, the
+1-D exclusive scan against the oracle (bit-exact for integers and min/max,
+the f32 add bound otherwise)."""
 import numpy as np
 import pytest
 import torch
 
 import workloads
 from checks import assert_rows_close
-from oracle import allcore
+import oracle
+from baselines import allcore
 
 
 def as_tensor(y, dtype):
@@ -42,3 +45,22 @@ def test_allcore_rounding_is_torchs(dtype):
     assert torch.equal(got[~nan], ref[~nan])
     # out[0] = RN(0 + x0): the value itself, except that -0 becomes +0
     assert torch.equal(y[:, 0].view(torch.int16), (0.0 + x[:, 0].float()).to(tdt).view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype", ["i32", "i64", "f32"])
+@pytest.mark.parametrize("op", ["add", "min", "max"])
+@pytest.mark.parametrize("n,cap,threads", [(0, 5, 4), (1, 1, 4), (7, 9, 3), (100003, 100010, 16), (4096, 4096, 1)])
+def test_allcore_exclusive_scan_matches_oracle(dtype, op, n, cap, threads):
+    x = workloads.scan1d(dtype, capacity=cap, seed=50 + n)
+    y = allcore.exclusive_scan(x, n, dtype, op, threads)
+    want = oracle.exclusive_scan(x, n, dtype, op)
+    if dtype == "f32" and op == "add":
+        mag = np.concatenate([[0.0], np.cumsum(np.abs(x.numpy()[:n].astype(np.float64)))])[:n]
+        assert np.all(np.abs(y[:n].astype(np.float64) - want.astype(np.float64)) <= 1e-5 * mag + 1e-6)
+    else:
+        assert np.array_equal(y[:n], want)
+
+
+def test_allcore_exclusive_scan_wraps_like_the_oracle():
+    x = torch.full((1000,), 2**31 - 7, dtype=torch.int32)
+    assert np.array_equal(allcore.exclusive_scan(x, 1000, "i32", "add", 7), oracle.exclusive_scan(x, 1000, "i32", "add"))
