@@ -2,37 +2,41 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step is one pass of the row-wise scan over the bf16/f16 workload:
-[8192, 8192] exclusive and [4096, 4099] inclusive, each in bf16 and f16
-storage (N(0, 1) inputs, seed 1), f32 accumulation -- four mt_scan_rows calls.
-The metric is algorithmic HBM bytes (one read and one write of every element
-in its storage width) per second, in GB/s. Inputs are resident in HBM when
-the timed region starts; one step moves 671 MB, more than the 129 MB L2, and
-no buffer is touched twice within a step, so nothing is served from L2
-across iterations.
+One step is the device-wide 1-D exclusive scan workload, the largest of the
+library's configured workloads: capacity 2^28 with a live count
+n = 2^28 - 12345 held in device memory, i32 values uniform in [0, 15], f32
+uniform[-1, 1) and i64 uniform in [0, 2^20) (seed 3), and exclusive_scan
+add, min and max of each -- nine mt_exclusive_scan calls (each a status reset
+kernel and the single-pass scan kernel), 25.77 GB of algorithmic traffic.
+The metric is algorithmic HBM bytes (one read and one write of every live
+element in its storage width) per second, in GB/s. Inputs are resident in HBM
+when the timed region starts; every call moves 2.1 or 4.3 GB, many times the
+129 MB L2, so nothing is served from L2 across calls.
 
 Printed: one JSON line (rank 0). Besides the device-timed value it carries
-`e2e` (the same metric through the C ABI with host buffers: pinned host ->
-device copy, the four calls, device -> host copy, every step), `roofline` for
-the dominant kernel (the [8192, 8192] bf16 launch), `cpu_baseline` (the CPU
-oracle, single-threaded, on a bounded sample), `cpu_all_cores` (an all-core
-C row scan on the host, a second baseline), `clocks` sampled during the timed
-region and `gpu_launches` counted by the library.
+`e2e` (the same step through the C ABI from pinned host buffers: host ->
+device copy of the inputs, the nine calls, device -> host copy of the nine
+results, every step), `roofline` for the dominant kernel (the i64 add scan),
+`kernels` (every scan kernel on its configured workload: rows, long rows, the
+nine 1-D scans and select at both densities, each timed back to back over
+buffer sets larger than twice the L2), `cpu_baseline` (the CPU oracle, one
+thread), `cpu_all_cores` (an all-core C scan, a second baseline), `clocks`
+sampled during the timed region and `gpu_launches` counted by the library.
 
 `--impl reference` times the CPU oracle instead (the only reference this
 library has), on the same workload, metric and unit.
 
 With N > 1 (torchrun), every rank runs the same per-GPU workload (weak
-scaling: rows are independent and shard with no exchange); the time is the
-max over ranks and the value the bytes of all ranks over that time.
+scaling: the replicas are independent, no data crosses ranks); the time is
+the max over ranks and the value the bytes of all ranks over that time.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
-import re
 import statistics
 import sys
 import threading
@@ -51,38 +55,48 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
 
-# (name, rows, n, storage dtype, inclusive); the first is the dominant launch
-CALLS = [
-    ("bf16_8192x8192_excl", 8192, 8192, "bf16", False),
-    ("f16_8192x8192_excl", 8192, 8192, "f16", False),
-    ("bf16_4096x4099_incl", 4096, 4099, "bf16", True),
-    ("f16_4096x4099_incl", 4096, 4099, "f16", True),
-]
-DOMINANT = CALLS[0][0]
-WORKLOAD = ("row-wise sum scan, bf16 and f16 storage with f32 accumulation: "
-            "[8192,8192] exclusive + [4096,4099] inclusive (ragged, misaligned rows), "
-            "iid N(0,1) seed 1; one step = the 4 calls")
+N_LIVE = workloads.SCAN1D_LIVE
+CAPACITY = workloads.SCAN1D_CAPACITY
+DTYPES = ("i32", "f32", "i64")
+OPS = ("add", "min", "max")
+SIZE = {"i32": 4, "f32": 4, "i64": 8, "bf16": 2, "f16": 2}
+TORCH_DT = {"i32": torch.int32, "f32": torch.float32, "i64": torch.int64}
+# (dtype, op) of the step's calls, in launch order
+CALLS = [(d, op) for d in DTYPES for op in OPS]
+DOMINANT = ("i64", "add")
+WORKLOAD = ("device-wide 1-D exclusive_scan add/min/max: capacity 2^28, live count n = 2^28-12345 in "
+            "device memory; i32 uniform in [0,15], f32 uniform[-1,1), i64 uniform in [0,2^20), seed 3; "
+            "one step = the 9 calls (3 dtypes x 3 ops)")
+
+
+def scan_bytes(dtype, n=N_LIVE):
+    return 2 * SIZE[dtype] * n
 
 
 def call_bytes(rows, n, dtype):
-    return 2 * rows * n * (4 if dtype == "f32" else 2)
+    return 2 * rows * n * SIZE[dtype]
 
 
-STEP_BYTES = sum(call_bytes(r, n, d) for _, r, n, d, _ in CALLS)
-STEP_ELEMS = sum(r * n for _, r, n, _, _ in CALLS)
-DOM_BYTES = call_bytes(*CALLS[0][1:4])
-DOM_EVERY = 8  # steps per event-timed dominant launch
+STEP_BYTES = sum(scan_bytes(d) for d, _ in CALLS)
+STEP_ELEMS = N_LIVE * len(CALLS)
+DOM_BYTES = scan_bytes(DOMINANT[0])
+B2B_LAUNCHES = 20  # back-to-back calls per kernel entry
 
-KERNEL_SOURCES = ["prefix_scan_row_gb300/csrc/mt_internal.h", "prefix_scan_row_gb300/csrc/mt_tile.cuh",
-                  "prefix_scan_row_gb300/csrc/mt_lookback.cuh", "prefix_scan_row_gb300/csrc/mt_tilescan.cuh",
-                  "prefix_scan_row_gb300/csrc/mt_rows.cuh", "prefix_scan_row_gb300/csrc/mt_rows.cu"]
-PROFILE = "profiles/rows_bf16_8192x8192_excl.md"
+# Sources of each kernel family: a profile's counters hold while these are
+# unchanged (each sidecar in profiles/ stores the hash it was captured on).
+_CSRC = "prefix_scan_row_gb300/csrc/"
+FAMILY_SOURCES = {
+    "rows": ["mt_internal.h", "mt_tile.cuh", "mt_lookback.cuh", "mt_tilescan.cuh", "mt_rows.cuh", "mt_rows.cu",
+             "mt_staged.cuh"],
+    "scan1d": ["mt_internal.h", "mt_tile.cuh", "mt_lookback.cuh", "mt_staged.cuh", "mt_scan1d.cuh", "mt_scan1d.cu"],
+    "select": ["mt_internal.h", "mt_tile.cuh", "mt_lookback.cuh", "mt_select.cu"],
+}
 
 
-def kernel_source_hash():
+def kernel_source_hash(family):
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
+    for p in FAMILY_SOURCES[family]:
+        with open(os.path.join(ROOT, _CSRC + p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -96,18 +110,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None when that summary was taken on other kernel sources."""
+def profile_traffic(profile, family):
+    """Per-launch DRAM bytes (read + write) of a kernel from its ncu sidecar
+    (profiles/<name>.json), or None when there is none or it was captured on
+    other kernel sources."""
     try:
-        text = open(os.path.join(ROOT, PROFILE)).read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", profile + ".json")) as f:
+            side = json.load(f)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    h = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    if side.get("kernel_source_hash") != kernel_source_hash(family):
         return None
-    return int(m.group(1))
+    t = side.get("traffic_bytes_per_launch")
+    return int(t) if t is not None else None
 
 
 # ---------------------------------------------------------------------------
@@ -216,63 +231,198 @@ def barrier():
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the --impl reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample(host, frac):
-    """Scan the first `frac` of the rows of each of the step's tensors with the
-    single-threaded CPU oracle. Returns (seconds, algorithmic bytes, elements)."""
+def make_host_inputs():
+    """The step's three input arrays (the whole capacity), on the host."""
+    return {d: workloads.scan1d(d) for d in DTYPES}
+
+
+def oracle_sample(host, m):
+    """The oracle's exclusive scan of the first m live elements of each of the
+    step's nine calls. Returns (seconds, algorithmic bytes, elements)."""
     import oracle
-    secs = nbytes = elems = 0
-    for (name, r, n, d, inc), x in zip(CALLS, host):
-        rows = max(1, int(round(r * frac)))
-        xs = x[:rows]
+    secs = nbytes = 0
+    for d, op in CALLS:
         t = time.perf_counter()
-        oracle.scan_rows(xs, d, inc)
+        oracle.exclusive_scan(host[d], m, d, op)
         secs += time.perf_counter() - t
-        nbytes += call_bytes(rows, n, d)
-        elems += rows * n
-    return secs, nbytes, elems
+        nbytes += scan_bytes(d, m)
+    return secs, nbytes, m * len(CALLS)
 
 
 def calibrate_oracle(host):
     """Seconds one full step takes on the oracle, from a small sample."""
-    secs, nbytes, _ = oracle_sample(host, 16 / 4096)
+    m = 1 << 21
+    secs, nbytes, _ = oracle_sample(host, m)
     return secs * STEP_BYTES / nbytes
 
 
 def cpu_baseline(host, target_s=12.0):
     per_step = calibrate_oracle(host)
-    frac = min(1.0, target_s / per_step)
-    secs, nbytes, elems = oracle_sample(host, frac)
+    m = min(N_LIVE, max(1 << 20, int(N_LIVE * target_s / per_step)))
+    secs, nbytes, elems = oracle_sample(host, m)
     return {"value": nbytes / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "elements_per_s": elems / secs, "seconds": round(secs, 3),
-            "sample": f"first {frac:.4f} of the rows of each of the 4 tensors of one step "
-                      f"({elems} elements, {nbytes} algorithmic bytes), plain C, 1 thread"}
+            "sample": f"the first {m} live elements of each of the step's 9 calls ({elems} elements, "
+                      f"{nbytes} algorithmic bytes), plain C oracle, 1 thread"}
 
 
-def cpu_all_cores(host, reps=5):
-    """A second CPU baseline: the step's four row scans by an all-core C scan
-    (pthreads, f32 accumulation; oracle/mt_cpu_allcore.c), median of `reps`
-    whole steps. Not the oracle, and not a target."""
-    from oracle import allcore
+def cpu_all_cores(host, reps=3):
+    """A second CPU baseline: the step's nine exclusive scans by an all-core C
+    scan (pthreads, two-pass blocked; baselines/cpu_allcore.c), median of
+    `reps` whole steps. Not the oracle, and not a target."""
+    import numpy as np
+
+    from baselines import allcore
     cores = allcore.cores()
-    outs = [None] * len(host)
+    outs = {d: np.empty(host[d].shape, dtype=host[d].numpy().dtype) for d in DTYPES}
     times = []
     for _ in range(reps + 1):
         t0 = time.perf_counter()
-        for i, (h, (_, r, n, d, inc)) in enumerate(zip(host, CALLS)):
-            outs[i] = allcore.scan_rows(h, d, inc, cores, out=outs[i])
+        for d, op in CALLS:
+            allcore.exclusive_scan(host[d], N_LIVE, d, op, cores, out=outs[d])
         times.append(time.perf_counter() - t0)
     secs = statistics.median(times[1:])  # the first pass pages the buffers in
     return {"value": STEP_BYTES / secs / 1e9, "unit": UNIT, "cores": cores,
-            "kind": "all-core C row scan (pthreads, f32 accumulation); a baseline, not the oracle",
+            "kind": "all-core C exclusive scan (pthreads, two-pass blocked); a baseline, not the oracle",
             "elements_per_s": STEP_ELEMS / secs, "seconds_per_step": round(secs, 4),
-            "sample": f"the whole step (4 tensors, {STEP_ELEMS} elements), median of {reps}"}
+            "sample": f"the whole step (9 calls, {STEP_ELEMS} elements), median of {reps}"}
 
 
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
-def make_host_inputs():
-    return [workloads.rows_half(r, n, d) for _, r, n, d, _ in CALLS]
+class Scan1D:
+    """Device buffers of the step: one input, one output and one scratch per
+    dtype, and the live count in device memory."""
+
+    def __init__(self, mt, host, dev):
+        self.mt = mt
+        self.arr = {d: host[d].to(dev) for d in DTYPES}
+        self.out = {d: torch.empty_like(self.arr[d]) for d in DTYPES}
+        self.scratch = {d: mt.alloc_scratch(CAPACITY, TORCH_DT[d], mt.MT_SCRATCH_SCAN, device=dev) for d in DTYPES}
+        self.n_dev = torch.tensor([N_LIVE], dtype=torch.int32, device=dev)
+
+    def call(self, d, op, stream, out=None):
+        self.mt.mt_exclusive_scan(self.arr[d], self.out[d] if out is None else out, self.scratch[d], self.n_dev,
+                                  op, stream)
+
+    def step(self, stream):
+        for d, op in CALLS:
+            self.call(d, op, stream)
+
+
+def back_to_back(fns, stream, launches=B2B_LAUNCHES):
+    """Average milliseconds per call of `fns` (closures over distinct buffer
+    sets, together larger than twice the L2) called round-robin back to back
+    between one event pair, after one warm-up round."""
+    for f in fns:
+        f()
+    rounds = max(1, math.ceil(launches / len(fns)))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(rounds):
+        for f in fns:
+            f()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / (rounds * len(fns)), rounds * len(fns)
+
+
+def kernel_entry(kernel, workload, nbytes, ms, launches, sets, peak, profile, family, **extra):
+    achieved = nbytes / (ms / 1e3) / 1e9
+    e = {"kernel": kernel, "workload": workload, "bound": "hbm", "bytes_per_launch": int(nbytes),
+         "avg_launch_ms": round(ms, 5), "achieved": round(achieved, 1), "peak": peak, "unit": UNIT,
+         "frac": round(achieved / peak, 4),
+         "traffic": profile_traffic(profile, family) if profile else None,
+         "profile": f"profiles/{profile}.json" if profile else None, "launches_timed": launches, "buffer_sets": sets}
+    e.update(extra)
+    return e
+
+
+def sets_for(nbytes):
+    """Buffer sets whose bytes together exceed twice the L2."""
+    return max(1, -(-2 * L2_BYTES // nbytes))
+
+
+def measure_kernels(mt, s1d, stream, dev, peak):
+    """Every scan kernel on its configured workload, each timed back to back
+    after the main timed region (see back_to_back)."""
+    ks = {}
+    for d, op in CALLS:
+        ms, n = back_to_back([lambda d=d, op=op: s1d.call(d, op, stream)], stream)
+        name = f"exclusive_scan_{d}_{op}"
+        ks[name] = kernel_entry(
+            f"k_scan_staged ({d}, {op})", f"1-D exclusive scan {d} {op}, n = 2^28-12345 (capacity 2^28)",
+            scan_bytes(d), ms, n, 1, peak, f"scan1d_{d}_{op}", "scan1d",
+            note="each call is a status-reset launch plus the scan launch; the time covers both")
+    # row scans: f32 [1024, 4096] (seed 0), bf16/f16 [8192, 8192] exclusive and
+    # [4096, 4099] inclusive (seed 1), long rows f32 [4, 2^24] (seed 2)
+    rows_cases = [
+        ("rows_f32_1024x4096_incl", "k_scan_rows (f32)", "row scan f32 [1024,4096] inclusive", 1024, 4096, "f32", True),
+        ("rows_f32_1024x4096_excl", "k_scan_rows (f32)", "row scan f32 [1024,4096] exclusive", 1024, 4096, "f32", False),
+        ("rows_bf16_8192x8192_excl", "k_scan_rows (bf16)", "row scan bf16 [8192,8192] exclusive", 8192, 8192, "bf16",
+         False),
+        ("rows_f16_8192x8192_excl", "k_scan_rows (f16)", "row scan f16 [8192,8192] exclusive", 8192, 8192, "f16", False),
+        ("rows_bf16_4096x4099_incl", "k_scan_rows (bf16)", "row scan bf16 [4096,4099] inclusive (ragged rows)", 4096,
+         4099, "bf16", True),
+        ("rows_f16_4096x4099_incl", "k_scan_rows (f16)", "row scan f16 [4096,4099] inclusive (ragged rows)", 4096,
+         4099, "f16", True),
+        ("rows_f32_4x2p24_incl", "k_scan_staged (long rows, f32)", "long-row scan f32 [4,2^24] inclusive", 4, 1 << 24,
+         "f32", True),
+        ("rows_f32_4x2p24_excl", "k_scan_staged (long rows, f32)", "long-row scan f32 [4,2^24] exclusive", 4, 1 << 24,
+         "f32", False),
+    ]
+    half = {}
+    for name, kern, wl, r, n, d, inc in rows_cases:
+        if d == "f32":
+            x = (workloads.rows_f32(r, n) if r == 1024 else workloads.rows_long(r, n)).to(dev)
+        else:
+            x = half.get((r, n, d))
+            if x is None:
+                x = half[(r, n, d)] = workloads.rows_half(r, n, d).to(dev)
+        nb = call_bytes(r, n, d)
+        sets = sets_for(nb)
+        xs = [x] + [x.clone() for _ in range(sets - 1)]
+        os_ = [torch.empty_like(x) for _ in range(sets)]
+        fns = [lambda xi=xi, oi=oi: mt.mt_scan_rows(xi, oi, inc, stream) for xi, oi in zip(xs, os_)]
+        ms, nl = back_to_back(fns, stream)
+        ks[name] = kernel_entry(kern, wl, nb, ms, nl, sets, peak, name, "rows")
+        del xs, os_, fns
+    # the four row calls of the bf16/f16 workload as one sequence
+    seq = [(8192, 8192, "bf16", False), (8192, 8192, "f16", False), (4096, 4099, "bf16", True),
+           (4096, 4099, "f16", True)]
+    outs = [torch.empty_like(half[(r, n, d)]) for r, n, d, _ in seq]
+    fns = [lambda x=half[(r, n, d)], o=o, inc=inc: mt.mt_scan_rows(x, o, inc, stream)
+           for (r, n, d, inc), o in zip(seq, outs)]
+    ms, nl = back_to_back(fns, stream)
+    nb = sum(call_bytes(r, n, d) for r, n, d, _ in seq) / len(seq)
+    ks["rows_half_4_calls"] = kernel_entry(
+        "k_scan_rows (bf16, f16)", "bf16 and f16 [8192,8192] exclusive then [4096,4099] inclusive, in turn", nb, ms,
+        nl, 1, peak, None, "rows",
+        note="bytes_per_launch and avg_launch_ms are the means over the four calls")
+    del half, outs, fns
+    # select: f32 values n = 2^28 uniform[-1,1) (seed 4), u8 flags Bernoulli(p) (seed 5)
+    ns = workloads.SELECT_N
+    vals = workloads.uniform((ns,), workloads.SEED_SELECT, -1.0, 1.0, "f32").to(dev)
+    out = torch.empty_like(vals)
+    num = torch.zeros(1, dtype=torch.int32, device=dev)
+    scr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_SELECT, device=dev)
+    nd = torch.tensor([ns], dtype=torch.int32, device=dev)
+    for p, tag in ((0.5, "p05"), (0.01, "p001")):
+        flags = workloads.bernoulli_u8(ns, p, workloads.SEED_SELECT + 1).to(dev)
+        k = int(flags.sum().item())
+        ms, nl = back_to_back([lambda f=flags: mt.mt_select(vals, f, out, num, scr, nd, stream)], stream)
+        ks[f"select_f32_{tag}"] = kernel_entry(
+            "k_select_staged (4-byte values)", f"select f32, n = 2^28, flags Bernoulli(p = {p})", 5 * ns + 4 * k, ms,
+            nl, 1, peak, f"select_f32_{tag}", "select", selected=k,
+            note="bytes_per_launch = 5 n + 4 num_out (flags and values read, selected values written); each call "
+                 "is a status-reset launch plus the select launch")
+        del flags
+    del vals, out, scr
+    torch.cuda.synchronize()
+    assert mt.mt_scan_status(stream) == 0, "device error word set while timing the kernels"
+    return ks
 
 
 def run_ours(args, world, rank, local):
@@ -284,29 +434,13 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.current_stream()
     host = make_host_inputs()
-    xs = [h.to(dev) for h in host]
-    outs = [torch.empty_like(x) for x in xs]
-    incl = [c[4] for c in CALLS]
-
-    def step(ev=None):
-        for i in range(len(CALLS)):
-            if i == 0 and ev is not None:
-                ev[0].record(stream)
-            mt.mt_scan_rows(xs[i], outs[i], incl[i], stream)
-            if i == 0 and ev is not None:
-                ev[1].record(stream)
+    s1d = Scan1D(mt, host, dev)
 
     for _ in range(args.warmup):
-        step()
+        s1d.step(stream)
     torch.cuda.synchronize()
     assert mt.mt_scan_status(stream) == 0
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    # The dominant launch is timed by an event pair on every DOM_EVERY-th step
-    # only: the pair stops that launch from overlapping its neighbours' launch
-    # and drain (about 9 us per instrumented step), which would otherwise
-    # slow every step of the timed region.
-    dom = [(ev(), ev()) for _ in range((args.steps + DOM_EVERY - 1) // DOM_EVERY)]
-    start, end = ev(), ev()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local).start()
     time.sleep(0.05)
     barrier()
@@ -314,97 +448,96 @@ def run_ours(args, world, rank, local):
     l0 = mt.mt_scan_launches()
     th0 = time.perf_counter()
     start.record(stream)
-    for k in range(args.steps):
-        step(dom[k // DOM_EVERY] if k % DOM_EVERY == 0 else None)
+    for _ in range(args.steps):
+        s1d.step(stream)
     end.record(stream)
     torch.cuda.synchronize()
     th1 = time.perf_counter()
     barrier()
     launches = mt.mt_scan_launches() - l0
-    time.sleep(0.05)
-    sampler.stop()
     assert mt.mt_scan_status(stream) == 0, "device error word set during the timed region"
     ms_local = start.elapsed_time(end)
-    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom)
     ms, nbytes = aggregate(ms_local, STEP_BYTES * args.steps, dev if world > 1 else None)
+    peak, peak_src = measured_peak()
 
-    # End to end through the C ABI with host buffers: every step scans inputs
-    # that live in pinned host memory into outputs in pinned host memory. The
-    # row kernels read and write those buffers directly over the host link
-    # (NVLink-C2C on a Grace host), so the host->device and device->host
-    # traffic happens inside the calls. Where the library refuses host
-    # memory, each step copies the inputs in and the results out instead.
-    pin_in = [h.pin_memory() for h in host]
-    pin_out = [torch.empty(h.shape, dtype=h.dtype).pin_memory() for h in host]
-    zero_copy = True
-    try:
-        mt.mt_scan_rows(pin_in[0], pin_out[0], incl[0], stream)
-        torch.cuda.synchronize()
-    except mt.ScanError:
-        zero_copy = False
+    # The dominant kernel (the i64 add scan, the largest call of the step),
+    # timed back to back after the timed region, then every other kernel on
+    # its own workload.
+    tk0 = time.perf_counter()
+    dom_ms, dom_n = back_to_back([lambda: s1d.call(*DOMINANT, stream)], stream)
+    kernels = measure_kernels(mt, s1d, stream, dev, peak) if not args.no_kernels else {}
+    tk1 = time.perf_counter()
+    time.sleep(0.05)
+    sampler.stop()
+
+    # End to end through the C ABI from host buffers: every step copies the
+    # three inputs' live elements from pinned host memory to the device, makes
+    # the nine calls, and copies each call's result to its own pinned host
+    # buffer (on a second stream, so a result's copy overlaps the next call).
+    pin_in = {d: host[d][:N_LIVE].pin_memory() for d in DTYPES}
+    pin_out = [torch.empty(N_LIVE, dtype=TORCH_DT[d]).pin_memory() for d, _ in CALLS]
+    dev_out = [torch.empty(N_LIVE, dtype=TORCH_DT[d], device=dev) for d, _ in CALLS]
+    copy = torch.cuda.Stream(dev)
+    done = [torch.cuda.Event() for _ in CALLS]
 
     def e2e_step():
-        if zero_copy:
-            for i in range(len(CALLS)):
-                mt.mt_scan_rows(pin_in[i], pin_out[i], incl[i], stream)
-            return
-        for i in range(len(CALLS)):
-            xs[i].copy_(pin_in[i], non_blocking=True)
-        for i in range(len(CALLS)):
-            mt.mt_scan_rows(xs[i], outs[i], incl[i], stream)
-        for i in range(len(CALLS)):
-            pin_out[i].copy_(outs[i], non_blocking=True)
+        for d in DTYPES:
+            s1d.arr[d][:N_LIVE].copy_(pin_in[d], non_blocking=True)
+        for i, (d, op) in enumerate(CALLS):
+            s1d.call(d, op, stream, out=dev_out[i])
+            done[i].record(stream)
+            copy.wait_event(done[i])
+            with torch.cuda.stream(copy):
+                pin_out[i].copy_(dev_out[i], non_blocking=True)
+        stream.wait_stream(copy)
 
-    e2e_steps = max(1, min(args.steps, 100))
-    for _ in range(max(1, min(args.warmup, 3))):
-        e2e_step()
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
     torch.cuda.synchronize()
     barrier()
-    e0, e1 = ev(), ev()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms, e2e_bytes = aggregate(e0.elapsed_time(e1), STEP_BYTES * e2e_steps,
-                                  dev if world > 1 else None)
-    h2d = sum(h.numel() * h.element_size() for h in host)
+    assert mt.mt_scan_status(stream) == 0
+    e2e_ms, e2e_bytes = aggregate(e0.elapsed_time(e1), STEP_BYTES * e2e_steps, dev if world > 1 else None)
+    h2d = sum(pin_in[d].numel() * pin_in[d].element_size() for d in DTYPES)
+    d2h = sum(t.numel() * t.element_size() for t in pin_out)
 
-    peak, peak_src = measured_peak()
     value = nbytes / (ms / 1e3) / 1e9
     achieved = DOM_BYTES / (dom_ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i32+f32+i64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "storage": "bf16+f16", "accumulate": "f32",
-                   "calls_per_step": [c[0] for c in CALLS], "bytes_per_step": STEP_BYTES,
+        "config": {"workload": WORKLOAD, "calls_per_step": [f"exclusive_scan {d} {op}" for d, op in CALLS],
+                   "live_n": N_LIVE, "capacity": CAPACITY, "bytes_per_step": STEP_BYTES,
                    "elements_per_step": STEP_ELEMS,
-                   "l2": f"inputs larger than L2: {STEP_BYTES/1e6:.0f} MB moved per step vs "
-                         f"{L2_BYTES/1e6:.0f} MB L2, no buffer touched twice within a step",
-                   "parallelism": f"replicas x{world} (rows shard with no exchange)"},
+                   "l2": f"inputs larger than L2: each call moves {scan_bytes('i32') / 1e9:.2f} or "
+                         f"{scan_bytes('i64') / 1e9:.2f} GB vs a {L2_BYTES / 1e6:.0f} MB L2",
+                   "parallelism": f"replicas x{world} (independent problems, no exchange)"},
         "elements_per_s": round(STEP_ELEMS * world * args.steps / (ms / 1e3), 1),
         "frac_of_peak": {"measured": round(value / world / peak, 4), "peak_gbs": peak,
                          "peak_source": peak_src, "datasheet_8000_gbs": round(value / world / 8000.0, 4)},
         "e2e": {"value": round(e2e_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d, "steps": e2e_steps,
-                "how": ("4 mt_scan_rows calls on pinned host buffers: the kernels read the inputs "
-                        "from and write the results to host memory over the host link (no staging "
-                        "copy), one stream, CUDA events around the steps" if zero_copy else
-                        "pinned host -> device copy, 4 mt_scan_rows calls, device -> pinned host "
-                        "copy, all on one stream, CUDA events around the steps")},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "how": "pinned host -> device copy of the 3 inputs' live elements, the 9 mt_exclusive_scan calls, "
+                       "device -> pinned host copy of each call's result on a second stream (overlapping the next "
+                       "call); CUDA events around the steps"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
-                     "kernel": "k_scan_rows<__nv_bfloat16,OpAdd,4,256> on [8192,8192] exclusive",
-                     "bytes_per_launch": DOM_BYTES, "avg_launch_ms": round(dom_ms, 5),
-                     "timed_launches": len(dom),
-                     "timing": f"event pair around the launch on every {DOM_EVERY}th timed step; the pair "
-                               "also stops that launch from overlapping its neighbours, so this duration "
-                               "includes an exposed launch ramp",
+                     "frac": round(achieved / peak, 4), "traffic": profile_traffic("scan1d_i64_add", "scan1d"),
+                     "kernel": "k_scan_staged<long, OpAdd, 4, 3, 256> (1-D exclusive scan, i64 add)",
+                     "bytes_per_launch": DOM_BYTES, "avg_launch_ms": round(dom_ms, 5), "timed_launches": dom_n,
+                     "timing": f"{dom_n} calls back to back between one event pair after the timed region (each "
+                               "call is a status-reset launch plus the scan launch; the time covers both)",
                      "peak_of": peak_src},
+        "kernels": kernels,
         "clocks": sampler.summary(th0, th1),
+        "clocks_kernels": sampler.summary(tk0, tk1),
         "gpu_launches": int(launches),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -426,22 +559,22 @@ def run_reference(args, world, rank):
     host = make_host_inputs()
     per_step = calibrate_oracle(host)
     budget = 150.0  # seconds for the whole --warmup W --steps K run
-    frac = min(1.0, budget / max(1, args.steps + args.warmup) / per_step)
+    m = min(N_LIVE, max(1 << 16, int(N_LIVE * budget / max(1, args.steps + args.warmup) / per_step)))
     for _ in range(args.warmup):
-        oracle_sample(host, frac)
+        oracle_sample(host, m)
     secs = nbytes = elems = 0
     for _ in range(args.steps):
-        s, b, e = oracle_sample(host, frac)
+        s, b, e = oracle_sample(host, m)
         secs, nbytes, elems = secs + s, nbytes + b, elems + e
     value = nbytes / secs / 1e9
-    sample = (f"each step: the first {frac:.5f} of the rows of each of the 4 tensors "
-              f"({elems // max(1, args.steps)} elements), plain C oracle, 1 thread")
+    sample = (f"each step: the first {m} live elements of each of the 9 calls ({m * len(CALLS)} elements), "
+              f"plain C oracle, 1 thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "storage": "bf16+f16", "accumulate": "f64 (oracle)"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "i32+f32+i64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "accumulate": "exact integers; f32 add in f64 (oracle)"},
         "elements_per_s": round(elems / secs, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -666,11 +799,13 @@ def run_suite(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
-                    help="skip the CPU-oracle baseline (profiling runs)")
+                    help="skip the CPU baselines (profiling runs)")
+    ap.add_argument("--no-kernels", action="store_true",
+                    help="skip the per-kernel back-to-back entries (profiling runs)")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every configured shape")
     ap.add_argument("--suite-out", default=None)
     ap.add_argument("--only", default=None, help="suite: run only configs whose name contains this")
