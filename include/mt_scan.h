@@ -7,8 +7,9 @@
  * as `void*`; NULL means the legacy default stream. Every call only enqueues
  * work on `stream` and returns without synchronising, except
  * mt_scan_status(), which synchronises the stream it is given. The enqueueing
- * calls may therefore be captured in a CUDA graph and replayed (mt_scan_rows
- * on long rows then records its workspace allocation as a graph node).
+ * calls other than mt_scan_rows_noalloc (whose note says nothing on this) may
+ * therefore be captured in a CUDA graph and replayed (mt_scan_rows on long
+ * rows then records its workspace allocation as a graph node).
  * Calls on different streams, from any host threads, may run concurrently as
  * long as they share no output or scratch buffer.
  *
@@ -277,14 +278,35 @@ int mt_reduce_by_key_add(const void *keys_in, const void *values_in, void *keys_
  * dtype ignored) needs for any live count up to `capacity`. Plain host
  * arithmetic, no device access ([algos] "Scratch space": ask first, then
  * allocate). Returns -1 for a negative capacity or an unknown kind/dtype.
+ * The row scans need no scratch argument; the size of the workspace they
+ * take themselves is given by mt_scan_rows_scratch_slots.
  */
 int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind);
+
+/*
+ * mt_scan_rows_scratch_slots -- size, in 8-byte slots, of the look-back
+ * workspace that mt_scan_rows / mt_scan_rows_op take from the library's pool
+ * and mt_scan_rows_noalloc takes from its fixed array for a [rows, n] call of
+ * `dtype` (MT_F32, MT_BF16 or MT_F16), the larger of the two sizes that a row
+ * start on a 16-byte boundary or off it needs. 0 when every row fits in one
+ * tile (no workspace), -1 for a negative size, another dtype or an overflow.
+ * The size depends on both rows and n (each row rounds up to whole tiles), so
+ * it is not a kind of mt_scan_scratch_slots, whose sizes follow one capacity.
+ * Plain host arithmetic, no device access. A call of mt_scan_rows_noalloc
+ * fits its array when this times 8 is at most MT_NOALLOC_SCRATCH_BYTES.
+ */
+int64_t mt_scan_rows_scratch_slots(int64_t rows, int64_t n, int dtype);
 
 /*
  * mt_scan_status -- synchronise `stream`, then read and clear the device
  * error word of every kernel of the library on the current device.
  * Returns MT_OK, MT_ERR_LOOKBACK_TIMEOUT (a look-back wait gave up and the
  * results of the calls since the last check are not valid), or MT_ERR_CUDA.
+ * The error words belong to the device, not to a call or a stream: a wait
+ * that gave up in a call on any stream of the device is reported to the
+ * next mt_scan_status caller on that device, whatever stream it passes (so
+ * synchronise the other streams first when their calls must be covered), and
+ * that read clears it for everyone.
  */
 int mt_scan_status(void *stream);
 
@@ -316,18 +338,25 @@ int mt_scan_debug_lookback(int64_t skip_publish_tile, uint32_t spin_limit);
  * memory pool; this variant takes them from one fixed array inside the
  * library instead, and calls no allocating routine.
  *
- * Arguments, results and the other errors are those of mt_scan_rows.
+ * Arguments, results and the other errors are those of mt_scan_rows, and the
+ * look-back test hook (mt_scan_debug_lookback) applies to it as well.
  * Limit: the array holds MT_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that
- * loads the library, for the life of the process, which covers
- * rows * tiles_per_row <= 8191 tiles (a tile is 12288 f32 or 16384
- * bf16/f16 elements of a row; rows that fit one CTA, up to about 16384
- * elements, use none of it). A larger call returns MT_ERR_TOO_LARGE and
- * launches nothing.
- * The first call on each device looks up the array's device address (a
- * cudaGetSymbolAddress call), so make that first call before any stream
- * capture. Every call uses the same array and clears the part it needs
- * first; calls whose kernels overlap on the GPU (different streams, no
- * ordering between them) race on it and must not be made.
+ * loads the library, for the life of the process. A call fits when
+ * mt_scan_rows_scratch_slots(rows, n, dtype) * 8 <= MT_NOALLOC_SCRATCH_BYTES;
+ * with the library's default tile sizes that is rows * tiles_per_row <= 8191
+ * tiles (a tile is 12288 f32 or 16384 bf16/f16 elements of a row; rows that
+ * fit one CTA, up to about 16384 elements, use none of it). A larger call
+ * returns MT_ERR_TOO_LARGE and launches nothing.
+ * The first call that needs the array (rows longer than one tile) in a CUDA
+ * context looks up the array's device address in that context (a
+ * cudaGetSymbolAddress call, which may load the library's device code), so
+ * make that first call before any stream capture. The address is kept per
+ * device together with the id of the context it came from and looked up
+ * again when another context is current (after cudaDeviceReset, for
+ * instance, the next call finds the new context's copy of the array). Every
+ * call uses the same array and clears the part it needs first; calls whose
+ * kernels overlap on the GPU (different streams, no ordering between them)
+ * race on it and must not be made.
  */
 #define MT_NOALLOC_SCRATCH_BYTES (1 << 20)
 int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, int64_t n, int dtype,

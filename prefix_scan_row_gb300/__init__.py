@@ -52,7 +52,7 @@ OP_CODE = {"add": MT_ADD, "min": MT_MIN, "max": MT_MAX, "mul": MT_MUL}
 EXPORTS = ("mt_scan_rows", "mt_scan_rows_op", "mt_exclusive_scan", "mt_inclusive_scan", "mt_reduce", "mt_select",
            "mt_select_wide", "mt_reduce_by_key_add", "mt_scan_scratch_slots",
            "mt_scan_status", "mt_scan_launches", "mt_scan_strerror", "mt_scan_debug_lookback",
-           "mt_scan_rows_noalloc")
+           "mt_scan_rows_noalloc", "mt_scan_rows_scratch_slots")
 
 
 class ScanError(RuntimeError):
@@ -96,6 +96,8 @@ def _load():
     L.mt_scan_debug_lookback.restype = i32
     L.mt_scan_rows_noalloc.argtypes = [p, p, i64, i64, i32, i32, p]
     L.mt_scan_rows_noalloc.restype = i32
+    L.mt_scan_rows_scratch_slots.argtypes = [i64, i64, i32]
+    L.mt_scan_rows_scratch_slots.restype = i64
     return L
 
 
@@ -251,6 +253,17 @@ def mt_scan_scratch_slots(capacity: int, dtype, kind: int) -> int:
     return r
 
 
+def mt_scan_rows_scratch_slots(rows: int, n: int, dtype) -> int:
+    """8-byte slots of look-back workspace a [rows, n] row scan of `dtype`
+    takes (from the library's pool, or from mt_scan_rows_noalloc's array);
+    0 when every row fits in one tile."""
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    r = lib.mt_scan_rows_scratch_slots(int(rows), int(n), code)
+    if r < 0:
+        raise ValueError("mt_scan_rows_scratch_slots: bad size or dtype")
+    return r
+
+
 def alloc_scratch(capacity: int, dtype, kind: int, device="cuda") -> torch.Tensor:
     """Caller-owned scratch of mt_scan_scratch_slots(...) 8-byte slots."""
     return torch.empty(mt_scan_scratch_slots(capacity, dtype, kind), dtype=torch.int64,
@@ -274,8 +287,10 @@ def mt_scan_rows_noalloc(inp: torch.Tensor, out: torch.Tensor, inclusive: bool, 
     """mt_scan_rows without any device allocation, for callers that may not
     allocate: the look-back records of long rows live in a fixed 1 MiB array
     inside the library. Raises ScanError(MT_ERR_TOO_LARGE) for a shape that
-    needs more. The first call on a device looks up that array's address;
-    calls that overlap on the GPU must not be made."""
+    needs more (mt_scan_rows_scratch_slots(rows, n, dtype) * 8 above
+    MT_NOALLOC_SCRATCH_BYTES). The first long-row call in a CUDA context
+    looks up that array's address there; calls that overlap on the GPU must
+    not be made."""
     if inp.dim() == 1:
         rows, n = 1, inp.shape[0]
     else:

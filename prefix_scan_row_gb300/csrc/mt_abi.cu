@@ -94,7 +94,7 @@ static cudaError_t device_pool(int dev, cudaMemPool_t *out) {
     return cudaSuccess;
 }
 
-static bool make_launch(void *stream, Launch *L, int *dev) {
+bool make_launch(void *stream, Launch *L, int *dev) {
     L->stream = static_cast<cudaStream_t>(stream);
     L->sm_count = device_sm_count(dev);
     L->skip_tile = g_skip_tile.load(std::memory_order_relaxed);
@@ -387,6 +387,27 @@ extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) 
     if (kind == MT_SCRATCH_REDUCE)
         return elem_size(dtype) > 0 && dtype != MT_BF16 && dtype != MT_F16 ? reduce_scratch_slots() : -1;
     return -1;
+}
+
+extern "C" int64_t mt_scan_rows_scratch_slots(int64_t rows, int64_t n, int dtype) {
+    if (rows < 0 || n < 0 || (dtype != MT_F32 && dtype != MT_BF16 && dtype != MT_F16))
+        return -1;
+    if (rows == 0 || n == 0)
+        return 0;
+    if (n > INT64_MAX / elem_size(dtype) / rows)
+        return -1;
+    // the larger of the two plans: a row start on a 16-byte boundary, or not
+    int64_t tiles = 1;
+    for (const bool heads_zero : {true, false}) {
+        const RowPlan p = rows_plan(dtype, n, heads_zero);
+        if (p.tiles_per_row > tiles)
+            tiles = p.tiles_per_row;
+    }
+    if (tiles == 1)
+        return 0;  // every row fits in one tile: no look-back, no workspace
+    if (tiles > (INT64_MAX - kHeaderSlots) / rows_rec_slots() / rows)
+        return -1;
+    return kHeaderSlots + rows * tiles * rows_rec_slots();
 }
 
 extern "C" int mt_scan_status(void *stream) {

@@ -32,6 +32,11 @@ struct Launch {
 
 void note_launch();
 
+// Fills L for a launch on `stream` on the current device (its id in *dev):
+// SM count, and the look-back test hook's skip tile and poll limit
+// (mt_abi.cu). False when the device cannot be queried.
+bool make_launch(void *stream, Launch *L, int *dev);
+
 // Whether the kernels can dereference p on device `dev` (mt_abi.cu); `host`
 // is set for host memory.
 bool ptr_reachable(const void *p, int dev, bool *host);

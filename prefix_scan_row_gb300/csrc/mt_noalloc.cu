@@ -8,6 +8,8 @@
 // small look-back workspace for rows longer than one tile and takes it from
 // a memory pool; this variant uses one fixed array that lives in the library
 // instead, so nothing is allocated. The pages describe no such variant.
+#include <cuda.h>  // CUcontext / CUresult types only; the calls come through the runtime
+
 #include <mutex>
 
 #include "mt_internal.h"
@@ -17,8 +19,9 @@ namespace mt {
 
 constexpr int64_t kNoAllocSlots = MT_NOALLOC_SCRATCH_BYTES / 8;
 
-// The shared look-back workspace: a tile counter and header, then one 8-byte
-// record per tile. Every GPU that loads the library holds it until exit.
+// The shared look-back workspace: the header slots (the tile counter first),
+// then one status record per tile of rows_rec_slots() 8-byte slots (one
+// 128-byte line). Every GPU that loads the library holds it until exit.
 // Host code must not use this name as an address: on the host it is only a
 // stand-in for the symbol; the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocSlots];
@@ -32,27 +35,63 @@ __global__ void k_noalloc_clear(int64_t nwords) {
         g_noalloc_scratch[i] = 0ull;
 }
 
-static std::mutex g_noalloc_mu;
-static uint64_t *g_noalloc_ptr[kMaxDevices] = {};
+// The process-unique id of the context current on this thread, or 0 when
+// there is none (or the driver does not offer the calls). The driver calls
+// are fetched through the runtime, so the library does not link libcuda.
+static unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static std::once_flag once;
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        (void)cudaGetLastError();
+    });
+    if (get_current == nullptr || get_id == nullptr)
+        return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
-// Device address of the array on the current device, looked up once per
-// device (with that device current) and cached.
-static cudaError_t noalloc_scratch(uint64_t **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
+// Device address of the array in the current context, cached per device with
+// the id of the context it was found in. A device reset, or a context of the
+// caller's own made current, gives a new context whose copy of the array may
+// sit elsewhere: the address is then looked up again (with that context
+// current), never reused from another context.
+struct NoAllocEntry {
+    unsigned long long ctx;
+    uint64_t *ptr;
+};
+static std::mutex g_noalloc_mu;
+static NoAllocEntry g_noalloc_cache[kMaxDevices] = {};
+
+static cudaError_t noalloc_scratch(int dev, uint64_t **out) {
+    unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    NoAllocEntry &e = g_noalloc_cache[dev];
+    if (ctx == 0 || e.ptr == nullptr || e.ctx != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_noalloc_ptr[dev] = static_cast<uint64_t *>(p);
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess)
+            return err;
+        // the lookup makes the device's context current if none was
+        e.ctx = ctx != 0 ? ctx : current_context_id();
+        e.ptr = static_cast<uint64_t *>(p);
     }
-    *out = g_noalloc_ptr[dev];
+    *out = e.ptr;
     return cudaSuccess;
 }
 
@@ -85,22 +124,18 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
     if (nwords > kNoAllocSlots)
         return MT_ERR_TOO_LARGE;
 
-    uint64_t *ws = nullptr;
-    if (noalloc_scratch(&ws) != cudaSuccess)
-        return MT_ERR_CUDA;
     Launch L;
-    L.stream = static_cast<cudaStream_t>(stream);
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&L.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (!make_launch(stream, &L, &dev))
         return MT_ERR_CUDA;
     bool in_host = false, out_host = false;
     if (!ptr_reachable(inp, dev, &in_host) || !ptr_reachable(out, dev, &out_host) ||
         (p.staged && (in_host || out_host)))
         return MT_ERR_MEMORY;  // as mt_scan_rows
-    L.skip_tile = -1;
-    L.spin_limit = kDefaultSpin;
-    if (nwords > 0) {
+    uint64_t *ws = nullptr;
+    if (nwords > 0) {  // rows longer than one tile: look-back records in the fixed array
+        if (noalloc_scratch(dev, &ws) != cudaSuccess)
+            return MT_ERR_CUDA;
         int64_t grid = (nwords + 255) / 256;
         if (grid > 1024)
             grid = 1024;
@@ -108,9 +143,7 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
         note_launch();
         if (e != cudaSuccess)
             return MT_ERR_CUDA;
-    } else {
-        ws = nullptr;  // rows fit in one tile: no look-back, no workspace
     }
-    cudaError_t e = rows_launch(inp, out, rows, n, dtype, MT_ADD, p, inclusive != 0, aligned_io, ws, L);
+    const cudaError_t e = rows_launch(inp, out, rows, n, dtype, MT_ADD, p, inclusive != 0, aligned_io, ws, L);
     return e == cudaSuccess ? MT_OK : MT_ERR_CUDA;
 }

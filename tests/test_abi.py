@@ -174,6 +174,25 @@ def test_scratch_slots(lib):
     assert f(6141, 0, 4) == 4 + 16 and f(6142, 0, 4) == 4 + 32 and f(0, 0, 4) == 4
 
 
+def test_rows_scratch_slots(lib):
+    """Workspace of the row scans: header + rows x tiles per row x one
+    128-byte record, for the worse of the two row-start alignments."""
+    lib.mt_scan_rows_scratch_slots.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+    lib.mt_scan_rows_scratch_slots.restype = ctypes.c_int64
+    f = lib.mt_scan_rows_scratch_slots
+    assert f(0, 5, F32) == 0 and f(5, 0, BF16) == 0
+    assert f(-1, 5, F32) == -1 and f(1, -5, F32) == -1 and f(1, 5, I32) == -1
+    # rows that fit one CTA take none
+    assert f(1024, 4096, F32) == 0 and f(8192, 8192, BF16) == 0 and f(4096, 4099, F16) == 0
+    # 16384 f32 fit one CTA from a 16-byte boundary, but not from off it: then
+    # two tiles of 12288 (virtual) elements
+    assert f(1, 16384, F32) == 4 + 16 * 2
+    # long rows: 12288 f32 / 16384 bf16 elements per tile, up to 3 / 7 of head
+    assert f(4, 1 << 24, F32) == 4 + 4 * 1366 * 16
+    assert f(1, 1 << 24, BF16) == 4 + 1025 * 16 and f(3, 1 << 24, F16) == 4 + 3 * 1025 * 16
+    assert f(1 << 40, 1 << 40, F32) == -1  # overflow
+
+
 def test_strerror_and_counter(lib):
     assert lib.mt_scan_strerror(0) == b"ok"
     assert b"look-back" in lib.mt_scan_strerror(TIMEOUT)

@@ -33,7 +33,7 @@ def test_calls_replay_in_a_cuda_graph(mt):
     sto = torch.empty_like(st)
     num3 = torch.zeros(1, dtype=i32, device="cuda")
     st_scr = mt.alloc_scratch(n, i32, mt.MT_SCRATCH_SELECT)
-    so, lo, lo2 = torch.empty_like(short_rows), torch.empty_like(long_rows), torch.empty_like(long_rows)
+    so, lo = torch.empty_like(short_rows), torch.empty_like(long_rows)
     ao, vo, ko, kvo = torch.empty_like(a), torch.empty_like(v), torch.empty_like(keys), torch.empty_like(vals)
     red = torch.empty(1, dtype=i32, device="cuda")
     num = torch.zeros(1, dtype=i32, device="cuda")
@@ -47,7 +47,6 @@ def test_calls_replay_in_a_cuda_graph(mt):
     def calls():
         mt.mt_scan_rows(short_rows, so, True)
         mt.mt_scan_rows(long_rows, lo, False)  # look-back records from the library's pool
-        mt.mt_scan_rows_noalloc(long_rows, lo2, True)
         mt.mt_exclusive_scan(a, ao, scan_scr, nd, "add")
         mt.mt_reduce(a, red, red_scr, nd, "max")
         mt.mt_select(v, fl, vo, num, sel_scr, nd)
@@ -76,7 +75,6 @@ def test_calls_replay_in_a_cuda_graph(mt):
     def check(x):
         assert_rows_close(so, x["short"], "bf16", True)
         assert_rows_close(lo, x["long"], "f32", False)
-        assert_rows_close(lo2, x["long"], "f32", True)
         assert_scan_matches(ao, x["a"], n, "i32", "add")
         assert_reduce_matches(red, x["a"], n, "i32", "max")
         assert_select_matches(vo, num, x["v"], x["fl"], n)
