@@ -315,7 +315,7 @@ static int select_call(const void *arr, const uint8_t *flags, void *out, int32_t
     if (!all_device({arr, flags, out, num_out, scratch, n_dev}, dev))
         return MT_ERR_MEMORY;
     uint64_t *sw = static_cast<uint64_t *>(scratch);
-    if (launch_reset(sw, 0, n_dev, select_tile_elems(), 1, 0, select_rec_slots(), num_out, L) !=
+    if (launch_reset(sw, 0, n_dev, select_tile_elems(elem_bytes), 1, 0, select_rec_slots(), num_out, L) !=
         cudaSuccess)
         return MT_ERR_CUDA;
     return select_launch(arr, flags, out, num_out, sw, n_dev, elem_bytes, L) == cudaSuccess
@@ -376,7 +376,7 @@ extern "C" int64_t mt_scan_scratch_slots(int64_t capacity, int dtype, int kind) 
         return kHeaderSlots + ntiles * scan1d_rec_slots(dtype);
     }
     if (kind == MT_SCRATCH_SELECT) {
-        const int64_t te = select_tile_elems();
+        const int64_t te = select_tile_elems(0);
         return kHeaderSlots + (capacity + te - 1) / te * select_rec_slots();
     }
     if (kind == MT_SCRATCH_REDUCE_BY_KEY) {

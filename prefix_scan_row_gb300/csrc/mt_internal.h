@@ -121,7 +121,7 @@ cudaError_t rbk_launch(const void *keys, const void *vals, void *keys_out, void 
 cudaError_t rbk_take_error(int *code);
 
 // ---- select (mt_select.cu) ------------------------------------------------
-int64_t select_tile_elems();
+int64_t select_tile_elems(int elem_bytes);  // 0: the smallest over every element size
 int select_rec_slots();
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                           uint64_t *scratch, const int32_t *n_dev, int elem_bytes, const Launch &L);

@@ -90,11 +90,10 @@ constexpr int kLbPerLane = MT_LB_PER_LANE;
 // (the combine of every earlier tile of the segment [first, tile)).
 // Lane l reads tiles pos - l*K - i, i = 0..K-1 (i = 0 newest), so lanes hold
 // consecutive groups and a higher lane always holds older tiles.
-template <class Acc, class Op>
+template <class Acc, class Op, int K = kLbPerLane>
 __device__ __forceinline__ Acc warp_lookback(const uint64_t *recs, int64_t tile, int64_t first,
                                              uint32_t spin_limit) {
     using St = Status<Acc>;
-    constexpr int K = kLbPerLane;
     const int lane = threadIdx.x & 31;
     const Acc ident = Op::template identity<Acc>();
     Acc excl = ident;
@@ -177,7 +176,10 @@ __device__ __forceinline__ void publish_aggregate(const LookBack &lb, int64_t ti
 // Block-wide, after publish_aggregate: warp 0 looks back, thread 0 publishes
 // the inclusive prefix; every thread gets the tile's exclusive prefix.
 // `tile` and `first` are block-uniform; `agg` is needed in thread 0 only.
-template <class Acc, class Op>
+// (The whole block reading one group of 32 predecessors per warp, 256 per
+// round trip, was measured slower for every kernel: the polling traffic
+// costs more than the round trips it saves.)
+template <class Acc, class Op, int K = kLbPerLane>
 __device__ __forceinline__ Acc lookback_prefix(const LookBack &lb, int64_t tile, int64_t first,
                                                Acc agg, Acc *sm_prefix) {
     using St = Status<Acc>;
@@ -185,7 +187,7 @@ __device__ __forceinline__ Acc lookback_prefix(const LookBack &lb, int64_t tile,
     if (lb.recs == nullptr || tile == first)
         return ident;
     if (threadIdx.x < 32) {
-        const Acc ex = warp_lookback<Acc, Op>(lb.recs, tile, first, lb.spin_limit);
+        const Acc ex = warp_lookback<Acc, Op, K>(lb.recs, tile, first, lb.spin_limit);
         if (threadIdx.x == 0) {
             if (tile != lb.skip_tile)
                 St::publish(lb.recs + tile * St::kSlots, kIncl, Op::apply(ex, agg));

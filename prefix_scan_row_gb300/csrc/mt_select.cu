@@ -19,12 +19,34 @@
 
 namespace mt {
 
-#ifndef MT_SEL_ITEMS
-#define MT_SEL_ITEMS 2
+// Flag chunks (16 flags each) per thread of a tile: a tile holds 256 x 16 x
+// items elements. The staged kernel takes 16384-element tiles for 4-byte
+// values and 8192 for 8-byte ones (its shared memory holds a tile's values);
+// the struct kernel 8192 (a warp's flags are 32 steps of 32 elements). Each
+// tile costs one look-back, whose front moves about 32 tiles per L2 round
+// trip, so the elements per tile bound the elements per second.
+#ifndef MT_SEL_ITEMS4
+#define MT_SEL_ITEMS4 2
 #endif
-constexpr int kSelItems = MT_SEL_ITEMS;  // flag chunks (16 flags) per thread
-constexpr int kSelChunks = kThreads * kSelItems;
-constexpr int64_t kSelTE = (int64_t)kSelChunks * 16;  // elements per tile (8192)
+#ifndef MT_SEL_ITEMS8
+#define MT_SEL_ITEMS8 2
+#endif
+constexpr int kSelWordsItems = 2;
+#ifndef MT_SEL_GATHER4
+#define MT_SEL_GATHER4 0  // sparse tiles of 4-byte values gather (else every tile is staged)
+#endif
+#ifndef MT_SEL_GATHER8
+#define MT_SEL_GATHER8 1  // the same for 8-byte values
+#endif
+template <class VT>
+struct SelShape {
+    static constexpr int kItems = sizeof(VT) == 4 ? MT_SEL_ITEMS4 : MT_SEL_ITEMS8;
+    static constexpr bool kGather = (sizeof(VT) == 4 ? MT_SEL_GATHER4 : MT_SEL_GATHER8) != 0;
+    static constexpr int kChunks = kThreads * kItems;
+    static constexpr int64_t kTE = (int64_t)kChunks * 16;  // elements per tile
+};
+constexpr int kSelWordsChunks = kThreads * kSelWordsItems;
+constexpr int64_t kSelWordsTE = (int64_t)kSelWordsChunks * 16;  // elements per struct tile (8192)
 
 struct SelArgs {
     const void *arr;  // 4-byte (k_select_staged<uint32_t>) or 8-byte elements
@@ -56,8 +78,8 @@ __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
 // multiple of 16 elements).
 template <class VT>
 struct SelStagedSmem {
-    uint4 flags[kSelChunks + 2];  // 16 flags per chunk, hf leading bytes, slack for the last warp
-    VT vals[kSelTE + 16 / sizeof(VT)];  // the tile's values; each warp packs its selected ones in place
+    uint4 flags[SelShape<VT>::kChunks + 2];  // 16 flags per chunk, hf leading bytes, slack for the last warp
+    VT vals[SelShape<VT>::kTE + 16 / sizeof(VT)];  // the tile's values or the warps' packed runs
     uint64_t bar_f;           // the flags' copy
     uint64_t bar_v;           // the values' copy
     int64_t tile;
@@ -75,17 +97,19 @@ __device__ __forceinline__ uint4 keep_byte_range(uint4 f, int lo, int hi) {
 }
 
 // This thread's share of a tile's selected count: popcounts of its 16-flag
-// chunks of the copy (warp w owns the flag bytes [1024 w, 1024 (w + 1)); the
-// last warp also the copy's extra chunk when hf + elems passes the tile),
-// bytes outside [hf, hf + elems) masked. FAST: hf = 0 and a full tile.
-template <bool FAST>
+// chunks of the copy (warp w owns the flag bytes [512 I w, 512 I (w + 1)) of
+// a tile of I chunks per thread; the last warp also the copy's extra chunk
+// when hf + elems passes the tile), bytes outside [hf, hf + elems) masked.
+// FAST: hf = 0 and a full tile.
+template <bool FAST, int ITEMS>
 __device__ __forceinline__ uint32_t count_flags(const uint4 *flags, int warp, int lane, int hf, int elems) {
-    constexpr int kTE = (int)kSelTE;
+    constexpr int kChunks = kThreads * ITEMS;
+    constexpr int kTE = kChunks * 16;
     const int hi = hf + elems;  // one past the copy's last flag byte of the tile
     uint32_t mine = 0u;
 #pragma unroll
-    for (int j = 0; j < kSelItems; ++j) {
-        const int c = warp * 32 * kSelItems + j * 32 + lane;
+    for (int j = 0; j < ITEMS; ++j) {
+        const int c = warp * 32 * ITEMS + j * 32 + lane;
         if (FAST || 16 * c < hi) {
             uint4 f = lds128(&flags[c]);
             if (!FAST)
@@ -94,31 +118,65 @@ __device__ __forceinline__ uint32_t count_flags(const uint4 *flags, int warp, in
         }
     }
     if (!FAST && warp == kWarps - 1 && lane == 0 && hi > kTE) {
-        const uint4 f = keep_byte_range(lds128(&flags[kSelChunks]), 0, hi - kTE);
+        const uint4 f = keep_byte_range(lds128(&flags[kChunks]), 0, hi - kTE);
         mine += __popc(f.x) + __popc(f.y) + __popc(f.z) + __popc(f.w);
     }
     return mine;
 }
 
-// One staged tile: count and publish the count, pack each warp's selected
-// words in place, look back for the tile's output offset, copy the packed
-// runs out. Warp w owns the flag bytes [1024 w, 1024 (w + 1)) of the copy
-// (the last warp also the copy's extra chunk when hf + elems passes the
-// tile) and packs the elements they hold. FAST: a full tile with hf = hv =
-// 0, so no flag or element needs a range check. (Looking back before the
-// packing, overlapped with it, was measured slower: the look-back then meets
-// more predecessors that have only published their counts.)
+// One staged tile: count and publish the count, gather each warp's selected
+// elements into a packed run at the start of its own range of the stage,
+// look back for the tile's output offset, copy the packed runs out. Warp w
+// owns the flag bytes [1024 w, 1024 (w + 1)) of the copy (the last warp also
+// the copy's extra chunk when hf + elems passes the tile) and packs the
+// elements they hold. FAST: a full tile with hf = hv = 0, so no flag or
+// element needs a range check. (Looking back before the packing, overlapped
+// with it, was measured slower: the look-back then meets more predecessors
+// that have only published their counts.)
+//
+// The values reach the run one of two ways. A dense tile (more than one
+// element in kSelDenseDiv selected) has all its values bulk-copied into the
+// stage, and each warp packs its selected ones in place. A sparse tile reads
+// only its selected values: every selected lane issues a 4- or 8-byte
+// asynchronous copy from HBM straight to its slot of the run, all in flight
+// together, so most value sectors are never read. Whether the bulk copy is
+// issued is guessed before the flags are counted (the CTA's previous tile:
+// density is usually alike across an array) so that the copies of a dense
+// tile overlap; a tile guessed sparse that turns out dense issues its copy
+// late, and one guessed dense that turns out sparse uses the copied values.
+//   v_issued : the values' bulk copy was issued with the flags'
+//   vphase   : the parity of the values' barrier phase a copy would complete
+//   dense    : set to whether the tile turned out dense (the next guess)
 // Returns false when the values' copy did not complete in time (the caller
-// records the error and drains it).
+// records the error; a copy issued here is then drained here).
+#ifndef MT_SEL_DENSE_DIV
+#define MT_SEL_DENSE_DIV 8  // a tile with more than elems / MT_SEL_DENSE_DIV selected is dense
+#endif
+constexpr int kSelDenseDiv = MT_SEL_DENSE_DIV;
+#ifndef MT_SEL_BATCH
+#define MT_SEL_BATCH 8  // packing steps whose loads are issued together
+#endif
+constexpr int kSelBatch = MT_SEL_BATCH;
+#ifndef MT_SEL_CHUNK_BATCH
+#define MT_SEL_CHUNK_BATCH 2  // chunk-wise packing steps whose loads are issued together
+#endif
+constexpr int kSelChunkBatch = MT_SEL_CHUNK_BATCH;
+#ifndef MT_SEL_LB_PER_LANE
+#define MT_SEL_LB_PER_LANE 2  // predecessors per lane per look-back poll of the staged select
+#endif
+constexpr int kSelLbPerLane = MT_SEL_LB_PER_LANE;
+
 template <bool FAST, class VT>
 __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs &a, int64_t g,
-                                            int64_t ntiles, int elems, int hf_, int hv_, uint32_t phase) {
-    constexpr int kTE = (int)kSelTE;
+                                            int64_t ntiles, int elems, int hf_, int hv_, bool v_issued,
+                                            uint32_t vphase, bool &dense) {
+    using Sh = SelShape<VT>;
+    constexpr int kTE = (int)Sh::kTE;
     const int hf = FAST ? 0 : hf_, hv = FAST ? 0 : hv_;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hi = hf + elems;  // one past the copy's last flag byte of the tile
     const bool extra = !FAST && warp == kWarps - 1 && hi > kTE;
-    const uint32_t mine = count_flags<FAST>(sm.flags, warp, lane, hf, elems);
+    const uint32_t mine = count_flags<FAST, Sh::kItems>(sm.flags, warp, lane, hf, elems);
     // The tile's count, published as soon as the flags are in.
     uint32_t wsum = mine;
 #pragma unroll
@@ -137,44 +195,137 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     }
     publish_aggregate<uint32_t, OpAdd>(a.lb, g, 0, agg);
 
-    // The values were copied alongside the flags; their copy is the larger one.
-    bool ok = true;
-    if (threadIdx.x < 32)
-        ok = mbar_wait(&sm.bar_v, phase, kCopyWaitLimit);
-    if (__syncthreads_or(!ok))
-        return false;
+    dense = !Sh::kGather || (int64_t)agg * kSelDenseDiv > (int64_t)elems;  // block-uniform
+    const bool staged = v_issued || dense;
+    if (staged && !v_issued && threadIdx.x == 0) {  // guessed sparse, turned out dense
+        const int hvb = hv * (int)sizeof(VT);
+        const uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
+        const unsigned char *vsrc = static_cast<const unsigned char *>(a.arr) + g * Sh::kTE * (int64_t)sizeof(VT);
+        mbar_arrive_expect_tx(&sm.bar_v, vbytes);
+        bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
+    }
+    if (staged) {
+        bool ok = true;
+        if (threadIdx.x < 32)
+            ok = mbar_wait(&sm.bar_v, vphase, kCopyWaitLimit);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0)
+                mbar_wait(&sm.bar_v, vphase, kCopyWaitLimit);  // drain the copy before leaving
+            return false;
+        }
+    }
 
-    // Pack this warp's selected words in place, in element order, from the
-    // slot of its first element on. A write goes to a slot at or before
-    // every slot this warp reads later and inside this warp's own slots; the
-    // warp barrier orders a step's reads before its writes.
     const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
-    const int wstart = warp * 32 * kSelItems * 16;
+    const int wstart = warp * 32 * Sh::kItems * 16;
     const int ebase = FAST ? wstart : max(wstart - hf, 0);
     VT *const run = sm.vals + hv + ebase;
     const unsigned lt = (1u << lane) - 1u;
     uint32_t cnt = 0u;
-    auto step = [&](int s) {
-        const int b = wstart + s * 32 + lane;
-        const int e = b - hf;
-        const bool sel = (FAST || (unsigned)e < (unsigned)elems) && fb[b] != 0;
-        const unsigned bal = __ballot_sync(kFull, sel);
-        VT val = 0;
-        if (sel)
-            val = sm.vals[hv + e];
-        __syncwarp();
-        if (sel)
-            run[cnt + __popc(bal & lt)] = val;
-        cnt += __popc(bal);
-    };
+    if (staged) {
+        // Pack this warp's selected words in place, in element order, from
+        // the slot of its first element on. A selected element is written at
+        // or before its own slot, and every slot read later lies after the
+        // slots of the elements read so far; so reads of a batch of steps
+        // only need to complete before that batch's writes (the warp
+        // barrier), and a batch's loads are all issued together.
+        auto batch = [&](int s0, int nsteps) {
+            VT v[kSelBatch];
+            unsigned bal[kSelBatch];
+            bool sel[kSelBatch];
 #pragma unroll
-    for (int s = 0; s < kSelItems * 16; ++s)
-        step(s);
-    if (extra)  // warp-uniform
-        step(kSelItems * 16);
-    __syncwarp();
+            for (int j = 0; j < kSelBatch; ++j) {
+                if (j < nsteps) {
+                    const int b = wstart + (s0 + j) * 32 + lane;
+                    const int e = b - hf;
+                    sel[j] = (FAST || (unsigned)e < (unsigned)elems) && fb[b] != 0;
+                    bal[j] = __ballot_sync(kFull, sel[j]);
+                    v[j] = 0;
+                    if (sel[j])
+                        v[j] = sm.vals[hv + e];
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kSelBatch; ++j) {
+                if (j < nsteps) {
+                    if (sel[j])
+                        run[cnt + __popc(bal[j] & lt)] = v[j];
+                    cnt += __popc(bal[j]);
+                }
+            }
+        };
+        static_assert((Sh::kItems * 16) % kSelBatch == 0, "whole batches of steps");
+        if constexpr (FAST && sizeof(VT) == 4) {
+            // A full tile at the 16-byte boundaries: lane l of step s takes
+            // the 4 elements of chunk 32 s + l of the warp's range, as one
+            // 4-byte flag word and one 16-byte value chunk. Flags are exactly
+            // 0 or 1, so popc(word) is the chunk's count, and the warp's
+            // exclusive prefix of those counts (0 to 4) comes from 3 ballots.
+            const uint32_t *fw = reinterpret_cast<const uint32_t *>(fb) + wstart / 4;
+            const uint4 *vc = reinterpret_cast<const uint4 *>(sm.vals + wstart);
+            constexpr int kSteps = Sh::kItems * 4;  // 128 elements per step
+            constexpr int kB = kSteps < kSelChunkBatch ? kSteps : kSelChunkBatch;
+#pragma unroll
+            for (int s0 = 0; s0 < kSteps; s0 += kB) {
+                uint32_t f[kB];
+                uint4 v[kB];
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    f[j] = fw[(s0 + j) * 32 + lane];
+                    v[j] = make_uint4(0u, 0u, 0u, 0u);
+                    if (f[j] != 0u)
+                        v[j] = lds128(&vc[(s0 + j) * 32 + lane]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    const uint32_t k = __popc(f[j]);
+                    const unsigned b1 = __ballot_sync(kFull, k & 1u), b2 = __ballot_sync(kFull, k & 2u),
+                                   b4 = __ballot_sync(kFull, k & 4u);
+                    uint32_t o = cnt + __popc(b1 & lt) + 2u * __popc(b2 & lt) + 4u * __popc(b4 & lt);
+                    if (f[j] & 0x000000ffu)
+                        run[o++] = v[j].x;
+                    if (f[j] & 0x0000ff00u)
+                        run[o++] = v[j].y;
+                    if (f[j] & 0x00ff0000u)
+                        run[o++] = v[j].z;
+                    if (f[j] & 0xff000000u)
+                        run[o] = v[j].w;
+                    cnt += __popc(b1) + 2u * __popc(b2) + 4u * __popc(b4);
+                }
+                __syncwarp();  // this batch's writes before the next batch's reads
+            }
+        } else {
+#pragma unroll 1
+            for (int s0 = 0; s0 < Sh::kItems * 16; s0 += kSelBatch)
+                batch(s0, kSelBatch);
+            if (extra)  // warp-uniform
+                batch(Sh::kItems * 16, 1);
+        }
+    } else {
+        // Gather each selected value from HBM into its slot of the run; the
+        // copies complete while warp 0 looks back.
+        const VT *src = static_cast<const VT *>(a.arr) + g * Sh::kTE;
+        auto step = [&](int s) {
+            const int b = wstart + s * 32 + lane;
+            const int e = b - hf;
+            const bool sel = (FAST || (unsigned)e < (unsigned)elems) && fb[b] != 0;
+            const unsigned bal = __ballot_sync(kFull, sel);
+            if (sel)
+                cp_async_small<(int)sizeof(VT)>(run + cnt + __popc(bal & lt), src + e);
+            cnt += __popc(bal);
+        };
+#pragma unroll
+        for (int s = 0; s < Sh::kItems * 16; ++s)
+            step(s);
+        if (extra)  // warp-uniform
+            step(Sh::kItems * 16);
+    }
     // The tile's output offset (the look-back ends with a block barrier).
-    const uint32_t G = lookback_prefix<uint32_t, OpAdd>(a.lb, g, 0, agg, &sm.prefix);
+    const uint32_t G = lookback_prefix<uint32_t, OpAdd, kSelLbPerLane>(a.lb, g, 0, agg, &sm.prefix);
+    if (!staged)
+        cp_async_wait_all();
+    __syncwarp();
     VT *dst = static_cast<VT *>(a.out) + G + wpre;
     for (uint32_t i = lane; i < cnt; i += 32)
         dst[i] = run[i];
@@ -183,11 +334,17 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     return true;
 }
 
-// Resident blocks per SM: shared memory allows 5 (4-byte values) or 3
-// (8-byte values); the bound keeps the registers within that.
+// Resident blocks per SM that the shared memory allows (the bound keeps the
+// registers within that): 5 for 8192 4-byte values, 2 for 16384; 3 for
+// 8192 8-byte values.
 template <class VT>
-__global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_staged(SelArgs a) {
+constexpr int sel_staged_minb() {
+    return (int)((227u * 1024u) / (sizeof(SelStagedSmem<VT>) + 1024u));
+}
+template <class VT>
+__global__ void __launch_bounds__(kThreads, sel_staged_minb<VT>()) k_select_staged(SelArgs a) {
     pdl_prologue();
+    constexpr int64_t kSelTE = SelShape<VT>::kTE;
     extern __shared__ __align__(128) unsigned char dsm[];
     SelStagedSmem<VT> &sm = *reinterpret_cast<SelStagedSmem<VT> *>(dsm);
     const int32_t n32 = *a.n_dev;
@@ -202,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_st
         mbar_init(&sm.bar_v, 1);
         fence_mbar_init();
     }
-    uint32_t phase = 0;
+    uint32_t fphase = 0, vphase = 0;
+    bool guess_dense = true;  // whether to copy the values along with the flags (always, without gathering)
     for (;;) {
         if (threadIdx.x == 0)
             sm.tile = (int64_t)atomicAdd(a.counter, 1ull);
@@ -215,35 +373,43 @@ __global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_st
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
             const uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
-            const uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
-            const unsigned char *vsrc = static_cast<const unsigned char *>(a.arr) + t0 * (int64_t)sizeof(VT);
             mbar_arrive_expect_tx(&sm.bar_f, fbytes);
             bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
-            mbar_arrive_expect_tx(&sm.bar_v, vbytes);
-            bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
+            if (guess_dense) {
+                const uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
+                const unsigned char *vsrc = static_cast<const unsigned char *>(a.arr) + t0 * (int64_t)sizeof(VT);
+                mbar_arrive_expect_tx(&sm.bar_v, vbytes);
+                bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
+            }
         }
         // Warp 0 waits for the flags; the block barrier passes the
         // completion (and the copied bytes) on to the other warps. The
         // tile's count is published before the values are waited for.
         bool ok = true;
         if (threadIdx.x < 32)
-            ok = mbar_wait(&sm.bar_f, phase, kCopyWaitLimit);
-        if (__syncthreads_or(!ok))
-            ok = false;  // every thread: the flags did not arrive
-        else
-            ok = (elems == kSelTE && hf == 0 && hvb == 0)
-                     ? select_tile<true, VT>(sm, a, g, ntiles, elems, hf, hv, phase)
-                     : select_tile<false, VT>(sm, a, g, ntiles, elems, hf, hv, phase);
-        if (!ok) {  // block-uniform
+            ok = mbar_wait(&sm.bar_f, fphase, kCopyWaitLimit);
+        bool dense = guess_dense;
+        if (__syncthreads_or(!ok)) {  // every thread: the flags did not arrive
             if (threadIdx.x == 0) {
-                atomicCAS(&g_mt_err, 0, kErrTimeout);
-                // drain both copies before leaving
-                mbar_wait(&sm.bar_f, phase, kCopyWaitLimit);
-                mbar_wait(&sm.bar_v, phase, kCopyWaitLimit);
+                mbar_wait(&sm.bar_f, fphase, kCopyWaitLimit);  // drain the copies before leaving
+                if (guess_dense)
+                    mbar_wait(&sm.bar_v, vphase, kCopyWaitLimit);
             }
+            ok = false;
+        } else {
+            ok = (elems == kSelTE && hf == 0 && hvb == 0)
+                     ? select_tile<true, VT>(sm, a, g, ntiles, elems, hf, hv, guess_dense, vphase, dense)
+                     : select_tile<false, VT>(sm, a, g, ntiles, elems, hf, hv, guess_dense, vphase, dense);
+        }
+        if (!ok) {  // block-uniform
+            if (threadIdx.x == 0)
+                atomicCAS(&g_mt_err, 0, kErrTimeout);
             return;
         }
-        phase ^= 1u;
+        fphase ^= 1u;
+        if (guess_dense || dense)  // a values copy completed
+            vphase ^= 1u;
+        guess_dense = dense;
         fence_proxy_async_smem();  // this thread's shared writes precede the next bulk copies
     }
 }
@@ -260,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, sizeof(VT) == 4 ? 5 : 3) k_select_st
 // k-th selected element, E elements per lane per round, all their words in
 // flight together. WT: W known at compile time (0: at run time).
 struct SelWordsSmem {
-    uint4 flags[kSelChunks + 2];  // as in SelStagedSmem
+    uint4 flags[kSelWordsChunks + 2];  // as in SelStagedSmem
     uint64_t bar_f;
     int64_t tile;
     uint32_t red[kWarps];
@@ -285,11 +451,11 @@ __host__ __device__ constexpr int sel_words_minb(int) { return MT_SEL_WORDS_MINB
 template <bool FAST, int WT>
 __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArgs &a, int W_rt, int vec,
                                                   int64_t g, int64_t ntiles, int elems, int hf_) {
-    constexpr int kTE = (int)kSelTE;
+    constexpr int kTE = (int)kSelWordsTE;
     const int W = WT != 0 ? WT : W_rt;
     const int hf = FAST ? 0 : hf_;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t mine = count_flags<FAST>(sm.flags, warp, lane, hf, elems);
+    const uint32_t mine = count_flags<FAST, kSelWordsItems>(sm.flags, warp, lane, hf, elems);
     uint32_t wsum = mine;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
@@ -312,9 +478,9 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
     const uint8_t *fb = reinterpret_cast<const uint8_t *>(sm.flags);
     const uint32_t *src = static_cast<const uint32_t *>(a.arr);
     uint32_t *dst = static_cast<uint32_t *>(a.out);
-    const int wstart = warp * 32 * kSelItems * 16;
-    const int64_t t0 = g * kSelTE;
-    static_assert(kSelItems * 16 == 32, "a warp's flag bytes are 32 steps of 32");
+    const int wstart = warp * 32 * kSelWordsItems * 16;
+    const int64_t t0 = g * kSelWordsTE;
+    static_assert(kSelWordsItems * 16 == 32, "a warp's flag bytes are 32 steps of 32");
     // The ballots of the warp's 32 steps of 32 elements: lane s keeps step
     // s's ballot and the number of selected elements in the steps before s.
     unsigned my_bal = 0u;
@@ -442,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(S
     __shared__ __align__(128) SelWordsSmem sm;
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
-    const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
+    const int64_t ntiles = (n + kSelWordsTE - 1) / kSelWordsTE;
     const int hf = (int)(reinterpret_cast<uintptr_t>(a.flags) & 15u);
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar_f, 1);
@@ -456,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(S
         const int64_t g = sm.tile;
         if (g >= ntiles)
             break;
-        const int64_t t0 = g * kSelTE;
-        const int elems = (int)((n - t0 < kSelTE) ? n - t0 : kSelTE);
+        const int64_t t0 = g * kSelWordsTE;
+        const int elems = (int)((n - t0 < kSelWordsTE) ? n - t0 : kSelWordsTE);
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
             const uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
@@ -474,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(S
             }
             return;
         }
-        if (elems == kSelTE && hf == 0)
+        if (elems == kSelWordsTE && hf == 0)
             select_words_tile<true, WT>(sm, a, sw.words, sw.vec, g, ntiles, elems, hf);
         else
             select_words_tile<false, WT>(sm, a, sw.words, sw.vec, g, ntiles, elems, hf);
@@ -506,7 +672,17 @@ static cudaError_t launch_words_select(const SelArgs &a, const SelWords &sw, con
     return e;
 }
 
-int64_t select_tile_elems() { return kSelTE; }
+int64_t select_tile_elems(int elem_bytes) {
+    if (elem_bytes == 4)
+        return SelShape<uint32_t>::kTE;
+    if (elem_bytes == 8)
+        return SelShape<uint64_t>::kTE;
+    if (elem_bytes > 8)
+        return kSelWordsTE;
+    // any element size: the smallest tile (the most status records)
+    int64_t t = SelShape<uint32_t>::kTE < SelShape<uint64_t>::kTE ? SelShape<uint32_t>::kTE : SelShape<uint64_t>::kTE;
+    return t < kSelWordsTE ? t : kSelWordsTE;
+}
 int select_rec_slots() { return Status<uint32_t>::kSlots; }
 
 template <class VT>

@@ -297,6 +297,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
+// Asynchronous 4- or 8-byte copy global -> shared: no register holds the
+// value while it is in flight, so a thread can have many outstanding.
+// Both addresses aligned to the size; complete after cp_async_wait_all().
+template <int BYTES>
+__device__ __forceinline__ void cp_async_small(void *dst, const void *src) {
+    static_assert(BYTES == 4 || BYTES == 8, "4- or 8-byte copies");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" :: "r"(smem_addr(dst)), "l"(src), "n"(BYTES)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
