@@ -176,7 +176,10 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hi = hf + elems;  // one past the copy's last flag byte of the tile
     const bool extra = !FAST && warp == kWarps - 1 && hi > kTE;
-    const uint32_t mine = count_flags<FAST, Sh::kItems>(sm.flags, warp, lane, hf, elems);
+    // (the flags' own alignment decides the masking, whatever the values')
+    const uint32_t mine = (FAST || (hf == 0 && elems == kTE))
+                              ? count_flags<true, Sh::kItems>(sm.flags, warp, lane, 0, kTE)
+                              : count_flags<false, Sh::kItems>(sm.flags, warp, lane, hf, elems);
     // The tile's count, published as soon as the flags are in.
     uint32_t wsum = mine;
 #pragma unroll
