@@ -64,7 +64,8 @@ typedef enum {
     MT_ERR_LOOKBACK_TIMEOUT = -5, /* device: a tile waited too long for a predecessor */
     MT_ERR_ALIGN = -6,            /* pointer not aligned to its element size */
     MT_ERR_TOO_LARGE = -7,        /* needs more than the fixed no-allocation scratch */
-    MT_ERR_MEMORY = -8            /* a pointer the call's kernels cannot reach (see each call) */
+    MT_ERR_MEMORY = -8,           /* a pointer the call's kernels cannot reach (see each call) */
+    MT_ERR_BOUNDS = -9            /* device, checked build only: an access outside its buffer was skipped */
 } mt_status;
 
 /*
@@ -301,7 +302,10 @@ int64_t mt_scan_rows_scratch_slots(int64_t rows, int64_t n, int dtype);
  * mt_scan_status -- synchronise `stream`, then read and clear the device
  * error word of every kernel of the library on the current device.
  * Returns MT_OK, MT_ERR_LOOKBACK_TIMEOUT (a look-back wait gave up and the
- * results of the calls since the last check are not valid), or MT_ERR_CUDA.
+ * results of the calls since the last check are not valid), MT_ERR_BOUNDS
+ * (only from the bounds-checked build of the library, libmtscan_checked.so:
+ * a kernel computed an address outside the buffer it was writing or the
+ * shared memory it was using, and skipped that access), or MT_ERR_CUDA.
  * The error words belong to the device, not to a call or a stream: a wait
  * that gave up in a call on any stream of the device is reported to the
  * next mt_scan_status caller on that device, whatever stream it passes (so
@@ -316,6 +320,12 @@ uint64_t mt_scan_launches(void);
 
 /* Human-readable name of an mt_status code. */
 const char *mt_scan_strerror(int code);
+
+/* 1 in the bounds-checked build of the library (libmtscan_checked.so, whose
+ * kernels check every global store and shared-memory access against its
+ * buffer and report a bad one as MT_ERR_BOUNDS instead of making it), 0 in
+ * the ordinary one. */
+int mt_scan_build_checked(void);
 
 /*
  * mt_scan_debug_lookback -- test hook for failure detection. Sets, for the

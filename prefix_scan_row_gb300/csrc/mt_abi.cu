@@ -414,9 +414,9 @@ extern "C" int mt_scan_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MT_ERR_CUDA;
     int worst = MT_OK;
-    cudaError_t (*takers[7])(int *) = {rows_take_error,   rows_minmax_take_error, rows_mul_take_error,
+    cudaError_t (*takers[9])(int *) = {rows_take_error,   rows_minmax_take_error, rows_mul_take_error,
                                        scan1d_take_error, scan1d_ext_take_error,  select_take_error,
-                                       rbk_take_error};
+                                       rbk_take_error,    noalloc_take_error,     reduce_take_error};
     for (auto take : takers) {
         int code = 0;
         if (take(&code) != cudaSuccess)
@@ -429,6 +429,14 @@ extern "C" int mt_scan_status(void *stream) {
 
 extern "C" uint64_t mt_scan_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+extern "C" int mt_scan_build_checked(void) {
+#if defined(MT_CHECKED) && MT_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 extern "C" const char *mt_scan_strerror(int code) {
     switch (code) {
     case MT_OK: return "ok";
@@ -440,6 +448,7 @@ extern "C" const char *mt_scan_strerror(int code) {
     case MT_ERR_ALIGN: return "pointer misaligned";
     case MT_ERR_TOO_LARGE: return "needs more than the fixed no-allocation scratch (MT_NOALLOC_SCRATCH_BYTES)";
     case MT_ERR_MEMORY: return "a pointer the kernels cannot reach (host memory where device memory is needed)";
+    case MT_ERR_BOUNDS: return "a kernel's access fell outside its buffer and was skipped (bounds-checked build)";
     default: return "unknown status";
     }
 }

@@ -111,6 +111,7 @@ cudaError_t scan1d_ext_take_error(int *code);
 int64_t reduce_scratch_slots();  // fixed: header + one partial per CTA
 cudaError_t reduce_launch(const void *arr, void *out, uint64_t *scratch, const int32_t *n_dev,
                           int dtype, int op, const Launch &L);
+cudaError_t reduce_take_error(int *code);
 
 // ---- reduce by key (mt_rbk.cu) ---------------------------------------------
 int64_t rbk_tile_elems();
@@ -126,5 +127,8 @@ int select_rec_slots();
 cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int32_t *num_out,
                           uint64_t *scratch, const int32_t *n_dev, int elem_bytes, const Launch &L);
 cudaError_t select_take_error(int *code);
+
+// ---- the no-allocation row scan (mt_noalloc.cu) -----------------------------
+cudaError_t noalloc_take_error(int *code);
 
 }  // namespace mt

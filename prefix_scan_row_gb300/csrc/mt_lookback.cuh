@@ -76,7 +76,16 @@ struct LookBack {
     uint64_t *recs;      // tile records; nullptr when every segment is one tile
     int64_t skip_tile;   // test hook: this tile never publishes (-1: none)
     uint32_t spin_limit; // polls before a waiter gives up
+    int64_t nrec;        // records of the call (set by the kernel; bounds every publish in a checked build)
 };
+
+// Publishes `v` with `flag` in tile `t`'s record (the checked build first
+// checks that t is a record of the call).
+template <class Acc>
+__device__ __forceinline__ void publish_record(const LookBack &lb, int64_t t, uint32_t flag, Acc v) {
+    if (MT_CHECK_INDEX(t, lb.nrec))
+        Status<Acc>::publish(lb.recs + t * Status<Acc>::kSlots, flag, v);
+}
 
 #ifndef MT_LB_PER_LANE
 #define MT_LB_PER_LANE 1
@@ -170,7 +179,7 @@ __device__ __forceinline__ void publish_aggregate(const LookBack &lb, int64_t ti
     using St = Status<Acc>;
     if (lb.recs == nullptr || threadIdx.x != 0 || tile == lb.skip_tile)
         return;
-    St::publish(lb.recs + tile * St::kSlots, tile == first ? kIncl : kAgg, agg);
+    publish_record<Acc>(lb, tile, tile == first ? kIncl : kAgg, agg);
 }
 
 // Block-wide, after publish_aggregate: warp 0 looks back, thread 0 publishes
@@ -190,7 +199,7 @@ __device__ __forceinline__ Acc lookback_prefix(const LookBack &lb, int64_t tile,
         const Acc ex = warp_lookback<Acc, Op, K>(lb.recs, tile, first, lb.spin_limit);
         if (threadIdx.x == 0) {
             if (tile != lb.skip_tile)
-                St::publish(lb.recs + tile * St::kSlots, kIncl, Op::apply(ex, agg));
+                publish_record<Acc>(lb, tile, kIncl, Op::apply(ex, agg));
             *sm_prefix = ex;
         }
     }

@@ -14,6 +14,7 @@
 
 #include "mt_internal.h"
 #include "mt_scan.h"
+#include "mt_tile.cuh"
 
 namespace mt {
 
@@ -32,7 +33,8 @@ __global__ void k_noalloc_clear(int64_t nwords) {
     pdl_prologue();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nwords; i += stride)
-        g_noalloc_scratch[i] = 0ull;
+        if (MT_CHECK_INDEX(i, kNoAllocSlots))
+            g_noalloc_scratch[i] = 0ull;
 }
 
 // The process-unique id of the context current on this thread, or 0 when
@@ -147,3 +149,15 @@ extern "C" int mt_scan_rows_noalloc(const void *inp, void *out, int64_t rows, in
     const cudaError_t e = rows_launch(inp, out, rows, n, dtype, MT_ADD, p, inclusive != 0, aligned_io, ws, L);
     return e == cudaSuccess ? MT_OK : MT_ERR_CUDA;
 }
+
+namespace mt {
+// Reads and clears this translation unit's device error word (set only by
+// the bounds-checked build's checks of the clear kernel).
+cudaError_t noalloc_take_error(int *code) {
+    const int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_mt_err, sizeof(int));
+    if (e != cudaSuccess)
+        return e;
+    return cudaMemcpyToSymbol(g_mt_err, &zero, sizeof(int));
+}
+}  // namespace mt

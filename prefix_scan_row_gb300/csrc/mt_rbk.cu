@@ -31,6 +31,10 @@
 
 namespace mt {
 
+#ifndef MT_RBK_LB_PER_LANE
+#define MT_RBK_LB_PER_LANE 1  // predecessors per lane per look-back poll
+#endif
+constexpr int kRbkLbPerLane = MT_RBK_LB_PER_LANE;
 #ifndef MT_RBK_TILE
 #define MT_RBK_TILE 6144  // elements per super-tile (a multiple of 2048)
 #endif
@@ -136,8 +140,9 @@ static_assert(offsetof(RbkSmem, bar) % 8 == 0, "shared-memory layout of the redu
 // touch 8 different 16-byte bank groups.
 __device__ __forceinline__ void load_unit(const uint4 *base, int u, uint4 &c0, uint4 &c1) {
     const bool sw = (threadIdx.x >> 2) & 1;
-    const uint4 p = lds128(&base[2 * u + (sw ? 1 : 0)]);
-    const uint4 q = lds128(&base[2 * u + (sw ? 0 : 1)]);
+    const bool in = MT_CHECK_INDEX(2 * u, kRbkChunks) && MT_CHECK_INDEX(2 * u + 1, kRbkChunks);
+    const uint4 p = in ? lds128(&base[2 * u + (sw ? 1 : 0)]) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 q = in ? lds128(&base[2 * u + (sw ? 0 : 1)]) : make_uint4(0u, 0u, 0u, 0u);
     c0 = sw ? q : p;
     c1 = sw ? p : q;
 }
@@ -163,7 +168,6 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
     using P = Seg<VF>;
     using V = typename P::V;
     using Op = SegOp<VF>;
-    using St = Status<uint64_t>;
     constexpr int kNW = kRbkThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t *skey = reinterpret_cast<const uint32_t *>(sm.keys);
@@ -180,7 +184,7 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
         load_unit(sm.vals, u, v0, v1);
         uint32_t prev = __shfl_up_sync(kFull, k1.w, 1);
         if (lane == 0)
-            prev = (8 * u - 1 >= llo) ? skey[8 * u - 1] : kprev;
+            prev = (8 * u - 1 >= llo && MT_CHECK_INDEX(8 * u - 1, kRbkTE)) ? skey[8 * u - 1] : kprev;
         uint32_t m = 0u;
         V sum = V(0);
 #pragma unroll
@@ -197,7 +201,8 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
             }
             prev = key;
         }
-        sm.heads[u] = (uint8_t)m;
+        if (MT_CHECK_INDEX(u, kRbkUnits))
+            sm.heads[u] = (uint8_t)m;
         mh[s] = m;
         P inc{(uint32_t)__popc(m), sum};
 #pragma unroll
@@ -244,15 +249,16 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
         publish_aggregate<uint64_t, Op>(a.lb, g, 0, aggp);
         uint64_t pre = 0;  // the identity pair
         if (a.lb.recs != nullptr && g != 0) {
-            pre = warp_lookback<uint64_t, Op>(a.lb.recs, g, 0, a.lb.spin_limit);
+            pre = warp_lookback<uint64_t, Op, kRbkLbPerLane>(a.lb.recs, g, 0, a.lb.spin_limit);
             if (lane == 0 && g != a.lb.skip_tile)
-                St::publish(a.lb.recs + g * St::kSlots, kIncl, Op::apply(pre, aggp));
+                publish_record<uint64_t>(a.lb, g, kIncl, Op::apply(pre, aggp));
         }
         if (lane == 0)
             sm.prefix = pre;
     }
     // Does the super-tile's last element end its run?
-    const bool last_ends = lhi > llo && (has_last || keys_differ<KF>(knext, skey[lhi - 1]));
+    const bool last_ends =
+        lhi > llo && (has_last || (MT_CHECK_INDEX(lhi - 1, kRbkTE) && keys_differ<KF>(knext, skey[lhi - 1])));
     const int u_last = (lhi - 1) >> 3;  // the unit of the last valid element
     __syncthreads();
     const P tp = P::unpack(sm.prefix);
@@ -298,9 +304,9 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
                 }
                 const uint32_t r = run.c - 1u;
                 const bool ok = !decltype(checked)::value || r < n_live;
-                if (h && ok)
+                if (h && ok && MT_CHECK_RANGE(a.keys_out + r, 4, a.keys_out, a.keys_out + n_live))
                     a.keys_out[r] = word8(k0, k1, k);
-                if (((e >> k) & 1u) && ok)
+                if (((e >> k) & 1u) && ok && MT_CHECK_RANGE(a.vals_out + r, 4, a.vals_out, a.vals_out + n_live))
                     a.vals_out[r] = P::bits(run.s);
             }
         };
@@ -330,6 +336,7 @@ __global__ void __launch_bounds__(kRbkThreads, MT_RBK_MINB) k_reduce_by_key(RbkA
     const uint32_t *ek = reinterpret_cast<const uint32_t *>(a.keys) - head;  // virtual element 0
     const int64_t lo = head, hi = head + n;
     const int64_t ntiles = n > 0 ? (hi + kRbkTE - 1) / kRbkTE : 0;
+    a.lb.nrec = ntiles;
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar, 1);
@@ -353,10 +360,14 @@ __global__ void __launch_bounds__(kRbkThreads, MT_RBK_MINB) k_reduce_by_key(RbkA
             int64_t cend = (hi + 3) / 4;
             if (cend > c0 + kRbkChunks)
                 cend = c0 + kRbkChunks;
-            const uint32_t bytes = (uint32_t)((cend - c0) * 16);
+            uint32_t bytes = (uint32_t)((cend - c0) * 16);
+            if (!MT_CHECK_RANGE(&sm.keys[0], bytes, &sm.keys[0], &sm.keys[kRbkChunks]))
+                bytes = 0u;  // checked build: no copies (the phase completes with no bytes)
             mbar_arrive_expect_tx(&sm.bar, 2 * bytes);
-            bulk_g2s(&sm.keys[0], vk + c0, bytes, &sm.bar);
-            bulk_g2s(&sm.vals[0], vv + c0, bytes, &sm.bar);
+            if (bytes != 0u) {
+                bulk_g2s(&sm.keys[0], vk + c0, bytes, &sm.bar);
+                bulk_g2s(&sm.vals[0], vv + c0, bytes, &sm.bar);
+            }
             sm.kprev = (t0 + llo - 1 >= lo) ? __ldg(ek + t0 + llo - 1) : 0u;
             sm.knext = (t0 + lhi < hi) ? __ldg(ek + t0 + lhi) : 0u;
         }
@@ -428,6 +439,7 @@ cudaError_t rbk_launch(const void *keys, const void *vals, void *keys_out, void 
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
+    a.lb.nrec = 0;  // set by the kernel
     if (key_float)
         return val_float ? launch_rbk<true, true>(a, L) : launch_rbk<true, false>(a, L);
     return val_float ? launch_rbk<false, true>(a, L) : launch_rbk<false, false>(a, L);

@@ -137,7 +137,7 @@ __device__ __forceinline__ typename F::T block_fold(typename F::T v, typename F:
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
         v = F::apply(v, F::shfl_down(v, d));  // lower lanes stay the left operand
-    if (lane == 0)
+    if (lane == 0 && MT_CHECK_INDEX(warp, kRedThreads / 32))
         sm[warp] = v;
     __syncthreads();
     typename F::T r = F::ident();
@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
 
     // Partial to scratch; the last CTA to arrive folds all partials.
     if (threadIdx.x == 0) {
-        F::store(a.scratch + kHeaderSlots + kRedPartialSlots * blockIdx.x, part);
+        if (MT_CHECK_INDEX(blockIdx.x, kRedMaxCtas))
+            F::store(a.scratch + kHeaderSlots + kRedPartialSlots * blockIdx.x, part);
         __threadfence();
         const unsigned long long ticket = atomicAdd(reinterpret_cast<unsigned long long *>(a.scratch), 1ull);
         last = ticket == gridDim.x - 1;
@@ -234,7 +235,8 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(S) == 8 ? 2 : 4) k_reduce(
     // thread i folds partials i, i + 256, ...; the block fold then combines the
     // threads in a fixed tree: the same grouping on every call.
     for (int i = threadIdx.x; i < (int)gridDim.x; i += kRedThreads)
-        r = F::apply(r, F::load(a.scratch + kHeaderSlots + kRedPartialSlots * i));
+        if (MT_CHECK_INDEX(i, kRedMaxCtas))
+            r = F::apply(r, F::load(a.scratch + kHeaderSlots + kRedPartialSlots * i));
     r = block_fold<F>(r, sm);
     if (threadIdx.x == 0) {
         if constexpr (!kChunk) {
@@ -317,6 +319,16 @@ cudaError_t reduce_launch(const void *arr, void *out, uint64_t *scratch, const i
     case 7: return reduce_op<double>(op, a, L);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// Reads and clears this translation unit's device error word (set only by
+// the bounds-checked build's checks).
+cudaError_t reduce_take_error(int *code) {
+    const int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_mt_err, sizeof(int));
+    if (e != cudaSuccess)
+        return e;
+    return cudaMemcpyToSymbol(g_mt_err, &zero, sizeof(int));
 }
 
 }  // namespace mt

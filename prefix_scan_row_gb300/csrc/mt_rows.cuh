@@ -46,11 +46,12 @@ __global__ void __launch_bounds__(MAXT, (rows_min_blocks<ITEMS, MAXT>())) k_scan
     const int head = (int)(((uintptr_t)in_row & 15u) / s);
     const uint4 *vin = reinterpret_cast<const uint4 *>(in_row - head * s);
     S *eout = reinterpret_cast<S *>(a.out + row * a.n * s) - head;
+    const char *olo = a.out + row * a.n * s, *ohi = olo + a.n * s;
     const int lo = head, hi = head + (int)a.n;
     if (lo == 0 && hi == (int)blockDim.x * ITEMS * T::E)  // the row fills the tile
-        T::template run<true>(vin, eout, a.aligned_io != 0, lo, hi, a.inclusive != 0, sm);
+        T::template run<true>(vin, eout, a.aligned_io != 0, lo, hi, a.inclusive != 0, sm, olo, ohi);
     else
-        T::template run<false>(vin, eout, a.aligned_io != 0, lo, hi, a.inclusive != 0, sm);
+        T::template run<false>(vin, eout, a.aligned_io != 0, lo, hi, a.inclusive != 0, sm, olo, ohi);
 }
 
 #ifndef MT_ROWS_SUB_WIDE
@@ -111,6 +112,8 @@ static cudaError_t rows_launch_op(const void *in, void *out, int64_t rows, int64
         a.lb.recs = chained ? ws + kHeaderSlots : nullptr;
         a.lb.skip_tile = L.skip_tile;
         a.lb.spin_limit = L.spin_limit;
+        a.lb.nrec = 0;        // set by the kernel
+        a.out_end = nullptr;  // set by the kernel
         const int64_t tiles = rows * p.tiles_per_row;
         if (dtype == 0)
             return launch_staged<float, Op, kMultiItems, sub_of<float>(), kMultiThreads>(a, tiles, L);

@@ -74,6 +74,8 @@ static SegArgs scan1d_args(const void *arr, void *out, uint64_t *scratch, const 
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
+    a.lb.nrec = 0;        // set by the kernel
+    a.out_end = nullptr;  // set by the kernel
     return a;
 }
 

@@ -56,6 +56,7 @@ struct SelArgs {
     const int32_t *n_dev;
     unsigned long long *counter;
     LookBack lb;
+    const char *out_end;  // one past the call's output (set by the kernel; checked build)
 };
 
 __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
@@ -77,9 +78,11 @@ __device__ __forceinline__ uint32_t keep_low_bytes(uint32_t w, int64_t nbytes) {
 // arrays' offsets from the boundary (the same for every tile, which holds a
 // multiple of 16 elements).
 template <class VT>
+constexpr int kSelValSlots = (int)SelShape<VT>::kTE + 16 / (int)sizeof(VT);
+template <class VT>
 struct SelStagedSmem {
     uint4 flags[SelShape<VT>::kChunks + 2];  // 16 flags per chunk, hf leading bytes, slack for the last warp
-    VT vals[SelShape<VT>::kTE + 16 / sizeof(VT)];  // the tile's values or the warps' packed runs
+    VT vals[kSelValSlots<VT>];               // the tile's values or the warps' packed runs
     uint64_t bar_f;           // the flags' copy
     uint64_t bar_v;           // the values' copy
     int64_t tile;
@@ -110,7 +113,7 @@ __device__ __forceinline__ uint32_t count_flags(const uint4 *flags, int warp, in
 #pragma unroll
     for (int j = 0; j < ITEMS; ++j) {
         const int c = warp * 32 * ITEMS + j * 32 + lane;
-        if (FAST || 16 * c < hi) {
+        if ((FAST || 16 * c < hi) && MT_CHECK_INDEX(c, kChunks + 2)) {
             uint4 f = lds128(&flags[c]);
             if (!FAST)
                 f = keep_byte_range(f, hf - 16 * c, hi - 16 * c);
@@ -204,8 +207,10 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
         const int hvb = hv * (int)sizeof(VT);
         const uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
         const unsigned char *vsrc = static_cast<const unsigned char *>(a.arr) + g * Sh::kTE * (int64_t)sizeof(VT);
-        mbar_arrive_expect_tx(&sm.bar_v, vbytes);
-        bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
+        const uint32_t vb = MT_CHECK_RANGE(&sm.vals[0], vbytes, &sm.vals[0], &sm.vals[kSelValSlots<VT>]) ? vbytes : 0u;
+        mbar_arrive_expect_tx(&sm.bar_v, vb);
+        if (vb != 0u)
+            bulk_g2s(&sm.vals[0], vsrc - hvb, vb, &sm.bar_v);
     }
     if (staged) {
         bool ok = true;
@@ -222,6 +227,8 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     const int wstart = warp * 32 * Sh::kItems * 16;
     const int ebase = FAST ? wstart : max(wstart - hf, 0);
     VT *const run = sm.vals + hv + ebase;
+    [[maybe_unused]] const int run0 = hv + ebase;  // the run's first slot of sm.vals
+    [[maybe_unused]] constexpr int kVals = kSelValSlots<VT>, kFlagBytes = 16 * (Sh::kChunks + 2);
     const unsigned lt = (1u << lane) - 1u;
     uint32_t cnt = 0u;
     if (staged) {
@@ -240,10 +247,10 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
                 if (j < nsteps) {
                     const int b = wstart + (s0 + j) * 32 + lane;
                     const int e = b - hf;
-                    sel[j] = (FAST || (unsigned)e < (unsigned)elems) && fb[b] != 0;
+                    sel[j] = (FAST || (unsigned)e < (unsigned)elems) && MT_CHECK_INDEX(b, kFlagBytes) && fb[b] != 0;
                     bal[j] = __ballot_sync(kFull, sel[j]);
                     v[j] = 0;
-                    if (sel[j])
+                    if (sel[j] && MT_CHECK_INDEX(hv + e, kVals))
                         v[j] = sm.vals[hv + e];
                 }
             }
@@ -251,7 +258,7 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
 #pragma unroll
             for (int j = 0; j < kSelBatch; ++j) {
                 if (j < nsteps) {
-                    if (sel[j])
+                    if (sel[j] && MT_CHECK_INDEX(run0 + cnt + __popc(bal[j] & lt), kVals))
                         run[cnt + __popc(bal[j] & lt)] = v[j];
                     cnt += __popc(bal[j]);
                 }
@@ -274,9 +281,9 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
                 uint4 v[kB];
 #pragma unroll
                 for (int j = 0; j < kB; ++j) {
-                    f[j] = fw[(s0 + j) * 32 + lane];
+                    f[j] = MT_CHECK_INDEX(wstart / 4 + (s0 + j) * 32 + lane, kFlagBytes / 4) ? fw[(s0 + j) * 32 + lane] : 0u;
                     v[j] = make_uint4(0u, 0u, 0u, 0u);
-                    if (f[j] != 0u)
+                    if (f[j] != 0u && MT_CHECK_INDEX(wstart / 4 + (s0 + j) * 32 + lane, kVals / 4))
                         v[j] = lds128(&vc[(s0 + j) * 32 + lane]);
                 }
                 __syncwarp();
@@ -286,6 +293,8 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
                     const unsigned b1 = __ballot_sync(kFull, k & 1u), b2 = __ballot_sync(kFull, k & 2u),
                                    b4 = __ballot_sync(kFull, k & 4u);
                     uint32_t o = cnt + __popc(b1 & lt) + 2u * __popc(b2 & lt) + 4u * __popc(b4 & lt);
+                    if (!MT_CHECK_RANGE(run + o, 4u * __popc(f[j]), &sm.vals[0], &sm.vals[kVals]))
+                        f[j] = 0u;  // checked build: skip this word's stores
                     if (f[j] & 0x000000ffu)
                         run[o++] = v[j].x;
                     if (f[j] & 0x0000ff00u)
@@ -312,9 +321,9 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
         auto step = [&](int s) {
             const int b = wstart + s * 32 + lane;
             const int e = b - hf;
-            const bool sel = (FAST || (unsigned)e < (unsigned)elems) && fb[b] != 0;
+            const bool sel = (FAST || (unsigned)e < (unsigned)elems) && MT_CHECK_INDEX(b, kFlagBytes) && fb[b] != 0;
             const unsigned bal = __ballot_sync(kFull, sel);
-            if (sel)
+            if (sel && MT_CHECK_INDEX(run0 + cnt + __popc(bal & lt), kVals))
                 cp_async_small<(int)sizeof(VT)>(run + cnt + __popc(bal & lt), src + e);
             cnt += __popc(bal);
         };
@@ -331,7 +340,8 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
     __syncwarp();
     VT *dst = static_cast<VT *>(a.out) + G + wpre;
     for (uint32_t i = lane; i < cnt; i += 32)
-        dst[i] = run[i];
+        if (MT_CHECK_INDEX(run0 + i, kVals) && MT_CHECK_RANGE(dst + i, sizeof(VT), a.out, a.out_end))
+            dst[i] = run[i];
     if (g == ntiles - 1 && threadIdx.x == 0)
         *a.num_out = (int32_t)(G + agg);
     return true;
@@ -353,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, sel_staged_minb<VT>()) k_select_stag
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
     const int64_t ntiles = (n + kSelTE - 1) / kSelTE;
+    a.lb.nrec = ntiles;
+    a.out_end = static_cast<const char *>(a.out) + n * (int64_t)sizeof(VT);
     // Offsets from the 16-byte boundary below (arr is aligned to its element size).
     const int hf = (int)(reinterpret_cast<uintptr_t>(a.flags) & 15u);
     const int hvb = (int)(reinterpret_cast<uintptr_t>(a.arr) & 15u);
@@ -375,14 +387,20 @@ __global__ void __launch_bounds__(kThreads, sel_staged_minb<VT>()) k_select_stag
         const int elems = (int)((n - t0 < kSelTE) ? n - t0 : kSelTE);
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
-            const uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
+            uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
+            if (!MT_CHECK_RANGE(&sm.flags[0], fbytes, &sm.flags[0], &sm.flags[SelShape<VT>::kChunks + 2]))
+                fbytes = 0u;  // checked build: no copy (the phase completes with no bytes)
             mbar_arrive_expect_tx(&sm.bar_f, fbytes);
-            bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
+            if (fbytes != 0u)
+                bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
             if (guess_dense) {
-                const uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
+                uint32_t vbytes = (uint32_t)((hvb + (int64_t)elems * (int64_t)sizeof(VT) + 15) / 16 * 16);
                 const unsigned char *vsrc = static_cast<const unsigned char *>(a.arr) + t0 * (int64_t)sizeof(VT);
+                if (!MT_CHECK_RANGE(&sm.vals[0], vbytes, &sm.vals[0], &sm.vals[kSelValSlots<VT>]))
+                    vbytes = 0u;
                 mbar_arrive_expect_tx(&sm.bar_v, vbytes);
-                bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
+                if (vbytes != 0u)
+                    bulk_g2s(&sm.vals[0], vsrc - hvb, vbytes, &sm.bar_v);
             }
         }
         // Warp 0 waits for the flags; the block barrier passes the
@@ -491,7 +509,8 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
     for (int st = 0; st < 32; ++st) {
         const int bb = wstart + st * 32 + lane;
         const int e = bb - hf;
-        const bool sel = (FAST || (unsigned)e < (unsigned)elems) && fb[bb] != 0;
+        const bool sel = (FAST || (unsigned)e < (unsigned)elems) && MT_CHECK_INDEX(bb, 16 * (kSelWordsChunks + 2)) &&
+                         fb[bb] != 0;
         const unsigned bal = __ballot_sync(kFull, sel);
         if (lane == st)
             my_bal = bal;
@@ -562,7 +581,7 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
                     const int64_t o = (int64_t)(obase + k0 + 32 * x + lane) * W4 + w0;
 #pragma unroll
                     for (int w = 0; w < C4; ++w)
-                        if (el[x] >= 0 && (WT != 0 || w0 + w < W4))
+                        if (el[x] >= 0 && (WT != 0 || w0 + w < W4) && MT_CHECK_RANGE(dst4 + o + w, 16, a.out, a.out_end))
                             dst4[o + w] = v[x][w];
                 }
             }
@@ -582,7 +601,7 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
                 const int64_t o = (int64_t)(obase + k0 + 32 * x + lane) * W + w0;
 #pragma unroll
                 for (int w = 0; w < C; ++w)
-                    if (el[x] >= 0 && (WT != 0 || w0 + w < W))
+                    if (el[x] >= 0 && (WT != 0 || w0 + w < W) && MT_CHECK_RANGE(dst + o + w, 4, a.out, a.out_end))
                         dst[o + w] = v[x][w];
             }
         }
@@ -592,13 +611,14 @@ __device__ __forceinline__ void select_words_tile(SelWordsSmem &sm, const SelArg
     if (!FAST && warp == kWarps - 1 && hf + elems > kTE) {
         const int bb = wstart + 1024 + lane;
         const int e = bb - hf;
-        const bool sel = (unsigned)e < (unsigned)elems && fb[bb] != 0;
+        const bool sel = (unsigned)e < (unsigned)elems && MT_CHECK_INDEX(bb, 16 * (kSelWordsChunks + 2)) && fb[bb] != 0;
         const unsigned bal = __ballot_sync(kFull, sel);
         if (sel) {
             const int64_t in = ibase + (int64_t)(1024 + lane) * W;
             const int64_t o = (int64_t)(obase + warp_cnt + __popc(bal & ((1u << lane) - 1u))) * W;
             for (int w = 0; w < W; ++w)
-                dst[o + w] = __ldg(src + in + w);
+                if (MT_CHECK_RANGE(dst + o + w, 4, a.out, a.out_end))
+                    dst[o + w] = __ldg(src + in + w);
         }
     }
     if (g == ntiles - 1 && threadIdx.x == 0)
@@ -612,6 +632,8 @@ __global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(S
     const int32_t n32 = *a.n_dev;
     const int64_t n = n32 > 0 ? n32 : 0;
     const int64_t ntiles = (n + kSelWordsTE - 1) / kSelWordsTE;
+    a.lb.nrec = ntiles;
+    a.out_end = static_cast<const char *>(a.out) + n * (int64_t)sw.words * 4;
     const int hf = (int)(reinterpret_cast<uintptr_t>(a.flags) & 15u);
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar_f, 1);
@@ -629,9 +651,12 @@ __global__ void __launch_bounds__(kThreads, sel_words_minb(WT)) k_select_words(S
         const int elems = (int)((n - t0 < kSelWordsTE) ? n - t0 : kSelWordsTE);
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
-            const uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
+            uint32_t fbytes = (uint32_t)((hf + elems + 15) / 16 * 16);
+            if (!MT_CHECK_RANGE(&sm.flags[0], fbytes, &sm.flags[0], &sm.flags[kSelWordsChunks + 2]))
+                fbytes = 0u;  // checked build: no copy (the phase completes with no bytes)
             mbar_arrive_expect_tx(&sm.bar_f, fbytes);
-            bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
+            if (fbytes != 0u)
+                bulk_g2s(&sm.flags[0], a.flags + t0 - hf, fbytes, &sm.bar_f);
         }
         bool ok = true;
         if (threadIdx.x < 32)
@@ -731,6 +756,8 @@ cudaError_t select_launch(const void *arr, const uint8_t *flags, void *out, int3
     a.lb.recs = scratch + kHeaderSlots;
     a.lb.skip_tile = L.skip_tile;
     a.lb.spin_limit = L.spin_limit;
+    a.lb.nrec = 0;        // set by the kernel
+    a.out_end = nullptr;  // set by the kernel
     if (elem_bytes == 4)
         return launch_staged_select<uint32_t>(a, L);
     if (elem_bytes == 8)

@@ -41,6 +41,7 @@ struct SegArgs {
     int inclusive;
     int aligned_io;               // output has the input's 16-byte phase
     LookBack lb;                  // lb.recs == nullptr: no tile waits on another
+    const char *out_end;          // one past the call's output (set by the kernel; checked build)
 };
 
 #ifndef MT_STAGED_WAIT_WARP0
@@ -109,7 +110,7 @@ struct Staged {
     // be stale: the copy only covers chunks that hold valid elements).
     template <bool FULL>
     __device__ __forceinline__ static void load(const Smem &sm, int c, int llo, int lhi, Acc (&x)[E]) {
-        C::unpack(lds128(&sm.stage[c]), x);
+        C::unpack(MT_CHECK_INDEX(c, kChunks) ? lds128(&sm.stage[c]) : make_uint4(0u, 0u, 0u, 0u), x);
         if (!FULL) {
             const int o = c * E;
             if (!(o >= llo && o + E <= lhi)) {
@@ -133,13 +134,14 @@ struct Staged {
 #pragma unroll
             for (int r = 0; r < kPerPlane; ++r)
                 d[r] = (p * kPerPlane + r < E) ? x[p * kPerPlane + r] : Acc(0);
-            sts128(plane(sm, p, c), w);
+            if (MT_CHECK_INDEX(c, kChunks))
+                sts128(plane(sm, p, c), w);
         }
     }
     __device__ __forceinline__ static void get(Smem &sm, int c, Acc (&x)[E]) {
 #pragma unroll
         for (int p = 0; p < kPlanes; ++p) {
-            const uint4 w = lds128(plane(sm, p, c));
+            const uint4 w = MT_CHECK_INDEX(c, kChunks) ? lds128(plane(sm, p, c)) : make_uint4(0u, 0u, 0u, 0u);
             const Acc *d = reinterpret_cast<const Acc *>(&w);
 #pragma unroll
             for (int r = 0; r < kPerPlane; ++r)
@@ -167,8 +169,9 @@ struct Staged {
             load<FULL>(sm, u, llo, lhi, x);
         } else {
             const bool s = pair_swap();
-            const uint4 p = lds128(&sm.stage[2 * u + (s ? 1 : 0)]);
-            const uint4 q = lds128(&sm.stage[2 * u + (s ? 0 : 1)]);
+            const bool in = MT_CHECK_INDEX(2 * u + 1, kChunks) && MT_CHECK_INDEX(2 * u, kChunks);
+            const uint4 p = in ? lds128(&sm.stage[2 * u + (s ? 1 : 0)]) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 q = in ? lds128(&sm.stage[2 * u + (s ? 0 : 1)]) : make_uint4(0u, 0u, 0u, 0u);
             Acc lo[E], hi[E];
             C::unpack(pick(s, q, p), lo);
             C::unpack(pick(s, p, q), hi);
@@ -202,8 +205,10 @@ struct Staged {
                     d[r] = x[q * E + r];
             }
             const bool s = pair_swap();
-            sts128(&sm.stage[2 * u + (s ? 1 : 0)], pick(s, w[1], w[0]));
-            sts128(&sm.stage[2 * u + (s ? 0 : 1)], pick(s, w[0], w[1]));
+            if (MT_CHECK_INDEX(2 * u + 1, kChunks) && MT_CHECK_INDEX(2 * u, kChunks)) {
+                sts128(&sm.stage[2 * u + (s ? 1 : 0)], pick(s, w[1], w[0]));
+                sts128(&sm.stage[2 * u + (s ? 0 : 1)], pick(s, w[0], w[1]));
+            }
         }
     }
 
@@ -348,7 +353,7 @@ struct Staged {
             if (a.lb.recs != nullptr && g != first) {
                 pre = warp_lookback<Acc, Op>(a.lb.recs, g, first, a.lb.spin_limit);
                 if (lane == 0 && g != a.lb.skip_tile)
-                    Status<Acc>::publish(a.lb.recs + g * Status<Acc>::kSlots, kIncl, Op::apply(pre, agg));
+                    publish_record<Acc>(a.lb, g, kIncl, Op::apply(pre, agg));
             }
             if (lane == 0)
                 sm.prefix[buf] = pre;
@@ -388,15 +393,17 @@ struct Staged {
                 const int o = c * E;
                 if (!FULL && !(o < lhi && o + E > llo))
                     continue;
-                const uint4 w = lds128(&sm.stage[c]);
+                const uint4 w = MT_CHECK_INDEX(c, kChunks) ? lds128(&sm.stage[c]) : make_uint4(0u, 0u, 0u, 0u);
                 if (a.aligned_io && (FULL || (o >= llo && o + E <= lhi))) {
-                    st_v4(reinterpret_cast<uint4 *>(eo) + c, w);
+                    uint4 *p = reinterpret_cast<uint4 *>(eo) + c;
+                    if (MT_CHECK_RANGE(p, 16, a.out, a.out_end))
+                        st_v4(p, w);
                 } else {
                     Acc x[E];
                     C::unpack(w, x);
 #pragma unroll
                     for (int k = 0; k < E; ++k)
-                        if (FULL || (o + k >= llo && o + k < lhi))
+                        if ((FULL || (o + k >= llo && o + k < lhi)) && MT_CHECK_RANGE(eo + o + k, sizeof(S), a.out, a.out_end))
                             C::store1(eo + o + k, x[k]);
                 }
             }
@@ -530,11 +537,13 @@ struct Staged {
                 for (int k = 0; k < E; ++k)
                     x[k] = Op::apply(tp, x[k]);
                 if (a.aligned_io && (FULL || (o >= llo && o + E <= lhi))) {
-                    st_v4(reinterpret_cast<uint4 *>(eo) + c, C::pack(x));
+                    uint4 *p = reinterpret_cast<uint4 *>(eo) + c;
+                    if (MT_CHECK_RANGE(p, 16, a.out, a.out_end))
+                        st_v4(p, C::pack(x));
                 } else {
 #pragma unroll
                     for (int k = 0; k < E; ++k)
-                        if (FULL || (o + k >= llo && o + k < lhi))
+                        if ((FULL || (o + k >= llo && o + k < lhi)) && MT_CHECK_RANGE(eo + o + k, sizeof(S), a.out, a.out_end))
                             C::store1(eo + o + k, x[k]);
                 }
             }
@@ -563,6 +572,8 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) k_scan_staged
         tpr = a.tpr;
         ntiles = a.nseg * tpr;
     }
+    a.lb.nrec = ntiles;
+    a.out_end = a.out + (a.n_dev != nullptr ? n : a.nseg * n) * s;
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar, 1);
@@ -596,9 +607,12 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) k_scan_staged
 
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();  // the last iteration's shared-memory writes come first
-            const uint32_t bytes = (uint32_t)((cend - c0) * 16);
+            uint32_t bytes = (uint32_t)((cend - c0) * 16);
+            if (!MT_CHECK_RANGE(&sm.stage[0], bytes, &sm.stage[0], &sm.stage[G::kChunks]))
+                bytes = 0u;  // checked build: no copy (the phase completes with no bytes)
             mbar_arrive_expect_tx(&sm.bar, bytes);
-            bulk_g2s(&sm.stage[0], vin + c0, bytes, &sm.bar);
+            if (bytes != 0u)
+                bulk_g2s(&sm.stage[0], vin + c0, bytes, &sm.bar);
         }
         // Warp 0 waits for the copy; the block barrier then passes the
         // completion (and the copied bytes) on to the other warps.

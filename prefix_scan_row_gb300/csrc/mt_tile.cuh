@@ -43,6 +43,41 @@ constexpr uint32_t kCopyWaitLimit = 1u << 26;  // mbarrier polls before a copy i
 static __device__ int g_mt_err;
 
 // ---------------------------------------------------------------------------
+// Bounds-checked build. Compiled with MT_CHECKED=1, every global store and
+// every shared-memory access of the kernels is first checked against the
+// buffer it belongs to; an access outside it records MT_ERR_BOUNDS in the
+// device error word and is skipped (a load then yields zero). Nothing traps,
+// so a bad index shows up in mt_scan_status() and the context stays usable.
+// In the ordinary build the checks are the constant `true` and cost nothing.
+// ---------------------------------------------------------------------------
+#ifndef MT_CHECKED
+#define MT_CHECKED 0
+#endif
+constexpr int kErrBounds = -9;  // same value as MT_ERR_BOUNDS
+
+__device__ __forceinline__ bool check_index(long long i, long long n) {
+    if (i >= 0 && i < n)
+        return true;
+    atomicCAS(&g_mt_err, 0, kErrBounds);
+    return false;
+}
+// [p, p + bytes) inside [lo, hi)
+__device__ __forceinline__ bool check_range(const void *p, unsigned long long bytes, const void *lo, const void *hi) {
+    const uintptr_t a = (uintptr_t)p, l = (uintptr_t)lo, h = (uintptr_t)hi;
+    if (a >= l && a <= h && bytes <= (unsigned long long)(h - a))
+        return true;
+    atomicCAS(&g_mt_err, 0, kErrBounds);
+    return false;
+}
+#if MT_CHECKED
+#define MT_CHECK_INDEX(i, n) ::mt::check_index((long long)(i), (long long)(n))
+#define MT_CHECK_RANGE(p, bytes, lo, hi) ::mt::check_range((p), (bytes), (lo), (hi))
+#else
+#define MT_CHECK_INDEX(i, n) true
+#define MT_CHECK_RANGE(p, bytes, lo, hi) true
+#endif
+
+// ---------------------------------------------------------------------------
 // Combine operators. apply(a, b): `a` covers earlier elements than `b`.
 // ---------------------------------------------------------------------------
 template <class T> struct Lim;

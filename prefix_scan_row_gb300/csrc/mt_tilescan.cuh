@@ -39,9 +39,11 @@ struct RowTile {
     //   eout      : output address of virtual element 0 (element pointer)
     //   aligned_io: eout is 16-byte aligned (same phase as the input)
     //   [lo, hi)  : the row's valid virtual range; FULL: all of the tile
+    //   [olo, ohi): the row's output bytes (every store is checked against
+    //               them in a bounds-checked build)
     template <bool FULL>
     __device__ __forceinline__ static void run(const uint4 *vin, S *eout, bool aligned_io, int lo, int hi,
-                                               bool inclusive, Smem &sm) {
+                                               bool inclusive, Smem &sm, const char *olo, const char *ohi) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const Acc ident = Op::template identity<Acc>();
 
@@ -106,7 +108,7 @@ struct RowTile {
             pre[j] = Op::apply(run, e);
             run = Op::apply(run, __shfl_sync(kFull, inc[j], 31));
         }
-        if (lane == 0)
+        if (lane == 0 && MT_CHECK_INDEX(warp, kMaxWarps))
             sm.warp_tot[warp] = run;
         __syncthreads();
 
@@ -141,11 +143,13 @@ struct RowTile {
             const int c = chunk_of(j);
             const int o = c * E;
             if (aligned_io && (FULL || (o >= lo && o + E <= hi))) {
-                st_v4(reinterpret_cast<uint4 *>(eout) + c, C::pack(x[j]));
+                uint4 *p = reinterpret_cast<uint4 *>(eout) + c;
+                if (MT_CHECK_RANGE(p, 16, olo, ohi))
+                    st_v4(p, C::pack(x[j]));
             } else if (FULL || (o < hi && o + E > lo)) {
 #pragma unroll
                 for (int k = 0; k < E; ++k)
-                    if (FULL || (o + k >= lo && o + k < hi))
+                    if ((FULL || (o + k >= lo && o + k < hi)) && MT_CHECK_RANGE(eout + o + k, sizeof(S), olo, ohi))
                         C::store1(eout + o + k, x[j][k]);
             }
         }

@@ -53,6 +53,17 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= exported
 
 
+def test_checked_build_exports_the_same_calls(lib):
+    """The bounds-checked twin exports every declared call too, and says which
+    build it is (no kernel is launched)."""
+    import __graft_entry__
+    checked = ctypes.CDLL(__graft_entry__._build_module().build(checked=True))
+    out = subprocess.run(["nm", "-D", "--defined-only", checked._name], capture_output=True, text=True).stdout
+    assert set(declared_functions()) <= set(re.findall(r"\bT (mt_\w+)", out))
+    assert checked.mt_scan_build_checked() == 1
+    assert lib.mt_scan_build_checked() == 0
+
+
 def test_binding_names_match_header():
     import prefix_scan_row_gb300 as m
     assert sorted(m.EXPORTS) == declared_functions()
