@@ -470,27 +470,70 @@ def run_ours(args, world, rank, local):
     time.sleep(0.05)
     sampler.stop()
 
-    # End to end through the C ABI from host buffers: every step copies the
-    # three inputs' live elements from pinned host memory to the device, makes
-    # the nine calls, and copies each call's result to its own pinned host
-    # buffer (on a second stream, so a result's copy overlaps the next call).
+    # End to end through the C ABI from host buffers (run_e2e).
+    if args.no_e2e:
+        e2e_line = None
+    else:
+        e2e_line = run_e2e(args, s1d, host, stream, dev, world)
+    value = nbytes / (ms / 1e3) / 1e9
+    achieved = DOM_BYTES / (dom_ms / 1e3) / 1e9
+    line = make_line(args, world, value, ms, peak, peak_src, achieved, dom_ms, dom_n, kernels, sampler, th0, th1,
+                     tk0, tk1, launches, e2e_line)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(host)
+        line["cpu_all_cores"] = cpu_all_cores(host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, s1d, host, stream, dev, world):
+    """The e2e entry: the step through the C ABI from pinned host buffers.
+
+    Every step copies the three inputs' live elements from pinned host memory
+    to the device, makes the nine calls, and copies each call's result to its
+    own pinned host buffer. Uploads run on one copy stream into two device
+    input sets in turn and downloads on another, so a step's upload overlaps
+    the previous step's downloads (the host link carries both directions at
+    once) and each result's download overlaps the next call."""
+    mt = s1d.mt
     pin_in = {d: host[d][:N_LIVE].pin_memory() for d in DTYPES}
     pin_out = [torch.empty(N_LIVE, dtype=TORCH_DT[d]).pin_memory() for d, _ in CALLS]
     dev_out = [torch.empty(N_LIVE, dtype=TORCH_DT[d], device=dev) for d, _ in CALLS]
-    copy = torch.cuda.Stream(dev)
-    done = [torch.cuda.Event() for _ in CALLS]
+    sets = [s1d.arr, {d: torch.empty_like(s1d.arr[d]) for d in DTYPES}]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = torch.cuda.Event
+    loaded = [ev(), ev()]          # a set's inputs are on the device
+    consumed = [ev(), ev()]        # a set's last call has read its inputs
+    computed = [ev() for _ in CALLS]   # call i's result is written
+    fetched = [ev() for _ in CALLS]    # call i's result has reached the host
+    step_no = [0]
 
     def e2e_step():
-        for d in DTYPES:
-            s1d.arr[d][:N_LIVE].copy_(pin_in[d], non_blocking=True)
+        k = step_no[0]
+        b = k % 2
+        arr = sets[b]
+        up.wait_event(consumed[b])  # the calls of step k - 2 are done with this set
+        with torch.cuda.stream(up):
+            for d in DTYPES:
+                arr[d][:N_LIVE].copy_(pin_in[d], non_blocking=True)
+        loaded[b].record(up)
+        stream.wait_event(loaded[b])
         for i, (d, op) in enumerate(CALLS):
-            s1d.call(d, op, stream, out=dev_out[i])
-            done[i].record(stream)
-            copy.wait_event(done[i])
-            with torch.cuda.stream(copy):
+            stream.wait_event(fetched[i])  # the previous step's copy of this result is out
+            mt.mt_exclusive_scan(arr[d], dev_out[i], s1d.scratch[d], s1d.n_dev, op, stream)
+            computed[i].record(stream)
+            down.wait_event(computed[i])
+            with torch.cuda.stream(down):
                 pin_out[i].copy_(dev_out[i], non_blocking=True)
-        stream.wait_stream(copy)
+            fetched[i].record(down)
+        consumed[b].record(stream)
+        step_no[0] += 1
 
+    for e in consumed + fetched:
+        e.record(stream)
     e2e_steps = max(1, min(args.steps, 5))
     e2e_step()
     torch.cuda.synchronize()
@@ -499,6 +542,8 @@ def run_ours(args, world, rank, local):
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
+    stream.wait_stream(down)
+    stream.wait_stream(up)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -506,9 +551,16 @@ def run_ours(args, world, rank, local):
     e2e_ms, e2e_bytes = aggregate(e0.elapsed_time(e1), STEP_BYTES * e2e_steps, dev if world > 1 else None)
     h2d = sum(pin_in[d].numel() * pin_in[d].element_size() for d in DTYPES)
     d2h = sum(t.numel() * t.element_size() for t in pin_out)
+    return {"value": round(e2e_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+            "how": "pinned host -> device copy of the 3 inputs' live elements (one copy stream, two device input "
+                   "sets in turn), the 9 mt_exclusive_scan calls, device -> pinned host copy of each call's result "
+                   "(a second copy stream); a step's upload overlaps the previous step's downloads; CUDA events "
+                   "around the steps"}
 
-    value = nbytes / (ms / 1e3) / 1e9
-    achieved = DOM_BYTES / (dom_ms / 1e3) / 1e9
+
+def make_line(args, world, value, ms, peak, peak_src, achieved, dom_ms, dom_n, kernels, sampler, th0, th1, tk0,
+              tk1, launches, e2e_line):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
@@ -523,11 +575,7 @@ def run_ours(args, world, rank, local):
         "elements_per_s": round(STEP_ELEMS * world * args.steps / (ms / 1e3), 1),
         "frac_of_peak": {"measured": round(value / world / peak, 4), "peak_gbs": peak,
                          "peak_source": peak_src, "datasheet_8000_gbs": round(value / world / 8000.0, 4)},
-        "e2e": {"value": round(e2e_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "how": "pinned host -> device copy of the 3 inputs' live elements, the 9 mt_exclusive_scan calls, "
-                       "device -> pinned host copy of each call's result on a second stream (overlapping the next "
-                       "call); CUDA events around the steps"},
+        "e2e": e2e_line,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic("scan1d_i64_add", "scan1d"),
                      "kernel": "k_scan_staged<long, OpAdd, 4, 3, 256> (1-D exclusive scan, i64 add)",
@@ -540,14 +588,9 @@ def run_ours(args, world, rank, local):
         "clocks_kernels": sampler.summary(tk0, tk1),
         "gpu_launches": int(launches),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(host)
-        line["cpu_all_cores"] = cpu_all_cores(host)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    if e2e_line is None:
+        del line["e2e"]
+    return line
 
 
 # ---------------------------------------------------------------------------
@@ -806,6 +849,8 @@ def main():
                     help="skip the CPU baselines (profiling runs)")
     ap.add_argument("--no-kernels", action="store_true",
                     help="skip the per-kernel back-to-back entries (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg through host buffers (profiling runs)")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every configured shape")
     ap.add_argument("--suite-out", default=None)
     ap.add_argument("--only", default=None, help="suite: run only configs whose name contains this")
