@@ -35,6 +35,9 @@ namespace mt {
 #define MT_RBK_LB_PER_LANE 1  // predecessors per lane per look-back poll
 #endif
 constexpr int kRbkLbPerLane = MT_RBK_LB_PER_LANE;
+#ifndef MT_RBK_EARLY
+#define MT_RBK_EARLY 1  // publish each super-tile's pair from a keys-only pass, before the scan
+#endif
 #ifndef MT_RBK_TILE
 #define MT_RBK_TILE 6144  // elements per super-tile (a multiple of 2048)
 #endif
@@ -131,6 +134,9 @@ struct RbkSmem {
     uint32_t kprev, knext;     // the neighbours' keys (when they exist)
     uint32_t warp_c[kRbkSub][kRbkThreads / 32];  // warp totals of each sub-tile's scan
     uint32_t warp_s[kRbkSub][kRbkThreads / 32];
+    uint32_t hcount[kRbkThreads / 32];  // each warp's heads in the super-tile
+    int32_t hlast[kRbkThreads / 32];    // each warp's last head (-1: none)
+    uint64_t agg;                       // the super-tile's pair
     uint64_t prefix;
 };
 static_assert(offsetof(RbkSmem, bar) % 8 == 0, "shared-memory layout of the reduce-by-key kernel");
@@ -173,15 +179,93 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
     const uint32_t *skey = reinterpret_cast<const uint32_t *>(sm.keys);
     const uint32_t kprev = sm.kprev, knext = sm.knext;
 
-    // Pass 1. The key before a unit is the last key of the lane to the left.
     uint32_t mh[kRbkSub];
+#if MT_RBK_EARLY
+    // Pass 0: each unit's head bits from the keys alone (the key before a
+    // unit is the last key of the lane to the left), and the super-tile's
+    // head count and last head.
+    {
+        uint32_t cnt = 0u;
+        int last = -1;
+#pragma unroll
+        for (int s = 0; s < kRbkSub; ++s) {
+            const int u = s * kRbkThreads + threadIdx.x;
+            uint4 k0, k1;
+            load_unit(sm.keys, u, k0, k1);
+            uint32_t prev = __shfl_up_sync(kFull, k1.w, 1);
+            if (lane == 0)
+                prev = (8 * u - 1 >= llo && MT_CHECK_INDEX(8 * u - 1, kRbkTE)) ? skey[8 * u - 1] : kprev;
+            uint32_t m = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = 8 * u + k;
+                const uint32_t key = word8(k0, k1, k);
+                if (FULL || (i >= llo && i < lhi)) {
+                    // the first element starts a run whatever its key
+                    const bool first = has_first && (FULL ? (k == 0 && u == 0) : i == llo);
+                    m |= ((first || keys_differ<KF>(key, prev)) ? 1u : 0u) << k;
+                }
+                prev = key;
+            }
+            if (MT_CHECK_INDEX(u, kRbkUnits))
+                sm.heads[u] = (uint8_t)m;
+            mh[s] = m;
+            cnt += (uint32_t)__popc(m);
+            if (m != 0u)
+                last = 8 * u + 31 - __clz(m);  // units grow with s: the thread's last head
+        }
+        cnt = __reduce_add_sync(kFull, cnt);
+        last = __reduce_max_sync(kFull, last);
+        if (lane == 0) {
+            sm.hcount[warp] = cnt;
+            sm.hlast[warp] = last;
+        }
+    }
+    __syncthreads();  // head bits and per-warp counts are written
+    // The last warp publishes the super-tile's pair before the scan: the
+    // head count, and the sum of the values from the last head on (of all
+    // valid values when the tile has no head), so later tiles' look-backs
+    // find it sooner.
+    if (warp == kNW - 1) {
+        const uint32_t c = __reduce_add_sync(kFull, lane < kNW ? sm.hcount[lane] : 0u);
+        const int hl = __reduce_max_sync(kFull, lane < kNW ? sm.hlast[lane] : -1);
+        const uint32_t *sval = reinterpret_cast<const uint32_t *>(sm.vals);
+        V part = V(0);
+        for (int i = (hl >= 0 ? hl : llo) + lane; i < lhi; i += 32)
+            part += P::val(MT_CHECK_INDEX(i, kRbkTE) ? sval[i] : 0u);
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1)
+            part += __shfl_xor_sync(kFull, part, d);
+        if (lane == 0) {
+            const uint64_t aggp = ((uint64_t)c << 32) | P::bits(part);
+            sm.agg = aggp;
+            if (a.lb.recs != nullptr && g != a.lb.skip_tile)
+                publish_record<uint64_t>(a.lb, g, g == 0 ? kIncl : kAgg, aggp);
+        }
+    }
+#endif
+
+    // Pass 1. The key before a unit is the last key of the lane to the left.
     P ex[kRbkSub];
 #pragma unroll
     for (int s = 0; s < kRbkSub; ++s) {
         const int u = s * kRbkThreads + threadIdx.x;
-        uint4 k0, k1, v0, v1;
-        load_unit(sm.keys, u, k0, k1);
+        uint4 v0, v1;
         load_unit(sm.vals, u, v0, v1);
+#if MT_RBK_EARLY
+        const uint32_t m = mh[s];
+        V sum = V(0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = 8 * u + k;
+            if (FULL || (i >= llo && i < lhi)) {
+                const V v = P::val(word8(v0, v1, k));
+                sum = ((m >> k) & 1u) ? v : sum + v;
+            }
+        }
+#else
+        uint4 k0, k1;
+        load_unit(sm.keys, u, k0, k1);
         uint32_t prev = __shfl_up_sync(kFull, k1.w, 1);
         if (lane == 0)
             prev = (8 * u - 1 >= llo && MT_CHECK_INDEX(8 * u - 1, kRbkTE)) ? skey[8 * u - 1] : kprev;
@@ -204,6 +288,7 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
         if (MT_CHECK_INDEX(u, kRbkUnits))
             sm.heads[u] = (uint8_t)m;
         mh[s] = m;
+#endif
         P inc{(uint32_t)__popc(m), sum};
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -245,8 +330,12 @@ __device__ __forceinline__ void rbk_tile(RbkSmem &sm, const RbkArgs &a, int64_t 
     // Warp 0: the super-tile's pair (published at once), the look-back, the
     // inclusive prefix.
     if (warp == 0) {
+#if MT_RBK_EARLY
+        const uint64_t aggp = sm.agg;  // published before the scan
+#else
         const uint64_t aggp = ((uint64_t)carry.c << 32) | P::bits(carry.s);
         publish_aggregate<uint64_t, Op>(a.lb, g, 0, aggp);
+#endif
         uint64_t pre = 0;  // the identity pair
         if (a.lb.recs != nullptr && g != 0) {
             pre = warp_lookback<uint64_t, Op, kRbkLbPerLane>(a.lb.recs, g, 0, a.lb.spin_limit);
