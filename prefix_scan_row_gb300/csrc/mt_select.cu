@@ -132,8 +132,9 @@ __device__ __forceinline__ uint32_t count_flags(const uint4 *flags, int warp, in
 // look back for the tile's output offset, copy the packed runs out. Warp w
 // owns the flag bytes [1024 w, 1024 (w + 1)) of the copy (the last warp also
 // the copy's extra chunk when hf + elems passes the tile) and packs the
-// elements they hold. FAST: a full tile with hf = hv = 0, so no flag or
-// element needs a range check. (Looking back before the packing, overlapped
+// elements they hold. FAST: a full tile with hf = 0 (the flags at a 16-byte
+// boundary, the values at any offset hv), so no flag or element needs a range
+// check. (Looking back before the packing, overlapped
 // with it, was measured slower: the look-back then meets more predecessors
 // that have only published their counts.)
 //
@@ -175,7 +176,7 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
                                             uint32_t vphase, bool &dense) {
     using Sh = SelShape<VT>;
     constexpr int kTE = (int)Sh::kTE;
-    const int hf = FAST ? 0 : hf_, hv = FAST ? 0 : hv_;
+    const int hf = FAST ? 0 : hf_, hv = hv_;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hi = hf + elems;  // one past the copy's last flag byte of the tile
     const bool extra = !FAST && warp == kWarps - 1 && hi > kTE;
@@ -266,11 +267,14 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
         };
         static_assert((Sh::kItems * 16) % kSelBatch == 0, "whole batches of steps");
         if constexpr (FAST && sizeof(VT) == 4) {
-            // A full tile at the 16-byte boundaries: lane l of step s takes
-            // the 4 elements of chunk 32 s + l of the warp's range, as one
-            // 4-byte flag word and one 16-byte value chunk. Flags are exactly
-            // 0 or 1, so popc(word) is the chunk's count, and the warp's
-            // exclusive prefix of those counts (0 to 4) comes from 3 ballots.
+            // A full tile with its flags at a 16-byte boundary: lane l of
+            // step s takes the 4 elements of chunk 32 s + l of the warp's
+            // range, as one 4-byte flag word and 16 bytes of values (one
+            // aligned chunk, or, with the values hv slots past the boundary,
+            // the two aligned chunks around them shifted by hv words). Flags
+            // are exactly 0 or 1, so popc(word) is the chunk's count, and the
+            // warp's exclusive prefix of those counts (0 to 4) comes from 3
+            // ballots.
             const uint32_t *fw = reinterpret_cast<const uint32_t *>(fb) + wstart / 4;
             const uint4 *vc = reinterpret_cast<const uint4 *>(sm.vals + wstart);
             constexpr int kSteps = Sh::kItems * 4;  // 128 elements per step
@@ -283,8 +287,18 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
                 for (int j = 0; j < kB; ++j) {
                     f[j] = MT_CHECK_INDEX(wstart / 4 + (s0 + j) * 32 + lane, kFlagBytes / 4) ? fw[(s0 + j) * 32 + lane] : 0u;
                     v[j] = make_uint4(0u, 0u, 0u, 0u);
-                    if (f[j] != 0u && MT_CHECK_INDEX(wstart / 4 + (s0 + j) * 32 + lane, kVals / 4))
-                        v[j] = lds128(&vc[(s0 + j) * 32 + lane]);
+                    const int c = (s0 + j) * 32 + lane;
+                    if (f[j] != 0u && MT_CHECK_INDEX(wstart / 4 + c, kVals / 4)) {
+                        const uint4 p = lds128(&vc[c]);
+                        if (hv == 0) {  // block-uniform
+                            v[j] = p;
+                        } else {
+                            const uint4 q = MT_CHECK_INDEX(wstart / 4 + c + 1, kVals / 4) ? lds128(&vc[c + 1])
+                                                                                        : make_uint4(0u, 0u, 0u, 0u);
+                            v[j] = hv == 1 ? make_uint4(p.y, p.z, p.w, q.x)
+                                           : (hv == 2 ? make_uint4(p.z, p.w, q.x, q.y) : make_uint4(p.w, q.x, q.y, q.z));
+                        }
+                    }
                 }
                 __syncwarp();
 #pragma unroll
@@ -418,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, sel_staged_minb<VT>()) k_select_stag
             }
             ok = false;
         } else {
-            ok = (elems == kSelTE && hf == 0 && hvb == 0)
+            ok = (elems == kSelTE && hf == 0)  // a full tile with aligned flags (the values at any offset)
                      ? select_tile<true, VT>(sm, a, g, ntiles, elems, hf, hv, guess_dense, vphase, dense)
                      : select_tile<false, VT>(sm, a, g, ntiles, elems, hf, hv, guess_dense, vphase, dense);
         }

@@ -130,7 +130,7 @@ def test_checked_scan_and_reduce(ck, dtype, op, n, off):
 
 @pytest.mark.parametrize("n", [1, 8191, 8193, 16385, 100003])
 @pytest.mark.parametrize("p", [0.5, 0.01])
-@pytest.mark.parametrize("voff,foff", [(0, 0), (1, 0), (0, 3), (3, 5)])
+@pytest.mark.parametrize("voff,foff", [(0, 0), (1, 0), (2, 0), (3, 0), (0, 3), (3, 5)])
 def test_checked_select(ck, n, p, voff, foff):
     vals, flags = workloads.select_inputs(n, p, seed=50 + n)
     v = _on_device(vals, voff)

@@ -84,6 +84,20 @@ def test_select_16_byte_phases_at_tile_edges(mt, arr_off, flag_off, n, p):
     assert_select_matches(out, num, vals, flags, n)
 
 
+@pytest.mark.parametrize("arr_off", [1, 2, 3])
+@pytest.mark.parametrize("n", [16384, 3 * 16384, 3 * 16384 + 5, 100003])
+@pytest.mark.parametrize("p", [0.01, 0.3, 0.9, 1.0])
+def test_select_aligned_flags_values_off_boundary(mt, arr_off, n, p):
+    """Flags at a 16-byte boundary and values 1 to 3 slots past one: the full
+    tiles take the chunk-wise packing, which reads each chunk's values from
+    the two aligned 16-byte chunks around them; the bit patterns make a
+    shift by the wrong number of slots visible."""
+    bits = workloads.randint((n,), 51 + arr_off, -(2**31), 2**31 - 1, "i32")
+    flags = workloads.bernoulli_u8(n, p, 52 + n)
+    out, num = run_select(mt, bits.view(torch.float32), flags, n, arr_off, 0, 0)
+    assert_select_matches(out, num, bits, flags, n)
+
+
 def test_select_bit_patterns(mt):
     """Any 32-bit pattern (NaNs, -0.0, denormals) is copied unchanged."""
     n = 40000
