@@ -90,6 +90,8 @@ FAMILY_SOURCES = {
              "mt_staged.cuh"],
     "scan1d": ["mt_internal.h", "mt_tile.cuh", "mt_lookback.cuh", "mt_staged.cuh", "mt_scan1d.cuh", "mt_scan1d.cu"],
     "select": ["mt_internal.h", "mt_tile.cuh", "mt_lookback.cuh", "mt_select.cu"],
+    "reduce": ["mt_internal.h", "mt_tile.cuh", "mt_reduce.cu"],
+    "rbk": ["mt_internal.h", "mt_tile.cuh", "mt_lookback.cuh", "mt_rbk.cu"],
 }
 
 
@@ -346,8 +348,10 @@ def sets_for(nbytes):
 
 
 def measure_kernels(mt, s1d, stream, dev, peak):
-    """Every scan kernel on its configured workload, each timed back to back
-    after the main timed region (see back_to_back)."""
+    """Every kernel on its configured workload (the scans, long rows and
+    select), and the struct select, the reduction and reduce-by-key on the
+    suite's workloads, each timed back to back after the main timed region
+    (see back_to_back)."""
     ks = {}
     for d, op in CALLS:
         ms, n = back_to_back([lambda d=d, op=op: s1d.call(d, op, stream)], stream)
@@ -419,7 +423,47 @@ def measure_kernels(mt, s1d, stream, dev, peak):
             note="bytes_per_launch = 5 n + 4 num_out (flags and values read, selected values written); each call "
                  "is a status-reset launch plus the select launch")
         del flags
-    del vals, out, scr
+    # select of 12-byte structs (k_select_words<3>): the f32 values above as
+    # the first word of each struct, p = 0.5
+    flags = workloads.bernoulli_u8(ns, 0.5, workloads.SEED_SELECT + 1).to(dev)
+    k = int(flags.sum().item())
+    v3 = vals.view(torch.int32).unsqueeze(1).expand(ns, 3).contiguous()
+    del out
+    o3 = torch.empty_like(v3)
+    ms, nl = back_to_back([lambda: mt.mt_select_wide(v3, flags, o3, num, scr, nd, stream)], stream)
+    ks["select_struct12_p05"] = kernel_entry(
+        "k_select_words<3> (12-byte structs)", "select of 12-byte structs, n = 2^28, flags Bernoulli(p = 0.5)",
+        13 * ns + 12 * k, ms, nl, 1, peak, "select_struct12_p05", "select", selected=k,
+        note="bytes_per_launch = 13 n + 12 num_out by the select formula (flags and structs read, selected "
+             "structs written); each call is a status-reset launch plus the select launch")
+    del v3, o3, flags, vals, scr
+    # reduce: i32 add over the step's i32 input (n = 2^28 - 12345), read only
+    rscr = mt.alloc_scratch(CAPACITY, torch.int32, mt.MT_SCRATCH_REDUCE, device=dev)
+    r1 = torch.empty(1, dtype=torch.int32, device=dev)
+    ms, nl = back_to_back([lambda: mt.mt_reduce(s1d.arr["i32"], r1, rscr, s1d.n_dev, "add", stream)], stream)
+    ks["reduce_i32_add"] = kernel_entry(
+        "k_reduce (i32, add)", "reduce i32 add, n = 2^28-12345 (the step's i32 input)", 4 * N_LIVE, ms, nl, 1, peak,
+        "reduce_i32_add", "reduce",
+        note="bytes_per_launch = 4 n, read only, against the read+write copy peak; each call is a reset launch "
+             "plus the reduce launch")
+    del rscr, r1
+    # reduce by key: n = 2^28 i32 keys in runs of geometric length (mean 8,
+    # keys from an alphabet of 64), f32 values (seed 11)
+    kk, vv = workloads.runs(ns, 8.0, workloads.SEED_SELECT + 7, "i32", "f32")
+    kk, vv = kk.to(dev), vv.to(dev)
+    ko, vo = torch.empty_like(kk), torch.empty_like(vv)
+    bscr = mt.alloc_scratch(ns, torch.int32, mt.MT_SCRATCH_REDUCE_BY_KEY, device=dev)
+    mt.mt_reduce_by_key_add(kk, vv, ko, vo, num, bscr, nd, stream)
+    torch.cuda.synchronize()
+    runs_n = int(num.item())
+    ms, nl = back_to_back([lambda: mt.mt_reduce_by_key_add(kk, vv, ko, vo, num, bscr, nd, stream)], stream)
+    ks["reduce_by_key_i32_f32"] = kernel_entry(
+        "k_reduce_by_key (i32 keys, f32 values)",
+        "reduce_by_key_add, n = 2^28, i32 keys in runs of geometric length (mean 8), f32 values",
+        8 * ns + 8 * runs_n, ms, nl, 1, peak, "reduce_by_key_i32_f32", "rbk", runs=runs_n,
+        note="bytes_per_launch = 8 n + 8 runs (keys and values read, one key and one sum written per run); each "
+             "call is a reset launch plus the reduce-by-key launch")
+    del kk, vv, ko, vo, bscr
     torch.cuda.synchronize()
     assert mt.mt_scan_status(stream) == 0, "device error word set while timing the kernels"
     return ks
