@@ -546,6 +546,8 @@ def run_e2e(args, s1d, host, stream, dev, world):
     pin_in = {d: host[d][:N_LIVE].pin_memory() for d in DTYPES}
     pin_out = [torch.empty(N_LIVE, dtype=TORCH_DT[d]).pin_memory() for d, _ in CALLS]
     dev_out = [torch.empty(N_LIVE, dtype=TORCH_DT[d], device=dev) for d, _ in CALLS]
+    # two device input sets: the step's own buffers (rewritten with the same
+    # values) and a second one of the same shape
     sets = [s1d.arr, {d: torch.empty_like(s1d.arr[d]) for d in DTYPES}]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = torch.cuda.Event
