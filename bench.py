@@ -674,9 +674,9 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------------------
-# --suite: each kernel on each configured shape (not the bench line; a table
-# for the design notes). Calls are timed one by one with CUDA events; L2 is
-# flushed before every timed call whose buffers would fit in it.
+# --suite: each kernel on each configured shape, one JSON line per call (not
+# the bench line). Calls are timed one by one with CUDA events; L2 is flushed
+# before every timed call whose buffers would fit in it.
 # ---------------------------------------------------------------------------
 def run_suite(args):
     import prefix_scan_row_gb300 as mt
