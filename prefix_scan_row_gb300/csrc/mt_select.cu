@@ -271,10 +271,13 @@ __device__ __forceinline__ bool select_tile(SelStagedSmem<VT> &sm, const SelArgs
             // step s takes the 4 elements of chunk 32 s + l of the warp's
             // range, as one 4-byte flag word and 16 bytes of values (one
             // aligned chunk, or, with the values hv slots past the boundary,
-            // the two aligned chunks around them shifted by hv words). Flags
-            // are exactly 0 or 1, so popc(word) is the chunk's count, and the
-            // warp's exclusive prefix of those counts (0 to 4) comes from 3
-            // ballots.
+            // the two aligned chunks around them shifted by hv words; the
+            // other words of those chunks belong to neighbouring elements and
+            // are dropped, so earlier packing writes that reached them do no
+            // harm, while the chunk's own 4 slots lie past every slot an
+            // earlier batch wrote). Flags are exactly 0 or 1, so popc(word)
+            // is the chunk's count, and the warp's exclusive prefix of those
+            // counts (0 to 4) comes from 3 ballots.
             const uint32_t *fw = reinterpret_cast<const uint32_t *>(fb) + wstart / 4;
             const uint4 *vc = reinterpret_cast<const uint4 *>(sm.vals + wstart);
             constexpr int kSteps = Sh::kItems * 4;  // 128 elements per step

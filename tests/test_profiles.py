@@ -57,3 +57,11 @@ def test_sidecar_traffic_near_algorithmic_bytes(tag):
 def test_dominant_kernel_sidecar_is_the_roofline_one():
     d = load("scan1d_i64_add")
     assert d["algorithmic_bytes_per_launch"] == bench.DOM_BYTES
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    src = "int a = 1;  // one\n/* block\n   comment */\nint b = a + 2;\n"
+    same = "int a = 1;  // another note\n\nint b = a + 2;   \n"
+    changed = "int a = 1;\nint b = a + 3;\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(changed)
