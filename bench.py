@@ -351,6 +351,13 @@ def kernel_entry(kernel, workload, nbytes, ms, launches, sets, peak, profile, fa
     return e
 
 
+def launches_for(nbytes):
+    """Back-to-back launches of a kernel entry: calls under 256 MB (tens of
+    microseconds each) take ten times as many, so each entry times a few
+    milliseconds of work at least."""
+    return B2B_LAUNCHES if nbytes >= (256 << 20) else 10 * B2B_LAUNCHES
+
+
 def sets_for(nbytes):
     """Buffer sets whose bytes together exceed twice the L2."""
     return max(1, -(-2 * L2_BYTES // nbytes))
@@ -399,7 +406,7 @@ def measure_kernels(mt, s1d, stream, dev, peak):
         xs = [x] + [x.clone() for _ in range(sets - 1)]
         os_ = [torch.empty_like(x) for _ in range(sets)]
         fns = [lambda xi=xi, oi=oi: mt.mt_scan_rows(xi, oi, inc, stream) for xi, oi in zip(xs, os_)]
-        ms, nl = back_to_back(fns, stream)
+        ms, nl = back_to_back(fns, stream, launches_for(nb))
         ks[name] = kernel_entry(kern, wl, nb, ms, nl, sets, peak, name, "rows")
         del xs, os_, fns
     # the four row calls of the bf16/f16 workload as one sequence
@@ -408,8 +415,8 @@ def measure_kernels(mt, s1d, stream, dev, peak):
     outs = [torch.empty_like(half[(r, n, d)]) for r, n, d, _ in seq]
     fns = [lambda x=half[(r, n, d)], o=o, inc=inc: mt.mt_scan_rows(x, o, inc, stream)
            for (r, n, d, inc), o in zip(seq, outs)]
-    ms, nl = back_to_back(fns, stream)
     nb = sum(call_bytes(r, n, d) for r, n, d, _ in seq) / len(seq)
+    ms, nl = back_to_back(fns, stream, launches_for(nb))
     ks["rows_half_4_calls"] = kernel_entry(
         "k_scan_rows (bf16, f16)", "bf16 and f16 [8192,8192] exclusive then [4096,4099] inclusive, in turn", nb, ms,
         nl, 1, peak, None, "rows",
