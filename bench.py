@@ -340,6 +340,39 @@ def back_to_back(fns, stream, launches=B2B_LAUNCHES):
     return a.elapsed_time(b) / (rounds * len(fns)), rounds * len(fns)
 
 
+def graph_back_to_back(fns, launches):
+    """The same as back_to_back for calls of a few microseconds: the calls
+    (each takes the stream to enqueue on) are captured once, round-robin, in
+    one CUDA graph on a side stream, and the graph is replayed between one
+    event pair after one warm-up replay, so each launch costs the GPU's own
+    scheduling and not a host submission."""
+    side = torch.cuda.Stream()
+    rounds = max(1, math.ceil(launches / len(fns)))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        for f in fns:  # warm-up outside the capture
+            f(side)
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(rounds):
+                for f in fns:
+                    f(side)
+        g.replay()
+        side.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(side)
+        g.replay()
+        b.record(side)
+        b.synchronize()
+    del g
+    return a.elapsed_time(b) / (rounds * len(fns)), rounds * len(fns)
+
+
+GRAPH_TIMING = ("calls captured round-robin in one CUDA graph and replayed between one event pair after a "
+                "warm-up replay (calls under 256 MB, a few microseconds each)")
+
+
 def kernel_entry(kernel, workload, nbytes, ms, launches, sets, peak, profile, family, **extra):
     achieved = nbytes / (ms / 1e3) / 1e9
     e = {"kernel": kernel, "workload": workload, "bound": "hbm", "bytes_per_launch": int(nbytes),
@@ -405,21 +438,26 @@ def measure_kernels(mt, s1d, stream, dev, peak):
         sets = sets_for(nb)
         xs = [x] + [x.clone() for _ in range(sets - 1)]
         os_ = [torch.empty_like(x) for _ in range(sets)]
-        fns = [lambda xi=xi, oi=oi: mt.mt_scan_rows(xi, oi, inc, stream) for xi, oi in zip(xs, os_)]
-        ms, nl = back_to_back(fns, stream, launches_for(nb))
-        ks[name] = kernel_entry(kern, wl, nb, ms, nl, sets, peak, name, "rows")
+        if nb < (256 << 20):  # single-tile rows: no allocation, capturable
+            fns = [lambda st, xi=xi, oi=oi: mt.mt_scan_rows(xi, oi, inc, st) for xi, oi in zip(xs, os_)]
+            ms, nl = graph_back_to_back(fns, launches_for(nb))
+            ks[name] = kernel_entry(kern, wl, nb, ms, nl, sets, peak, name, "rows", timing=GRAPH_TIMING)
+        else:
+            fns = [lambda xi=xi, oi=oi: mt.mt_scan_rows(xi, oi, inc, stream) for xi, oi in zip(xs, os_)]
+            ms, nl = back_to_back(fns, stream, launches_for(nb))
+            ks[name] = kernel_entry(kern, wl, nb, ms, nl, sets, peak, name, "rows")
         del xs, os_, fns
     # the four row calls of the bf16/f16 workload as one sequence
     seq = [(8192, 8192, "bf16", False), (8192, 8192, "f16", False), (4096, 4099, "bf16", True),
            (4096, 4099, "f16", True)]
     outs = [torch.empty_like(half[(r, n, d)]) for r, n, d, _ in seq]
-    fns = [lambda x=half[(r, n, d)], o=o, inc=inc: mt.mt_scan_rows(x, o, inc, stream)
+    fns = [lambda st, x=half[(r, n, d)], o=o, inc=inc: mt.mt_scan_rows(x, o, inc, st)
            for (r, n, d, inc), o in zip(seq, outs)]
     nb = sum(call_bytes(r, n, d) for r, n, d, _ in seq) / len(seq)
-    ms, nl = back_to_back(fns, stream, launches_for(nb))
+    ms, nl = graph_back_to_back(fns, launches_for(nb))
     ks["rows_half_4_calls"] = kernel_entry(
         "k_scan_rows (bf16, f16)", "bf16 and f16 [8192,8192] exclusive then [4096,4099] inclusive, in turn", nb, ms,
-        nl, 1, peak, None, "rows",
+        nl, 1, peak, None, "rows", timing=GRAPH_TIMING,
         note="bytes_per_launch and avg_launch_ms are the means over the four calls")
     del half, outs, fns
     # select: f32 values n = 2^28 uniform[-1,1) (seed 4), u8 flags Bernoulli(p) (seed 5)
